@@ -1,0 +1,542 @@
+// C ABI of libsffn: argument validation, workspace layout and the launch
+// sequence of the predictor-gated sparse FFN (declared in include/sffn.h).
+
+#include <algorithm>
+#include <cstdarg>
+#include <cstdio>
+#include <cstring>
+#include <numeric>
+#include <new>
+#include <string>
+#include <vector>
+
+#include "../../include/sffn.h"
+#include "kernels.cuh"
+
+using namespace sffn;
+
+struct sffn_layer {
+  sffn_layer_desc desc;
+  int device = 0;
+  int sms = 0;
+  size_t smem_optin = 0;
+  int esize = 0;
+  int W = 0;           // mask words per token
+  int kc_elems = 0;    // predictor K-chunk
+  int KS = 0;          // predictor K-chunks
+  int RG = 0;          // predictor row groups
+  int score_grid = 0;  // blocks of the score kernel
+  int gather_grid = 0; // blocks of the gather kernel (one per SM)
+  int max_bt = 0;      // tokens per gather pass
+  GatherConfig gcfg[3];  // tokens per pass 1, 2, 4
+  bool gcfg_ok[3] = {false, false, false};
+};
+
+namespace {
+
+thread_local std::string g_err;
+int64_t g_wait_ns = 1000000000LL;  // 1 s
+cudaEvent_t g_prof_start = nullptr, g_prof_stop = nullptr;  // bracket gather launches when set
+
+constexpr int kVersion = 1;
+
+sffn_status fail(sffn_status st, const char* fmt, ...) {
+  char buf[512];
+  va_list ap;
+  va_start(ap, fmt);
+  vsnprintf(buf, sizeof(buf), fmt, ap);
+  va_end(ap);
+  g_err = buf;
+  return st;
+}
+
+sffn_status cuda_fail(cudaError_t e, const char* where) {
+  return fail(SFFN_ERR_CUDA, "%s: %s", where, cudaGetErrorString(e));
+}
+
+bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+size_t align_up(size_t v, size_t a) { return (v + a - 1) / a * a; }
+
+int bt_slot(int bt) { return bt == 1 ? 0 : bt == 2 ? 1 : 2; }
+
+struct WsLayout {
+  size_t hdr, tickets, h_part, h, mask, y_part, total;
+};
+
+WsLayout layout(const sffn_layer* L, int batch) {
+  const auto& d = L->desc;
+  WsLayout w{};
+  size_t off = 0;
+  auto take = [&](size_t bytes) {
+    const size_t o = off;
+    off = align_up(off + bytes, 256);
+    return o;
+  };
+  w.hdr = take(sizeof(WsHeader));
+  w.tickets = take((size_t)L->RG * batch * sizeof(uint32_t));
+  w.h_part = take((size_t)L->KS * batch * d.rank * sizeof(float));
+  w.h = take((size_t)batch * d.rank * sizeof(float));
+  w.mask = take((size_t)batch * L->W * sizeof(uint32_t));
+  w.y_part = take((size_t)L->gather_grid * std::min(batch, L->max_bt) * d.d_model * sizeof(float));
+  w.total = off;
+  return w;
+}
+
+struct Ws {
+  WsLayout lay;
+  unsigned char* base;
+  WsHeader* hdr() const { return reinterpret_cast<WsHeader*>(base + lay.hdr); }
+  uint32_t* tickets() const { return reinterpret_cast<uint32_t*>(base + lay.tickets); }
+  float* h_part() const { return reinterpret_cast<float*>(base + lay.h_part); }
+  float* h() const { return reinterpret_cast<float*>(base + lay.h); }
+  uint32_t* mask() const { return reinterpret_cast<uint32_t*>(base + lay.mask); }
+  float* y_part() const { return reinterpret_cast<float*>(base + lay.y_part); }
+};
+
+sffn_status check_ws(const sffn_layer* L, int batch, void* ws, size_t bytes, Ws* out) {
+  if (ws == nullptr) return fail(SFFN_ERR_WORKSPACE, "workspace is NULL");
+  if ((reinterpret_cast<uintptr_t>(ws) & 255u) != 0) return fail(SFFN_ERR_WORKSPACE, "workspace not 256-byte aligned");
+  out->lay = layout(L, batch);
+  if (bytes < out->lay.total)
+    return fail(SFFN_ERR_WORKSPACE, "workspace too small: %zu bytes given, %zu needed", bytes, out->lay.total);
+  out->base = static_cast<unsigned char*>(ws);
+  return SFFN_OK;
+}
+
+sffn_status check_batch(const sffn_layer* L, int batch) {
+  if (batch < 1 || batch > L->desc.max_batch)
+    return fail(SFFN_ERR_INVALID_ARG, "batch %d outside [1, max_batch=%d]", batch, L->desc.max_batch);
+  return SFFN_OK;
+}
+
+sffn_status check_dev_ptr(const void* p, const char* name) {
+  if (p == nullptr) return fail(SFFN_ERR_INVALID_ARG, "%s is NULL", name);
+  if (!aligned16(p)) return fail(SFFN_ERR_INVALID_ARG, "%s is not 16-byte aligned", name);
+  return SFFN_OK;
+}
+
+#define SFFN_TRY(expr)                     \
+  do {                                     \
+    sffn_status _st = (expr);              \
+    if (_st != SFFN_OK) return _st;        \
+  } while (0)
+
+#define SFFN_CUDA(expr, where)                          \
+  do {                                                  \
+    cudaError_t _e = (expr);                            \
+    if (_e != cudaSuccess) return cuda_fail(_e, where); \
+  } while (0)
+
+// Predictor for `batch` tokens: h = V x (split-K, deterministic), then the
+// scores and the mask words (and optionally the scores themselves).
+sffn_status run_predictor(const sffn_layer* L, const void* x, int batch, const Ws& ws, float* scores,
+                          cudaStream_t s) {
+  const auto& d = L->desc;
+  PredHiddenArgs ha{d.pred_V, x, batch, d.rank, d.d_model, L->kc_elems, L->KS, ws.h_part(), ws.h(), ws.tickets()};
+  // token groups of up to 8 per launch
+  for (int b0 = 0; b0 < batch; b0 += 8) {
+    const int nb = std::min(8, batch - b0);
+    PredHiddenArgs a = ha;
+    a.x = static_cast<const unsigned char*>(x) + (size_t)b0 * d.d_model * L->esize;
+    a.B = nb;
+    a.h_part = ws.h_part() + (size_t)b0 * L->KS * d.rank;
+    a.h = ws.h() + (size_t)b0 * d.rank;
+    SFFN_CUDA(launch_pred_hidden(d.dtype, a, s), "predictor hidden launch");
+    PredScoreArgs sa{d.pred_U, a.h, d.pred_b, d.tau, nb, d.d_ff, d.rank, L->W,
+                     ws.mask() + (size_t)b0 * L->W,
+                     scores ? scores + (size_t)b0 * d.d_ff : nullptr, L->score_grid};
+    SFFN_CUDA(launch_pred_score(d.dtype, sa, s), "predictor score launch");
+  }
+  return SFFN_OK;
+}
+
+// Timing events must become graph nodes when the stream is being captured.
+sffn_status record_profile_event(cudaEvent_t ev, cudaStream_t s) {
+  cudaStreamCaptureStatus cs = cudaStreamCaptureStatusNone;
+  SFFN_CUDA(cudaStreamIsCapturing(s, &cs), "capture query");
+  const unsigned flags = cs == cudaStreamCaptureStatusActive ? cudaEventRecordExternal : cudaEventRecordDefault;
+  SFFN_CUDA(cudaEventRecordWithFlags(ev, s, flags), "profile event");
+  return SFFN_OK;
+}
+
+// Gather passes of up to max_bt tokens each.
+sffn_status run_gather(const sffn_layer* L, const void* x, int batch, float* y, const Ws& ws, bool dense,
+                       cudaStream_t s) {
+  const auto& d = L->desc;
+  for (int b0 = 0; b0 < batch; b0 += L->max_bt) {
+    const int nb = std::min(L->max_bt, batch - b0);
+    const int bt = nb == 1 ? 1 : nb == 2 ? 2 : 4;
+    if (!L->gcfg_ok[bt_slot(bt)]) return fail(SFFN_ERR_UNSUPPORTED, "no gather configuration for %d tokens", bt);
+    GatherArgs a{};
+    a.x = static_cast<const unsigned char*>(x) + (size_t)b0 * d.d_model * L->esize;
+    a.w_up = d.w_up;
+    a.w_gate = d.w_gate;
+    a.w_downT = d.w_downT;
+    a.b = d.b;
+    a.mask = ws.mask() + (size_t)b0 * L->W;
+    a.y = y + (size_t)b0 * d.d_model;
+    a.y_part = ws.y_part();
+    a.hdr = ws.hdr();
+    a.B = nb;
+    a.d = d.d_model;
+    a.f = d.d_ff;
+    a.W = L->W;
+    a.act = d.act;
+    a.dense = dense ? 1 : 0;
+    a.nstages = L->gcfg[bt_slot(bt)].nstages;
+    a.list_cap = L->gcfg[bt_slot(bt)].list_cap;
+    a.wait_ns = (uint64_t)g_wait_ns;
+    if (g_prof_start != nullptr) SFFN_TRY(record_profile_event(g_prof_start, s));
+    SFFN_CUDA(launch_gather(d.dtype, L->gcfg[bt_slot(bt)], a, L->gather_grid, s), "gather launch");
+    if (g_prof_stop != nullptr) SFFN_TRY(record_profile_event(g_prof_stop, s));
+  }
+  return SFFN_OK;
+}
+
+sffn_status check_x(const sffn_layer* L, const void* x) { return check_dev_ptr(x, "x"); }
+
+}  // namespace
+
+extern "C" {
+
+int32_t sffn_version(void) { return kVersion; }
+
+const char* sffn_last_error(void) { return g_err.c_str(); }
+
+const char* sffn_status_string(sffn_status st) {
+  switch (st) {
+    case SFFN_OK: return "ok";
+    case SFFN_ERR_INVALID_ARG: return "invalid argument";
+    case SFFN_ERR_UNSUPPORTED: return "unsupported";
+    case SFFN_ERR_CUDA: return "CUDA error";
+    case SFFN_ERR_CAPACITY: return "capacity exceeded";
+    case SFFN_ERR_TIMEOUT: return "device wait timed out";
+    case SFFN_ERR_WORKSPACE: return "bad workspace";
+  }
+  return "unknown status";
+}
+
+sffn_status sffn_set_profile_events(void* start_event, void* stop_event) {
+  g_prof_start = static_cast<cudaEvent_t>(start_event);
+  g_prof_stop = static_cast<cudaEvent_t>(stop_event);
+  return SFFN_OK;
+}
+
+sffn_status sffn_set_wait_limit_ns(int64_t ns) {
+  if (ns <= 0) return fail(SFFN_ERR_INVALID_ARG, "wait limit must be positive");
+  g_wait_ns = ns;
+  return SFFN_OK;
+}
+
+sffn_status sffn_create_layer(const sffn_layer_desc* desc, sffn_layer_t* out) {
+  g_err.clear();
+  if (desc == nullptr || out == nullptr) return fail(SFFN_ERR_INVALID_ARG, "desc/out is NULL");
+  *out = nullptr;
+  const sffn_layer_desc& d = *desc;
+  if (d.dtype != SFFN_F32 && d.dtype != SFFN_F16 && d.dtype != SFFN_BF16)
+    return fail(SFFN_ERR_INVALID_ARG, "unknown dtype %d", d.dtype);
+  if (d.act != SFFN_RELU && d.act != SFFN_REGLU) return fail(SFFN_ERR_INVALID_ARG, "unknown act %d", d.act);
+  if (d.d_model <= 0 || d.d_ff <= 0 || d.rank <= 0)
+    return fail(SFFN_ERR_INVALID_ARG, "d_model, d_ff and rank must be positive");
+  if (d.max_batch < 1 || d.max_batch > 32) return fail(SFFN_ERR_INVALID_ARG, "max_batch must be in [1, 32]");
+  const int esize = d.dtype == SFFN_F32 ? 4 : 2;
+  if (((size_t)d.d_model * esize) % 16 != 0)
+    return fail(SFFN_ERR_INVALID_ARG, "d_model * sizeof(dtype) must be a multiple of 16");
+  if (((size_t)d.rank * esize) % 16 != 0)
+    return fail(SFFN_ERR_INVALID_ARG, "rank * sizeof(dtype) must be a multiple of 16");
+  SFFN_TRY(check_dev_ptr(d.w_up, "w_up"));
+  SFFN_TRY(check_dev_ptr(d.w_downT, "w_downT"));
+  SFFN_TRY(check_dev_ptr(d.pred_U, "pred_U"));
+  SFFN_TRY(check_dev_ptr(d.pred_V, "pred_V"));
+  if (d.pred_b == nullptr) return fail(SFFN_ERR_INVALID_ARG, "pred_b is NULL");
+  if (d.act == SFFN_REGLU) {
+    SFFN_TRY(check_dev_ptr(d.w_gate, "w_gate"));
+  } else if (d.w_gate != nullptr) {
+    return fail(SFFN_ERR_INVALID_ARG, "w_gate must be NULL for ReLU layers");
+  }
+  if (d.rank / (16 / esize) > 256) return fail(SFFN_ERR_UNSUPPORTED, "rank too large for the score kernel");
+
+  sffn_layer* L = new (std::nothrow) sffn_layer();
+  if (L == nullptr) return fail(SFFN_ERR_INVALID_ARG, "out of host memory");
+  L->desc = d;
+  L->esize = esize;
+  cudaError_t e = cudaGetDevice(&L->device);
+  int optin = 0;
+  if (e == cudaSuccess) e = cudaDeviceGetAttribute(&L->sms, cudaDevAttrMultiProcessorCount, L->device);
+  if (e == cudaSuccess) e = cudaDeviceGetAttribute(&optin, cudaDevAttrMaxSharedMemoryPerBlockOptin, L->device);
+  if (e != cudaSuccess) {
+    delete L;
+    return cuda_fail(e, "device query");
+  }
+  L->smem_optin = (size_t)optin;
+  L->W = (d.d_ff + 31) / 32;
+
+  // predictor split: about two blocks per SM across (K-chunks x row groups)
+  const int E = 16 / esize;
+  const int unit = 32 * E;  // one warp-wide 16-byte load of a row
+  L->RG = pred_hidden_row_groups(d.rank);
+  const int ks_target = std::max(1, (2 * L->sms + L->RG - 1) / L->RG);
+  int kc = (d.d_model + ks_target - 1) / ks_target;
+  kc = (kc + unit - 1) / unit * unit;
+  const int max_kc = 8192 / esize;  // x chunk of 8 tokens must stay within 64 KB of shared memory
+  kc = std::min(kc, std::max(unit, max_kc / unit * unit));
+  L->kc_elems = kc;
+  L->KS = (d.d_model + kc - 1) / kc;
+  L->score_grid = std::min((d.d_ff + 63) / 64, 8 * L->sms);
+
+  L->gather_grid = L->sms;
+  L->max_bt = gather_max_bt(d.dtype, d.d_model);
+  if (L->max_bt == 0) {
+    delete L;
+    return fail(SFFN_ERR_UNSUPPORTED, "d_model %d too wide for the gather kernel", d.d_model);
+  }
+  for (int bt : {1, 2, 4}) {
+    if (bt > L->max_bt) continue;
+    L->gcfg_ok[bt_slot(bt)] =
+        gather_config(d.dtype, d.act, d.d_model, d.d_ff, bt, L->gather_grid, L->smem_optin, &L->gcfg[bt_slot(bt)]);
+  }
+  if (!L->gcfg_ok[0]) {
+    delete L;
+    return fail(SFFN_ERR_UNSUPPORTED, "rows of d_model %d do not fit two pipeline stages", d.d_model);
+  }
+  while (!L->gcfg_ok[bt_slot(L->max_bt)]) L->max_bt /= 2;
+  *out = L;
+  return SFFN_OK;
+}
+
+sffn_status sffn_destroy_layer(sffn_layer_t layer) {
+  delete layer;
+  return SFFN_OK;
+}
+
+size_t sffn_workspace_size(sffn_layer_t L, int32_t batch) {
+  if (L == nullptr || batch < 1 || batch > L->desc.max_batch) return 0;
+  return layout(L, batch).total;
+}
+
+sffn_status sffn_workspace_init(void* ws, size_t bytes, void* stream) {
+  if (ws == nullptr) return fail(SFFN_ERR_WORKSPACE, "workspace is NULL");
+  SFFN_CUDA(cudaMemsetAsync(ws, 0, bytes, static_cast<cudaStream_t>(stream)), "workspace memset");
+  return SFFN_OK;
+}
+
+sffn_status sffn_predict(sffn_layer_t L, const void* x, int32_t batch, int32_t* idx, int32_t* n_active,
+                         void* workspace, size_t ws_bytes, void* stream) {
+  g_err.clear();
+  if (L == nullptr) return fail(SFFN_ERR_INVALID_ARG, "layer is NULL");
+  SFFN_TRY(check_batch(L, batch));
+  SFFN_TRY(check_x(L, x));
+  if (idx == nullptr || n_active == nullptr) return fail(SFFN_ERR_INVALID_ARG, "idx/n_active is NULL");
+  Ws ws;
+  SFFN_TRY(check_ws(L, batch, workspace, ws_bytes, &ws));
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  SFFN_TRY(run_predictor(L, x, batch, ws, nullptr, s));
+  SFFN_CUDA(launch_compact(ws.mask(), batch, L->desc.d_ff, L->W, idx, n_active, s), "compaction launch");
+  return SFFN_OK;
+}
+
+sffn_status sffn_predict_scores(sffn_layer_t L, const void* x, int32_t batch, float* scores, void* workspace,
+                                size_t ws_bytes, void* stream) {
+  g_err.clear();
+  if (L == nullptr) return fail(SFFN_ERR_INVALID_ARG, "layer is NULL");
+  SFFN_TRY(check_batch(L, batch));
+  SFFN_TRY(check_x(L, x));
+  if (scores == nullptr) return fail(SFFN_ERR_INVALID_ARG, "scores is NULL");
+  Ws ws;
+  SFFN_TRY(check_ws(L, batch, workspace, ws_bytes, &ws));
+  return run_predictor(L, x, batch, ws, scores, static_cast<cudaStream_t>(stream));
+}
+
+sffn_status sffn_forward(sffn_layer_t L, const void* x, int32_t batch, float* y, int32_t* idx_out,
+                         int32_t* n_active_out, void* workspace, size_t ws_bytes, void* stream) {
+  g_err.clear();
+  if (L == nullptr) return fail(SFFN_ERR_INVALID_ARG, "layer is NULL");
+  SFFN_TRY(check_batch(L, batch));
+  SFFN_TRY(check_x(L, x));
+  SFFN_TRY(check_dev_ptr(y, "y"));
+  if ((idx_out == nullptr) != (n_active_out == nullptr))
+    return fail(SFFN_ERR_INVALID_ARG, "idx_out and n_active_out must both be given or both be NULL");
+  Ws ws;
+  SFFN_TRY(check_ws(L, batch, workspace, ws_bytes, &ws));
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  SFFN_TRY(run_predictor(L, x, batch, ws, nullptr, s));
+  if (idx_out != nullptr)
+    SFFN_CUDA(launch_compact(ws.mask(), batch, L->desc.d_ff, L->W, idx_out, n_active_out, s), "compaction launch");
+  return run_gather(L, x, batch, y, ws, false, s);
+}
+
+sffn_status sffn_dense_forward(sffn_layer_t L, const void* x, int32_t batch, float* y, void* workspace,
+                               size_t ws_bytes, void* stream) {
+  g_err.clear();
+  if (L == nullptr) return fail(SFFN_ERR_INVALID_ARG, "layer is NULL");
+  SFFN_TRY(check_batch(L, batch));
+  SFFN_TRY(check_x(L, x));
+  SFFN_TRY(check_dev_ptr(y, "y"));
+  Ws ws;
+  SFFN_TRY(check_ws(L, batch, workspace, ws_bytes, &ws));
+  return run_gather(L, x, batch, y, ws, true, static_cast<cudaStream_t>(stream));
+}
+
+sffn_status sffn_residual_layernorm(const void* x, const float* y, int32_t batch, int32_t d_model, int32_t dtype,
+                                    const float* gamma, const float* beta, float eps, void* x_out, void* stream) {
+  g_err.clear();
+  if (dtype != SFFN_F32 && dtype != SFFN_F16 && dtype != SFFN_BF16)
+    return fail(SFFN_ERR_INVALID_ARG, "unknown dtype %d", dtype);
+  const int esize = dtype == SFFN_F32 ? 4 : 2;
+  if (batch < 1 || d_model <= 0 || ((size_t)d_model * esize) % 16 != 0)
+    return fail(SFFN_ERR_INVALID_ARG, "bad batch/d_model");
+  if (!(eps >= 0.f)) return fail(SFFN_ERR_INVALID_ARG, "eps must be >= 0");
+  SFFN_TRY(check_dev_ptr(x, "x"));
+  SFFN_TRY(check_dev_ptr(y, "y"));
+  SFFN_TRY(check_dev_ptr(x_out, "x_out"));
+  SFFN_CUDA(launch_residual_layernorm(dtype, x, y, batch, d_model, gamma, beta, eps, x_out,
+                                      static_cast<cudaStream_t>(stream)),
+            "layernorm launch");
+  return SFFN_OK;
+}
+
+size_t sffn_stack_workspace_size(const sffn_layer_t* layers, int32_t n_layers, int32_t batch) {
+  if (layers == nullptr || n_layers < 1) return 0;
+  size_t per = 0;
+  for (int l = 0; l < n_layers; ++l) {
+    const size_t w = sffn_workspace_size(layers[l], batch);
+    if (w == 0) return 0;
+    per = std::max(per, w);
+  }
+  const auto& d = layers[0]->desc;
+  const size_t xb = align_up((size_t)batch * d.d_model * layers[0]->esize, 256);
+  const size_t yb = align_up((size_t)batch * d.d_model * sizeof(float), 256);
+  return align_up(per, 256) + 2 * xb + yb;
+}
+
+sffn_status sffn_forward_stack(const sffn_layer_t* layers, int32_t n_layers, const void* x0, int32_t batch,
+                               int32_t n_steps, void* x_out, void* x_trace, const float* ln_gamma,
+                               const float* ln_beta, float ln_eps, void* workspace, size_t ws_bytes,
+                               void* stream) {
+  g_err.clear();
+  if (layers == nullptr || n_layers < 1) return fail(SFFN_ERR_INVALID_ARG, "no layers");
+  if (n_steps < 1) return fail(SFFN_ERR_INVALID_ARG, "n_steps must be >= 1");
+  for (int l = 0; l < n_layers; ++l) {
+    if (layers[l] == nullptr) return fail(SFFN_ERR_INVALID_ARG, "layer %d is NULL", l);
+    SFFN_TRY(check_batch(layers[l], batch));
+    if (layers[l]->desc.d_model != layers[0]->desc.d_model || layers[l]->desc.dtype != layers[0]->desc.dtype)
+      return fail(SFFN_ERR_INVALID_ARG, "layer %d differs in d_model or dtype", l);
+  }
+  SFFN_TRY(check_dev_ptr(x0, "x0"));
+  SFFN_TRY(check_dev_ptr(x_out, "x_out"));
+  if (x_trace != nullptr) SFFN_TRY(check_dev_ptr(x_trace, "x_trace"));
+  if (!(ln_eps >= 0.f)) return fail(SFFN_ERR_INVALID_ARG, "ln_eps must be >= 0");
+  const size_t need = sffn_stack_workspace_size(layers, n_layers, batch);
+  if (workspace == nullptr || ws_bytes < need || (reinterpret_cast<uintptr_t>(workspace) & 255u))
+    return fail(SFFN_ERR_WORKSPACE, "stack workspace: %zu bytes needed (256-byte aligned)", need);
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  const auto& d0 = layers[0]->desc;
+  const int esize = layers[0]->esize;
+  size_t per = 0;
+  for (int l = 0; l < n_layers; ++l) per = std::max(per, sffn_workspace_size(layers[l], batch));
+  per = align_up(per, 256);
+  unsigned char* base = static_cast<unsigned char*>(workspace);
+  const size_t xbytes = (size_t)batch * d0.d_model * esize;
+  const size_t xb = align_up(xbytes, 256);
+  unsigned char* xbuf[2] = {base + per, base + per + xb};
+  float* ybuf = reinterpret_cast<float*>(base + per + 2 * xb);
+  unsigned char* trace = static_cast<unsigned char*>(x_trace);
+  unsigned char* xo = static_cast<unsigned char*>(x_out);
+
+  const void* xin = x0;
+  for (int t = 0; t < n_steps; ++t) {
+    for (int l = 0; l < n_layers; ++l) {
+      const sffn_layer* L = layers[l];
+      if (trace != nullptr)
+        SFFN_CUDA(cudaMemcpyAsync(trace + ((size_t)t * n_layers + l) * xbytes, xin, xbytes,
+                                  cudaMemcpyDeviceToDevice, s),
+                  "trace copy");
+      Ws ws;
+      SFFN_TRY(check_ws(L, batch, workspace, per, &ws));
+      SFFN_TRY(run_predictor(L, xin, batch, ws, nullptr, s));
+      SFFN_TRY(run_gather(L, xin, batch, ybuf, ws, false, s));
+      void* xnext = (l == n_layers - 1) ? static_cast<void*>(xo + (size_t)t * xbytes) : xbuf[l & 1];
+      SFFN_CUDA(launch_residual_layernorm(d0.dtype, xin, ybuf, batch, d0.d_model, ln_gamma, ln_beta, ln_eps,
+                                          xnext, s),
+                "layernorm launch");
+      xin = xnext;
+    }
+  }
+  return SFFN_OK;
+}
+
+sffn_status sffn_profile_counts(sffn_layer_t L, const void* X, int32_t n_tokens, int32_t* counts, void* workspace,
+                                size_t ws_bytes, void* stream) {
+  g_err.clear();
+  if (L == nullptr) return fail(SFFN_ERR_INVALID_ARG, "layer is NULL");
+  if (n_tokens < 1) return fail(SFFN_ERR_INVALID_ARG, "n_tokens must be >= 1");
+  SFFN_TRY(check_dev_ptr(X, "X"));
+  if (counts == nullptr) return fail(SFFN_ERR_INVALID_ARG, "counts is NULL");
+  const int chunk = std::min(L->desc.max_batch, 8);
+  Ws ws;
+  SFFN_TRY(check_ws(L, chunk, workspace, ws_bytes, &ws));
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  SFFN_CUDA(cudaMemsetAsync(counts, 0, (size_t)L->desc.d_ff * sizeof(int32_t), s), "counts memset");
+  const unsigned char* xb = static_cast<const unsigned char*>(X);
+  for (int t0 = 0; t0 < n_tokens; t0 += chunk) {
+    const int nb = std::min(chunk, n_tokens - t0);
+    SFFN_TRY(run_predictor(L, xb + (size_t)t0 * L->desc.d_model * L->esize, nb, ws, nullptr, s));
+    SFFN_CUDA(launch_count_bits(ws.mask(), nb, L->desc.d_ff, L->W, counts, s), "count launch");
+  }
+  return SFFN_OK;
+}
+
+sffn_status sffn_hot_first_perm(const int32_t* counts, int32_t d_ff, int32_t* perm) {
+  g_err.clear();
+  if (counts == nullptr || perm == nullptr || d_ff < 1) return fail(SFFN_ERR_INVALID_ARG, "bad arguments");
+  std::vector<int32_t> order(d_ff);
+  std::iota(order.begin(), order.end(), 0);
+  std::stable_sort(order.begin(), order.end(), [&](int32_t a, int32_t b) { return counts[a] > counts[b]; });
+  std::copy(order.begin(), order.end(), perm);
+  return SFFN_OK;
+}
+
+sffn_status sffn_permute_rows(const void* src, void* dst, const int32_t* perm, int32_t rows, int64_t row_bytes,
+                              void* stream) {
+  g_err.clear();
+  if (src == nullptr || dst == nullptr || (reinterpret_cast<uintptr_t>(src) & 3) || (reinterpret_cast<uintptr_t>(dst) & 3))
+    return fail(SFFN_ERR_INVALID_ARG, "src/dst NULL or not 4-byte aligned");
+  if (perm == nullptr || rows < 1 || row_bytes <= 0 || row_bytes % 4 != 0)
+    return fail(SFFN_ERR_INVALID_ARG, "bad perm/rows/row_bytes (row_bytes must be a multiple of 4)");
+  if (src == dst) return fail(SFFN_ERR_INVALID_ARG, "permute_rows is out of place");
+  SFFN_CUDA(launch_permute_rows(src, dst, perm, rows, row_bytes, static_cast<cudaStream_t>(stream)),
+            "permute launch");
+  return SFFN_OK;
+}
+
+sffn_status sffn_read_device_status(void* workspace, int32_t* status, void* stream) {
+  g_err.clear();
+  if (workspace == nullptr || status == nullptr) return fail(SFFN_ERR_INVALID_ARG, "NULL argument");
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  WsHeader h;
+  SFFN_CUDA(cudaMemcpyAsync(&h, workspace, sizeof(h), cudaMemcpyDeviceToHost, s), "status read");
+  SFFN_CUDA(cudaStreamSynchronize(s), "status sync");
+  *status = (int32_t)h.status;
+  if (h.status != 0) {
+    // clear the status; after a timeout the barrier words may be mid-generation
+    WsHeader z;
+    std::memset(&z, 0, sizeof(z));
+    z.bar_gen = h.bar_gen;
+    SFFN_CUDA(cudaMemcpyAsync(workspace, &z, sizeof(z), cudaMemcpyHostToDevice, s), "status clear");
+    SFFN_CUDA(cudaStreamSynchronize(s), "status clear sync");
+  }
+  return SFFN_OK;
+}
+
+sffn_status sffn_debug_wait_timeout(void* workspace, size_t ws_bytes, int64_t timeout_ns, void* stream) {
+  g_err.clear();
+  if (workspace == nullptr || ws_bytes < sizeof(WsHeader)) return fail(SFFN_ERR_WORKSPACE, "workspace too small");
+  if (timeout_ns <= 0 || timeout_ns > 10000000000LL) return fail(SFFN_ERR_INVALID_ARG, "timeout out of range");
+  SFFN_CUDA(launch_wait_timeout(static_cast<WsHeader*>(workspace), (uint64_t)timeout_ns,
+                                static_cast<cudaStream_t>(stream)),
+            "wait launch");
+  return SFFN_OK;
+}
+
+}  // extern "C"

@@ -1,0 +1,204 @@
+// Device helpers shared by the sparse-FFN kernels (sm_103a).
+#pragma once
+
+#include <cuda_bf16.h>
+#include <cuda_fp16.h>
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+namespace sffn {
+
+// Device status codes (values of sffn_status).
+enum : uint32_t { kStOk = 0, kStCapacity = 4, kStTimeout = 5 };
+
+// Header at offset 0 of every workspace (256 bytes).
+struct WsHeader {
+  uint32_t status;     // first device-side error (sticky until read)
+  uint32_t detail;     // where it happened (kernel-specific code)
+  uint32_t bar_count;  // grid barrier: arrivals in the current generation
+  uint32_t bar_gen;    // grid barrier: generation counter
+  uint32_t pad[60];
+};
+static_assert(sizeof(WsHeader) == 256, "workspace header is 256 bytes");
+
+enum DType : int { kF32 = 0, kF16 = 1, kBF16 = 2 };
+enum Act : int { kRelu = 0, kReglu = 1 };
+
+// ---------------------------------------------------------------- dtype chunks
+// Every row is processed in 16-byte chunks: 4 fp32 or 8 fp16/bf16 values.
+template <typename T> struct Chunk;
+template <> struct Chunk<float> { static constexpr int N = 4; };
+template <> struct Chunk<__half> { static constexpr int N = 8; };
+template <> struct Chunk<__nv_bfloat16> { static constexpr int N = 8; };
+
+__device__ __forceinline__ float bf16lo(uint32_t w) { return __uint_as_float(w << 16); }
+__device__ __forceinline__ float bf16hi(uint32_t w) { return __uint_as_float(w & 0xffff0000u); }
+
+template <typename T>
+__device__ __forceinline__ void unpack(const uint4& u, float* o);
+
+template <>
+__device__ __forceinline__ void unpack<float>(const uint4& u, float* o) {
+  o[0] = __uint_as_float(u.x); o[1] = __uint_as_float(u.y);
+  o[2] = __uint_as_float(u.z); o[3] = __uint_as_float(u.w);
+}
+template <>
+__device__ __forceinline__ void unpack<__half>(const uint4& u, float* o) {
+  const uint32_t w[4] = {u.x, u.y, u.z, u.w};
+#pragma unroll
+  for (int i = 0; i < 4; ++i) {
+    __half2 h = *reinterpret_cast<const __half2*>(&w[i]);
+    float2 f = __half22float2(h);
+    o[2 * i] = f.x; o[2 * i + 1] = f.y;
+  }
+}
+template <>
+__device__ __forceinline__ void unpack<__nv_bfloat16>(const uint4& u, float* o) {
+  const uint32_t w[4] = {u.x, u.y, u.z, u.w};
+#pragma unroll
+  for (int i = 0; i < 4; ++i) { o[2 * i] = bf16lo(w[i]); o[2 * i + 1] = bf16hi(w[i]); }
+}
+
+template <typename T> __device__ __forceinline__ T from_float(float v);
+template <> __device__ __forceinline__ float from_float<float>(float v) { return v; }
+template <> __device__ __forceinline__ __half from_float<__half>(float v) { return __float2half_rn(v); }
+template <> __device__ __forceinline__ __nv_bfloat16 from_float<__nv_bfloat16>(float v) {
+  return __float2bfloat16_rn(v);
+}
+
+// 16-byte global load through the read-only path, not kept in L1.
+__device__ __forceinline__ uint4 ldg_stream(const void* p) {
+  uint4 r;
+  asm volatile("ld.global.nc.L1::no_allocate.v4.u32 {%0,%1,%2,%3}, [%4];"
+               : "=r"(r.x), "=r"(r.y), "=r"(r.z), "=r"(r.w) : "l"(p));
+  return r;
+}
+
+__device__ __forceinline__ float warp_sum(float v) {
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
+  return v;
+}
+
+// ---------------------------------------------------------------- timing / status
+__device__ __forceinline__ uint64_t globaltimer_ns() {
+  uint64_t t;
+  asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
+  return t;
+}
+
+// Records the first device-side error; later ones are dropped.
+__device__ __forceinline__ void set_status(WsHeader* h, uint32_t code, uint32_t detail) {
+  if (atomicCAS(&h->status, 0u, code) == 0u) atomicExch(&h->detail, detail);
+}
+
+__device__ __forceinline__ uint32_t ld_acquire_gpu(const uint32_t* p) {
+  uint32_t v;
+  asm volatile("ld.acquire.gpu.global.u32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
+  return v;
+}
+__device__ __forceinline__ void st_release_gpu(uint32_t* p, uint32_t v) {
+  asm volatile("st.release.gpu.global.u32 [%0], %1;" ::"l"(p), "r"(v) : "memory");
+}
+
+// Grid-wide barrier over `expected` resident blocks (sense reversal through a
+// generation word, so it needs no reset between uses).  Every wait is bounded:
+// after limit_ns the block records kStTimeout and returns false instead of
+// spinning on.  All threads of the block must call it.
+__device__ __forceinline__ bool grid_barrier(WsHeader* h, uint32_t expected, uint64_t limit_ns,
+                                             uint32_t detail) {
+  __shared__ int s_ok;
+  __syncthreads();
+  if (threadIdx.x == 0) {
+    int ok = 1;
+    const uint32_t gen = ld_acquire_gpu(&h->bar_gen);  // read before arriving
+    __threadfence();                                     // publish this block's writes
+    const uint32_t old = atomicAdd(&h->bar_count, 1u);
+    if (old == expected - 1) {
+      atomicExch(&h->bar_count, 0u);
+      __threadfence();
+      st_release_gpu(&h->bar_gen, gen + 1u);
+    } else {
+      const uint64_t t0 = globaltimer_ns();
+      while (ld_acquire_gpu(&h->bar_gen) == gen) {
+        __nanosleep(32);
+        if (globaltimer_ns() - t0 > limit_ns) {
+          set_status(h, kStTimeout, detail);
+          ok = 0;
+          break;
+        }
+      }
+    }
+    __threadfence();
+    s_ok = ok;
+  }
+  __syncthreads();
+  return s_ok != 0;
+}
+
+// ---------------------------------------------------------------- mbarrier + bulk copy
+__device__ __forceinline__ uint32_t smem_addr(const void* p) {
+  return static_cast<uint32_t>(__cvta_generic_to_shared(p));
+}
+
+__device__ __forceinline__ void mbar_init(uint64_t* bar, uint32_t count) {
+  asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(smem_addr(bar)), "r"(count) : "memory");
+}
+
+// Makes initialised mbarriers visible to the async (bulk-copy) proxy.
+__device__ __forceinline__ void fence_mbar_init() {
+  asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+}
+
+__device__ __forceinline__ void mbar_arrive_expect_tx(uint64_t* bar, uint32_t bytes) {
+  asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(smem_addr(bar)), "r"(bytes)
+               : "memory");
+}
+
+__device__ __forceinline__ bool mbar_try_wait(uint64_t* bar, uint32_t parity) {
+  uint32_t done;
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
+      "selp.u32 %0, 1, 0, p;\n\t}"
+      : "=r"(done) : "r"(smem_addr(bar)), "r"(parity) : "memory");
+  return done != 0;
+}
+
+// Bounded wait on an mbarrier phase; false (and kStTimeout) if it never completes.
+__device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, WsHeader* h,
+                                          uint64_t limit_ns, uint32_t detail) {
+  if (mbar_try_wait(bar, parity)) return true;
+  const uint64_t t0 = globaltimer_ns();
+  while (!mbar_try_wait(bar, parity)) {
+    if (globaltimer_ns() - t0 > limit_ns) {
+      set_status(h, kStTimeout, detail);
+      return false;
+    }
+  }
+  return true;
+}
+
+// Bulk (non-tensor) async copy global -> this CTA's shared memory, completing
+// on `bar` with a byte count.  dst, src and bytes must be 16-byte aligned.
+__device__ __forceinline__ void bulk_g2s(void* dst, const void* src, uint32_t bytes, uint64_t* bar,
+                                         uint64_t policy) {
+  asm volatile(
+      "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes.L2::cache_hint "
+      "[%0], [%1], %2, [%3], %4;" ::"r"(smem_addr(dst)),
+      "l"(src), "r"(bytes), "r"(smem_addr(bar)), "l"(policy)
+      : "memory");
+}
+
+__device__ __forceinline__ uint64_t policy_evict_first() {
+  uint64_t p;
+  asm volatile("createpolicy.fractional.L2::evict_first.b64 %0, 1.0;" : "=l"(p));
+  return p;
+}
+__device__ __forceinline__ uint64_t policy_evict_normal() {
+  uint64_t p;
+  asm volatile("createpolicy.fractional.L2::evict_normal.b64 %0, 1.0;" : "=l"(p));
+  return p;
+}
+
+}  // namespace sffn

@@ -1,0 +1,86 @@
+// Launchers of the sparse-FFN kernels (host side, used by the C ABI).
+#pragma once
+
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+#include "common.cuh"
+
+namespace sffn {
+
+// ---- predictor hidden layer: h[b][k] = sum_j V[k][j] x[b][j]
+struct PredHiddenArgs {
+  const void* V;       // [r][d]
+  const void* x;       // [B][d]
+  int B, r, d;
+  int kc_elems;        // elements of d per K-chunk (multiple of 32 chunks' worth)
+  int KS;              // number of K-chunks
+  float* h_part;       // [KS][B][r] partial sums (workspace)
+  float* h;            // [B][r] final (workspace)
+  uint32_t* tickets;   // [row groups][token groups] arrival counters (zeroed)
+};
+int pred_hidden_row_groups(int r);
+cudaError_t launch_pred_hidden(int dtype, const PredHiddenArgs& a, cudaStream_t s);
+
+// ---- predictor scores + threshold: mask[b][w] bit j  <=>  U[32w+j].h[b] + pb > tau
+struct PredScoreArgs {
+  const void* U;       // [f][r]
+  const float* h;      // [B][r]
+  const float* pb;     // [f]
+  float tau;
+  int B, f, r, W;      // W = ceil(f / 32) mask words per token
+  uint32_t* mask;      // [B][W]
+  float* scores;       // NULL or [B][f]
+  int grid;            // blocks (grid-stride over 64-row blocks)
+};
+cudaError_t launch_pred_score(int dtype, const PredScoreArgs& a, cudaStream_t s);
+
+// ---- compaction: ascending active-index list per token
+cudaError_t launch_compact(const uint32_t* mask, int B, int f, int W, int32_t* idx, int32_t* n_active,
+                           cudaStream_t s);
+
+// ---- counts[i] += number of tokens with bit i set
+cudaError_t launch_count_bits(const uint32_t* mask, int B, int f, int W, int32_t* counts, cudaStream_t s);
+
+// ---- fused row-gather FFN (CUDA cores, up to 4 tokens per pass)
+struct GatherArgs {
+  const void* x;        // [B][d] tokens of this pass
+  const void* w_up;
+  const void* w_gate;   // ReGLU only
+  const void* w_downT;
+  const float* b;       // NULL or [f]
+  const uint32_t* mask; // [B][W] predicted bits of this pass (ignored when dense)
+  float* y;             // [B][d]
+  float* y_part;        // [grid][B][d] per-block partial outputs (workspace)
+  WsHeader* hdr;
+  int B, d, f, W;
+  int act;              // Act
+  int dense;            // 1: every neuron (no predictor)
+  int nstages;          // pipeline depth (>= 2)
+  int list_cap;         // per-block capacity of the local neuron list
+  uint64_t wait_ns;
+};
+struct GatherConfig {
+  int threads, cpt, bt, nstages, list_cap;
+  size_t smem;
+};
+// Largest tokens-per-pass the register budget allows for this row width.
+int gather_max_bt(int dtype, int d);
+bool gather_config(int dtype, int act, int d, int f, int bt, int grid, size_t smem_optin,
+                   GatherConfig* cfg);
+cudaError_t launch_gather(int dtype, const GatherConfig& cfg, const GatherArgs& a, int grid,
+                          cudaStream_t s);
+
+// ---- residual + LayerNorm: x_out = round(LN(x + y) * gamma + beta)
+cudaError_t launch_residual_layernorm(int dtype, const void* x, const float* y, int B, int d,
+                                      const float* gamma, const float* beta, float eps, void* x_out,
+                                      cudaStream_t s);
+
+// ---- dst[i] = src[perm[i]] rows
+cudaError_t launch_permute_rows(const void* src, void* dst, const int32_t* perm, int rows,
+                                int64_t row_bytes, cudaStream_t s);
+
+// ---- test hook: a barrier wait that cannot complete
+cudaError_t launch_wait_timeout(WsHeader* hdr, uint64_t limit_ns, cudaStream_t s);
+
+}  // namespace sffn

@@ -1,0 +1,189 @@
+// Small kernels around the sparse FFN: residual + LayerNorm between stacked
+// layers, row permutation for the hot-first neuron order, the bounded-wait
+// test hook, and the launch configuration of the gather kernel.
+
+#include <algorithm>
+
+#include "kernels.cuh"
+
+namespace sffn {
+
+cudaError_t launch_gather_f32(const GatherConfig&, const GatherArgs&, int, cudaStream_t);
+cudaError_t launch_gather_f16(const GatherConfig&, const GatherArgs&, int, cudaStream_t);
+cudaError_t launch_gather_bf16(const GatherConfig&, const GatherArgs&, int, cudaStream_t);
+
+namespace {
+
+constexpr int kLnThreads = 256;
+
+__device__ float block_sum(float v, float* s_warp) {
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  v = warp_sum(v);
+  __syncthreads();
+  if (lane == 0) s_warp[warp] = v;
+  __syncthreads();
+  float t = 0.f;
+  for (int w = 0; w < (int)(blockDim.x >> 5); ++w) t += s_warp[w];  // fixed order
+  return t;
+}
+
+// One block per token.  v = x + y in fp32; mean and biased variance by two
+// passes; out = (v - mean) / sqrt(var + eps) * gamma + beta, rounded to T.
+template <typename T>
+__global__ void __launch_bounds__(kLnThreads)
+    k_residual_ln(const T* __restrict__ x, const float* __restrict__ y, int d, const float* __restrict__ gamma,
+                  const float* __restrict__ beta, float eps, T* out) {
+  constexpr int E = Chunk<T>::N;
+  __shared__ float s_warp[kLnThreads / 32];
+  const T* xb = x + (size_t)blockIdx.x * d;
+  const float* yb = y + (size_t)blockIdx.x * d;
+  T* ob = out + (size_t)blockIdx.x * d;
+  const int nch = d / E;
+  auto load = [&](int ch, float* v) {
+    unpack<T>(*reinterpret_cast<const uint4*>(xb + ch * E), v);
+    const float4* yp = reinterpret_cast<const float4*>(yb + ch * E);
+#pragma unroll
+    for (int e = 0; e < E; e += 4) {
+      const float4 q = yp[e / 4];
+      v[e] += q.x; v[e + 1] += q.y; v[e + 2] += q.z; v[e + 3] += q.w;
+    }
+  };
+  float s = 0.f;
+  for (int ch = threadIdx.x; ch < nch; ch += blockDim.x) {
+    float v[E];
+    load(ch, v);
+#pragma unroll
+    for (int e = 0; e < E; ++e) s += v[e];
+  }
+  const float mean = block_sum(s, s_warp) / (float)d;
+  float q = 0.f;
+  for (int ch = threadIdx.x; ch < nch; ch += blockDim.x) {
+    float v[E];
+    load(ch, v);
+#pragma unroll
+    for (int e = 0; e < E; ++e) q = fmaf(v[e] - mean, v[e] - mean, q);
+  }
+  const float var = block_sum(q, s_warp) / (float)d;
+  const float rstd = 1.0f / sqrtf(var + eps);
+  __syncthreads();  // every thread has read x before any (possibly in-place) write
+  for (int ch = threadIdx.x; ch < nch; ch += blockDim.x) {
+    float v[E];
+    load(ch, v);
+    T o[E];
+#pragma unroll
+    for (int e = 0; e < E; ++e) {
+      float r = (v[e] - mean) * rstd;
+      if (gamma != nullptr) r *= gamma[ch * E + e];
+      if (beta != nullptr) r += beta[ch * E + e];
+      o[e] = from_float<T>(r);
+    }
+    *reinterpret_cast<uint4*>(ob + ch * E) = *reinterpret_cast<const uint4*>(o);
+  }
+}
+
+template <typename V>
+__global__ void k_permute_rows(const V* __restrict__ src, V* __restrict__ dst, const int32_t* __restrict__ perm,
+                               int rows, int64_t row_vec) {
+  for (int i = blockIdx.x; i < rows; i += gridDim.x) {
+    const int32_t from = perm[i];
+    if (from < 0 || from >= rows) continue;  // not a permutation entry: leave the row alone
+    const V* s = src + (int64_t)from * row_vec;
+    V* o = dst + (int64_t)i * row_vec;
+    for (int64_t k = threadIdx.x; k < row_vec; k += blockDim.x) o[k] = s[k];
+  }
+}
+
+// Waits at the grid barrier for one more block than the grid has: the arrival
+// never comes, so the wait must end by its limit with kStTimeout recorded.
+__global__ void k_wait_timeout(WsHeader* hdr, uint64_t limit_ns) {
+  grid_barrier(hdr, gridDim.x + 1u, limit_ns, 0x900u);
+}
+
+template <typename T>
+cudaError_t ln_launch(const void* x, const float* y, int B, int d, const float* gamma, const float* beta,
+                      float eps, void* out, cudaStream_t s) {
+  k_residual_ln<T><<<B, kLnThreads, 0, s>>>(static_cast<const T*>(x), y, d, gamma, beta, eps,
+                                            static_cast<T*>(out));
+  return cudaGetLastError();
+}
+
+int round_cpt(int cpt) {
+  if (cpt <= 4) return std::max(cpt, 1);
+  if (cpt <= 6) return 6;
+  return 0;
+}
+
+}  // namespace
+
+cudaError_t launch_residual_layernorm(int dtype, const void* x, const float* y, int B, int d,
+                                      const float* gamma, const float* beta, float eps, void* x_out,
+                                      cudaStream_t s) {
+  switch (dtype) {
+    case kF32: return ln_launch<float>(x, y, B, d, gamma, beta, eps, x_out, s);
+    case kF16: return ln_launch<__half>(x, y, B, d, gamma, beta, eps, x_out, s);
+    case kBF16: return ln_launch<__nv_bfloat16>(x, y, B, d, gamma, beta, eps, x_out, s);
+  }
+  return cudaErrorInvalidValue;
+}
+
+cudaError_t launch_permute_rows(const void* src, void* dst, const int32_t* perm, int rows, int64_t row_bytes,
+                                cudaStream_t s) {
+  const int grid = std::min(rows, 65535);
+  const bool vec16 = row_bytes % 16 == 0 && (reinterpret_cast<uintptr_t>(src) & 15) == 0 &&
+                     (reinterpret_cast<uintptr_t>(dst) & 15) == 0;
+  if (vec16)
+    k_permute_rows<uint4><<<grid, 256, 0, s>>>(static_cast<const uint4*>(src), static_cast<uint4*>(dst), perm, rows,
+                                               row_bytes / 16);
+  else
+    k_permute_rows<uint32_t><<<grid, 256, 0, s>>>(static_cast<const uint32_t*>(src), static_cast<uint32_t*>(dst),
+                                                  perm, rows, row_bytes / 4);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_wait_timeout(WsHeader* hdr, uint64_t limit_ns, cudaStream_t s) {
+  k_wait_timeout<<<1, 32, 0, s>>>(hdr, limit_ns);
+  return cudaGetLastError();
+}
+
+int gather_max_bt(int dtype, int d) {
+  const int E = dtype == kF32 ? 4 : 8;
+  const int cpt = round_cpt((d / E + 255) / 256);
+  if (cpt == 0) return 0;
+  for (int bt : {4, 2, 1})
+    if (bt * cpt * E <= 64) return bt;
+  return 0;
+}
+
+bool gather_config(int dtype, int act, int d, int f, int bt, int grid, size_t smem_optin, GatherConfig* cfg) {
+  const int esize = dtype == kF32 ? 4 : 2;
+  const int E = 16 / esize;
+  const int cpt = round_cpt((d / E + 255) / 256);
+  if (cpt == 0 || bt * cpt * E > 64) return false;
+  const size_t row_bytes = (size_t)d * esize;
+  const size_t stage = (act == kReglu ? 3 : 2) * row_bytes;
+  const int list_cap = (f + grid - 1) / grid + 1;
+  const size_t list_bytes = ((size_t)list_cap * 5 + 15) / 16 * 16;
+  const size_t static_smem = 8 * 1024;  // reduction scratch and scan words
+  if (smem_optin < static_smem + list_bytes) return false;
+  const size_t budget = smem_optin - static_smem - list_bytes;
+  const size_t s = std::min<size_t>(16, budget / (stage + 8));
+  if (s < 2) return false;
+  cfg->threads = 256;
+  cfg->cpt = cpt;
+  cfg->bt = bt;
+  cfg->nstages = (int)s;
+  cfg->list_cap = list_cap;
+  cfg->smem = s * stage + s * 8 + list_bytes;
+  return true;
+}
+
+cudaError_t launch_gather(int dtype, const GatherConfig& cfg, const GatherArgs& a, int grid, cudaStream_t s) {
+  switch (dtype) {
+    case kF32: return launch_gather_f32(cfg, a, grid, s);
+    case kF16: return launch_gather_f16(cfg, a, grid, s);
+    case kBF16: return launch_gather_bf16(cfg, a, grid, s);
+  }
+  return cudaErrorInvalidValue;
+}
+
+}  // namespace sffn

@@ -1,0 +1,348 @@
+// Online activation predictor: h = V x, s = U h + pb, mask = s > tau, and the
+// compaction of the mask into ascending neuron-index lists.
+//
+// The pages describe the predictor only in prose (PowerInfer page,
+// "Predictores de espacialidad adaptativa": a small per-layer predictor kept on
+// the GPU scores the neurons and only those predicted active are computed).
+// Here it is the rank-r linear scorer; both GEMVs are HBM-bound reads of V and
+// U and are laid out for full-width 16-byte coalesced loads.
+
+#include "kernels.cuh"
+
+namespace sffn {
+
+namespace {
+
+constexpr int kHiddenWarps = 8;
+constexpr int kHiddenRowsPerWarp = 2;
+constexpr int kHiddenRowsPerBlock = kHiddenWarps * kHiddenRowsPerWarp;
+
+// Grid (KS, row groups, token groups).  Each block stages its K-chunk of the
+// BT tokens in shared memory; each warp streams two rows of V over the chunk.
+// Partial sums go to h_part; the last block of a (row group, token group) to
+// arrive sums the KS partials in a fixed order, so h is deterministic.
+template <typename T, int BT>
+__global__ void __launch_bounds__(kHiddenWarps * 32)
+    k_pred_hidden(const T* __restrict__ V, const T* __restrict__ x, int B, int r, int d, int kc_elems,
+                  int KS, float* __restrict__ h_part, float* __restrict__ h, uint32_t* __restrict__ tickets) {
+  constexpr int E = Chunk<T>::N;
+  extern __shared__ uint4 xs[];  // [BT][kc_elems / E]
+  __shared__ uint32_t s_last;
+  const int ks = blockIdx.x, rg = blockIdx.y, tg = blockIdx.z;
+  const int b0 = tg * BT;
+  const int k0 = ks * kc_elems;
+  const int nch = min(kc_elems, d - k0) / E;
+  const int cstride = kc_elems / E;
+
+  for (int i = threadIdx.x; i < BT * nch; i += blockDim.x) {
+    const int bb = i / nch, c = i - bb * nch;
+    uint4 v = make_uint4(0, 0, 0, 0);
+    if (b0 + bb < B) v = *reinterpret_cast<const uint4*>(x + (size_t)(b0 + bb) * d + k0 + c * E);
+    xs[bb * cstride + c] = v;
+  }
+  __syncthreads();
+
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int row0 = rg * kHiddenRowsPerBlock + warp * kHiddenRowsPerWarp;
+  float acc[kHiddenRowsPerWarp][BT];
+#pragma unroll
+  for (int q = 0; q < kHiddenRowsPerWarp; ++q)
+#pragma unroll
+    for (int bb = 0; bb < BT; ++bb) acc[q][bb] = 0.f;
+
+#pragma unroll 4
+  for (int c = lane; c < nch; c += 32) {
+    uint4 raw[kHiddenRowsPerWarp];
+#pragma unroll
+    for (int q = 0; q < kHiddenRowsPerWarp; ++q) {
+      const int row = row0 + q;
+      raw[q] = row < r ? ldg_stream(V + (size_t)row * d + k0 + c * E) : make_uint4(0, 0, 0, 0);
+    }
+#pragma unroll
+    for (int bb = 0; bb < BT; ++bb) {
+      float xv[E];
+      unpack<T>(xs[bb * cstride + c], xv);
+#pragma unroll
+      for (int q = 0; q < kHiddenRowsPerWarp; ++q) {
+        float w[E];
+        unpack<T>(raw[q], w);
+#pragma unroll
+        for (int e = 0; e < E; ++e) acc[q][bb] = fmaf(w[e], xv[e], acc[q][bb]);
+      }
+    }
+  }
+#pragma unroll
+  for (int q = 0; q < kHiddenRowsPerWarp; ++q) {
+#pragma unroll
+    for (int bb = 0; bb < BT; ++bb) {
+      const float v = warp_sum(acc[q][bb]);
+      const int row = row0 + q;
+      if (lane == 0 && row < r && b0 + bb < B) h_part[((size_t)ks * B + b0 + bb) * r + row] = v;
+    }
+  }
+
+  // Last arriving K-chunk block of this (row group, token group) reduces.
+  __syncthreads();
+  if (threadIdx.x == 0) {
+    __threadfence();
+    uint32_t* t = &tickets[rg * gridDim.z + tg];
+    const uint32_t prev = atomicAdd(t, 1u);
+    s_last = (prev == (uint32_t)KS - 1u);
+    if (s_last) {
+      atomicExch(t, 0u);
+      __threadfence();
+    }
+  }
+  __syncthreads();
+  if (!s_last) return;
+  for (int i = threadIdx.x; i < kHiddenRowsPerBlock * BT; i += blockDim.x) {
+    const int q = i / BT, bb = i - q * BT;
+    const int row = rg * kHiddenRowsPerBlock + q;
+    if (row >= r || b0 + bb >= B) continue;
+    float s = 0.f;
+    for (int k = 0; k < KS; ++k) s += __ldcg(&h_part[((size_t)k * B + b0 + bb) * r + row]);
+    h[(size_t)(b0 + bb) * r + row] = s;
+  }
+}
+
+// Scores.  A block owns 64-row blocks (two mask words) in a grid-stride loop;
+// each warp streams 8 rows of U, lane l holding the 16-byte chunks l, l+32, ...
+// of every row (CPL chunks), and rows are summed with a warp all-reduce.
+constexpr int kScoreWarps = 8;
+constexpr int kScoreRowsPerWarp = 8;
+constexpr int kScoreRowsPerBlock = kScoreWarps * kScoreRowsPerWarp;  // 64 = 2 words
+
+template <typename T, int CPL, int BT>
+__global__ void __launch_bounds__(kScoreWarps * 32)
+    k_pred_score(const T* __restrict__ U, const float* __restrict__ h, const float* __restrict__ pb,
+                 float tau, int B, int f, int r, int W, uint32_t* __restrict__ mask,
+                 float* __restrict__ scores) {
+  constexpr int E = Chunk<T>::N;
+  constexpr int RIF = (8 / CPL) > 0 ? (8 / CPL) : 1;  // rows in flight per warp
+  extern __shared__ float hs[];                        // [BT][r]
+  __shared__ uint32_t s_words[BT][2];
+  const int b0 = blockIdx.y * BT;
+  const int nb = min(BT, B - b0);
+  const int NC = r / E;  // chunks per row
+
+  for (int i = threadIdx.x; i < BT * r; i += blockDim.x) {
+    const int bb = i / r;
+    hs[i] = bb < nb ? h[(size_t)(b0 + bb) * r + (i - bb * r)] : 0.f;
+  }
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+
+  for (int blk = blockIdx.x; blk * kScoreRowsPerBlock < f; blk += gridDim.x) {
+    if (threadIdx.x < 2 * BT) s_words[threadIdx.x >> 1][threadIdx.x & 1] = 0u;
+    __syncthreads();
+    const int wrow0 = blk * kScoreRowsPerBlock + warp * kScoreRowsPerWarp;
+    uint32_t bits[BT];
+#pragma unroll
+    for (int bb = 0; bb < BT; ++bb) bits[bb] = 0u;
+
+#pragma unroll
+    for (int g = 0; g < kScoreRowsPerWarp; g += RIF) {
+      uint4 raw[RIF][CPL];
+#pragma unroll
+      for (int q = 0; q < RIF; ++q) {
+        const int row = wrow0 + g + q;
+#pragma unroll
+        for (int c = 0; c < CPL; ++c) {
+          const int ch = lane + 32 * c;
+          raw[q][c] = (row < f && ch < NC) ? ldg_stream(U + (size_t)row * r + ch * E)
+                                           : make_uint4(0, 0, 0, 0);
+        }
+      }
+#pragma unroll
+      for (int q = 0; q < RIF; ++q) {
+        const int row = wrow0 + g + q;
+        float acc[BT];
+#pragma unroll
+        for (int bb = 0; bb < BT; ++bb) acc[bb] = 0.f;
+#pragma unroll
+        for (int c = 0; c < CPL; ++c) {
+          const int ch = lane + 32 * c;
+          if (ch < NC) {
+            float w[E];
+            unpack<T>(raw[q][c], w);
+#pragma unroll
+            for (int bb = 0; bb < BT; ++bb) {
+              const float* hp = hs + bb * r + ch * E;
+#pragma unroll
+              for (int e = 0; e < E; ++e) acc[bb] = fmaf(w[e], hp[e], acc[bb]);
+            }
+          }
+        }
+        const float bias = row < f ? __ldg(&pb[row]) : 0.f;
+#pragma unroll
+        for (int bb = 0; bb < BT; ++bb) {
+          const float s = warp_sum(acc[bb]) + bias;
+          if (row < f && s > tau) bits[bb] |= 1u << (g + q);
+          if (scores != nullptr && lane == q && row < f && bb < nb) scores[(size_t)(b0 + bb) * f + row] = s;
+        }
+      }
+    }
+    if (lane == 0) {
+      const int word_in_blk = warp >> 2, shift = (warp & 3) * kScoreRowsPerWarp;
+#pragma unroll
+      for (int bb = 0; bb < BT; ++bb) atomicOr(&s_words[bb][word_in_blk], bits[bb] << shift);
+    }
+    __syncthreads();
+    if (threadIdx.x < 2 * BT) {
+      const int bb = threadIdx.x >> 1, wi = threadIdx.x & 1;
+      const int word = blk * 2 + wi;
+      if (bb < nb && word < W) mask[(size_t)(b0 + bb) * W + word] = s_words[bb][wi];
+    }
+  }
+}
+
+// One block per token: exclusive scan of the popcounts of the mask words,
+// then every set bit is written at its rank.
+constexpr int kCompactThreads = 512;
+
+__global__ void __launch_bounds__(kCompactThreads)
+    k_compact(const uint32_t* __restrict__ mask, int f, int W, int32_t* __restrict__ idx,
+              int32_t* __restrict__ n_active) {
+  __shared__ int s_warp[kCompactThreads / 32];
+  const int b = blockIdx.x;
+  const uint32_t* m = mask + (size_t)b * W;
+  const int wpt = (W + blockDim.x - 1) / blockDim.x;
+  const int w0 = threadIdx.x * wpt;
+  int cnt = 0;
+  for (int k = 0; k < wpt; ++k)
+    if (w0 + k < W) cnt += __popc(m[w0 + k]);
+  // block exclusive scan of cnt
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  int incl = cnt;
+#pragma unroll
+  for (int o = 1; o < 32; o <<= 1) {
+    const int v = __shfl_up_sync(0xffffffffu, incl, o);
+    if (lane >= o) incl += v;
+  }
+  if (lane == 31) s_warp[warp] = incl;
+  __syncthreads();
+  if (warp == 0) {
+    const int nw = blockDim.x >> 5;
+    int v = lane < nw ? s_warp[lane] : 0;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+      const int u = __shfl_up_sync(0xffffffffu, v, o);
+      if (lane >= o) v += u;
+    }
+    if (lane < nw) s_warp[lane] = v;  // inclusive warp totals
+  }
+  __syncthreads();
+  int pos = incl - cnt + (warp > 0 ? s_warp[warp - 1] : 0);
+  int32_t* out = idx + (size_t)b * f;
+  for (int k = 0; k < wpt; ++k) {
+    const int w = w0 + k;
+    if (w >= W) break;
+    uint32_t bitsw = m[w];
+    while (bitsw) {
+      const int j = __ffs(bitsw) - 1;
+      bitsw &= bitsw - 1;
+      out[pos++] = w * 32 + j;
+    }
+  }
+  if (threadIdx.x == blockDim.x - 1) n_active[b] = pos;
+}
+
+__global__ void k_count_bits(const uint32_t* __restrict__ mask, int B, int f, int W,
+                             int32_t* __restrict__ counts) {
+  for (int i = blockIdx.x * blockDim.x + threadIdx.x; i < f; i += gridDim.x * blockDim.x) {
+    int c = 0;
+    for (int b = 0; b < B; ++b) c += (mask[(size_t)b * W + (i >> 5)] >> (i & 31)) & 1u;
+    counts[i] += c;
+  }
+}
+
+template <typename T, int BT>
+cudaError_t hidden_launch(const PredHiddenArgs& a, cudaStream_t s) {
+  const dim3 grid(a.KS, pred_hidden_row_groups(a.r), (a.B + BT - 1) / BT);
+  const size_t smem = (size_t)BT * a.kc_elems * sizeof(T);
+  static bool attr = false;
+  if (!attr) {
+    cudaFuncSetAttribute(k_pred_hidden<T, BT>, cudaFuncAttributeMaxDynamicSharedMemorySize, 200 * 1024);
+    attr = true;
+  }
+  k_pred_hidden<T, BT><<<grid, kHiddenWarps * 32, smem, s>>>(
+      static_cast<const T*>(a.V), static_cast<const T*>(a.x), a.B, a.r, a.d, a.kc_elems, a.KS,
+      a.h_part, a.h, a.tickets);
+  return cudaGetLastError();
+}
+
+template <typename T>
+cudaError_t hidden_dispatch(const PredHiddenArgs& a, cudaStream_t s) {
+  if (a.B == 1) return hidden_launch<T, 1>(a, s);
+  if (a.B == 2) return hidden_launch<T, 2>(a, s);
+  if (a.B <= 4) return hidden_launch<T, 4>(a, s);
+  return hidden_launch<T, 8>(a, s);
+}
+
+template <typename T, int CPL, int BT>
+cudaError_t score_launch(const PredScoreArgs& a, cudaStream_t s) {
+  const dim3 grid(a.grid, (a.B + BT - 1) / BT);
+  const size_t smem = (size_t)BT * a.r * sizeof(float);
+  static bool attr = false;
+  if (!attr) {
+    cudaFuncSetAttribute(k_pred_score<T, CPL, BT>, cudaFuncAttributeMaxDynamicSharedMemorySize, 200 * 1024);
+    attr = true;
+  }
+  k_pred_score<T, CPL, BT><<<grid, kScoreWarps * 32, smem, s>>>(
+      static_cast<const T*>(a.U), a.h, a.pb, a.tau, a.B, a.f, a.r, a.W, a.mask, a.scores);
+  return cudaGetLastError();
+}
+
+template <typename T, int CPL>
+cudaError_t score_bt(const PredScoreArgs& a, cudaStream_t s) {
+  if (a.B == 1) return score_launch<T, CPL, 1>(a, s);
+  if (a.B == 2) return score_launch<T, CPL, 2>(a, s);
+  if (a.B <= 4) return score_launch<T, CPL, 4>(a, s);
+  return score_launch<T, CPL, 8>(a, s);
+}
+
+template <typename T>
+cudaError_t score_dispatch(const PredScoreArgs& a, cudaStream_t s) {
+  const int nc = a.r / Chunk<T>::N;
+  if (nc <= 32) return score_bt<T, 1>(a, s);
+  if (nc <= 64) return score_bt<T, 2>(a, s);
+  if (nc <= 128) return score_bt<T, 4>(a, s);
+  if (nc <= 256) return score_bt<T, 8>(a, s);
+  return cudaErrorInvalidValue;
+}
+
+}  // namespace
+
+int pred_hidden_row_groups(int r) { return (r + kHiddenRowsPerBlock - 1) / kHiddenRowsPerBlock; }
+
+cudaError_t launch_pred_hidden(int dtype, const PredHiddenArgs& a, cudaStream_t s) {
+  switch (dtype) {
+    case kF32: return hidden_dispatch<float>(a, s);
+    case kF16: return hidden_dispatch<__half>(a, s);
+    case kBF16: return hidden_dispatch<__nv_bfloat16>(a, s);
+  }
+  return cudaErrorInvalidValue;
+}
+
+cudaError_t launch_pred_score(int dtype, const PredScoreArgs& a, cudaStream_t s) {
+  switch (dtype) {
+    case kF32: return score_dispatch<float>(a, s);
+    case kF16: return score_dispatch<__half>(a, s);
+    case kBF16: return score_dispatch<__nv_bfloat16>(a, s);
+  }
+  return cudaErrorInvalidValue;
+}
+
+cudaError_t launch_compact(const uint32_t* mask, int B, int f, int W, int32_t* idx, int32_t* n_active,
+                           cudaStream_t s) {
+  k_compact<<<B, kCompactThreads, 0, s>>>(mask, f, W, idx, n_active);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_count_bits(const uint32_t* mask, int B, int f, int W, int32_t* counts, cudaStream_t s) {
+  const int threads = 256;
+  const int grid = (f + threads - 1) / threads;
+  k_count_bits<<<grid, threads, 0, s>>>(mask, B, f, W, counts);
+  return cudaGetLastError();
+}
+
+}  // namespace sffn

@@ -1,0 +1,210 @@
+/*
+ * sffn.h -- C ABI of the predictor-gated, activation-sparse FFN decode library
+ * (libsffn.so, CUDA kernels for sm_103a).
+ *
+ * What it computes.  For one decode token x (or a small batch of tokens), a
+ * per-layer online predictor scores every FFN neuron, the neurons predicted
+ * active are compacted into an ascending index list, and only their rows of
+ * W_up (and W_gate for ReGLU) and of W_down^T are read and accumulated:
+ *
+ *   h      = V x                                   (predictor hidden layer)
+ *   s_i    = U_i . h + pb_i ;  i active  <=>  s_i > tau   (strict)
+ *   a_i    = max(0, W_up[i] . x + b_i)                       (ReLU)
+ *          = max(0, W_gate[i] . x + b_i) * (W_up[i] . x)      (ReGLU)
+ *   y      = sum over active i, of a_i * W_down^T[i, :]
+ *
+ * Sources (the pages on PowerInfer and activation sparsity):
+ *   - predict-then-skip: "Predictores de espacialidad adaptativa" of the
+ *     PowerInfer page (unite.ai) and the adaptive sparse predictor of the
+ *     sparsity page (blogs.novita.ai, section 在線推理);
+ *   - neuron table (index list -> matrix row): PowerInfer page, "Colocacion y
+ *     gestion de neuronas";
+ *   - row/column neuron-aware operators: PowerInfer page, "Operador consciente
+ *     de neuronas"; skipped rows contribute zero: sparsity page, opening
+ *     section on ReLU activation sparsity;
+ *   - coalesced, fused kernels: sparsity page, section 工程影響.
+ * The predictor's low-rank linear form and the row layouts below are this
+ * library's reading; the pages give no formula.
+ *
+ * Conventions shared by every entry point.
+ *   - Device pointers are borrowed, never freed, and must stay valid until the
+ *     work queued on `stream` has finished.  The library allocates no device
+ *     memory of its own: every call takes a caller-owned `workspace`.
+ *   - `stream` is a cudaStream_t passed as void* (NULL = the legacy default
+ *     stream).  All device work is queued asynchronously on it; no entry point
+ *     synchronises except sffn_read_device_status.
+ *   - Layouts are row-major with one row per neuron:
+ *       W_up, W_gate, W_down^T : [d_ff][d_model]   (dtype)
+ *       U : [d_ff][rank] (dtype),  V : [rank][d_model] (dtype)
+ *       b, pb : [d_ff] float32
+ *       x : [batch][d_model] (dtype),  y : [batch][d_model] float32
+ *     W_down^T is the down projection stored transposed, so the output row of
+ *     neuron i is contiguous.  Every matrix row, x row and y row must start on
+ *     a 16-byte boundary: base pointers 16-byte aligned and d_model * sizeof
+ *     (dtype) and rank * sizeof(dtype) multiples of 16.
+ *   - Index lists are in the stored (possibly hot-first permuted) neuron order.
+ *   - Return values report argument validation and launch errors.  Conditions
+ *     found on the device (a bounded wait that timed out, a capacity limit) are
+ *     recorded in a status word inside the workspace and read with
+ *     sffn_read_device_status.  Kernels never trap.
+ *   - The workspace must be zero-filled once before its first use
+ *     (sffn_workspace_init does it); every call leaves it reusable.  Two calls
+ *     that share a workspace must be ordered (same stream, or synchronised).
+ */
+#ifndef SFFN_H
+#define SFFN_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum {
+  SFFN_OK = 0,
+  SFFN_ERR_INVALID_ARG = 1,  /* null/misaligned pointer, bad size, mismatch  */
+  SFFN_ERR_UNSUPPORTED = 2,  /* valid but not implemented (e.g. dtype)       */
+  SFFN_ERR_CUDA = 3,         /* a CUDA runtime call or launch failed         */
+  SFFN_ERR_CAPACITY = 4,     /* device: a list outgrew its buffer            */
+  SFFN_ERR_TIMEOUT = 5,      /* device: a bounded wait ran out               */
+  SFFN_ERR_WORKSPACE = 6     /* workspace null, misaligned or too small      */
+} sffn_status;
+
+typedef enum { SFFN_F32 = 0, SFFN_F16 = 1, SFFN_BF16 = 2 } sffn_dtype;
+typedef enum { SFFN_RELU = 0, SFFN_REGLU = 1 } sffn_act;
+
+typedef struct sffn_layer* sffn_layer_t;
+
+/* One FFN layer and its predictor.  All pointers are device pointers. */
+typedef struct {
+  int32_t d_model;      /* model width d                                    */
+  int32_t d_ff;         /* FFN width (number of neurons)                    */
+  int32_t rank;         /* predictor rank r (rows of V, columns of U)       */
+  int32_t max_batch;    /* largest batch later calls may pass (1..32)       */
+  int32_t dtype;        /* sffn_dtype of weights, U, V and x               */
+  int32_t act;          /* sffn_act                                         */
+  const void* w_up;     /* [d_ff][d_model]                                  */
+  const void* w_gate;   /* [d_ff][d_model], ReGLU only, else NULL           */
+  const void* w_downT;  /* [d_ff][d_model]                                  */
+  const float* b;       /* [d_ff] bias of the gated pre-activation; NULL=0  */
+  const void* pred_U;   /* [d_ff][rank]                                     */
+  const void* pred_V;   /* [rank][d_model]                                  */
+  const float* pred_b;  /* [d_ff] predictor bias                            */
+  float tau;            /* threshold: neuron i is active iff s_i > tau      */
+} sffn_layer_desc;
+
+/* Validates the descriptor and records it with launch settings chosen for the
+ * current device.  Allocates only host memory.  Returns INVALID_ARG for bad
+ * shapes or pointers, UNSUPPORTED for shapes outside the kernels' limits. */
+sffn_status sffn_create_layer(const sffn_layer_desc* desc, sffn_layer_t* out);
+sffn_status sffn_destroy_layer(sffn_layer_t layer);
+
+/* Bytes of workspace a call with `batch` tokens needs (0 on bad arguments). */
+size_t sffn_workspace_size(sffn_layer_t layer, int32_t batch);
+
+/* Zero-fills a workspace (cudaMemsetAsync on `stream`). */
+sffn_status sffn_workspace_init(void* workspace, size_t workspace_bytes, void* stream);
+
+/* Predictor + compaction (the online predictor and the neuron table).
+ *   x        : [batch][d_model] dtype, device
+ *   idx      : [batch][d_ff] int32, device; row t receives the ascending list
+ *              of token t's active neurons in its first n_active[t] entries
+ *   n_active : [batch] int32, device */
+sffn_status sffn_predict(sffn_layer_t layer, const void* x, int32_t batch, int32_t* idx,
+                         int32_t* n_active, void* workspace, size_t workspace_bytes,
+                         void* stream);
+
+/* Predictor scores s = U (V x) + pb as float32 [batch][d_ff] (diagnostics:
+ * the same kernels as sffn_predict, scores written out). */
+sffn_status sffn_predict_scores(sffn_layer_t layer, const void* x, int32_t batch, float* scores,
+                                void* workspace, size_t workspace_bytes, void* stream);
+
+/* The sparse FFN for a batch of decode tokens: predict, compact, gather the
+ * active rows, apply ReLU / ReGLU, accumulate the down projection.
+ *   y            : [batch][d_model] float32, device (overwritten)
+ *   idx_out      : NULL or [batch][d_ff] int32 (as sffn_predict)
+ *   n_active_out : NULL or [batch] int32
+ * Each token uses its own predicted set; a batch reads the union of the rows
+ * once.  Results do not depend on which other tokens share the batch beyond
+ * floating-point summation order. */
+sffn_status sffn_forward(sffn_layer_t layer, const void* x, int32_t batch, float* y,
+                         int32_t* idx_out, int32_t* n_active_out, void* workspace,
+                         size_t workspace_bytes, void* stream);
+
+/* The no-skip FFN (every neuron computed, no predictor), same layouts as
+ * sffn_forward: the dense contrast of the sparse path. */
+sffn_status sffn_dense_forward(sffn_layer_t layer, const void* x, int32_t batch, float* y,
+                               void* workspace, size_t workspace_bytes, void* stream);
+
+/* x_out = round_dtype(LayerNorm(x + y) * gamma + beta) per token, biased
+ * variance, float32 arithmetic; gamma/beta NULL mean 1 and 0.
+ *   x, x_out : [batch][d_model] dtype;  y : [batch][d_model] float32 */
+sffn_status sffn_residual_layernorm(const void* x, const float* y, int32_t batch,
+                                    int32_t d_model, int32_t dtype, const float* gamma,
+                                    const float* beta, float eps, void* x_out, void* stream);
+
+/* Greedy-shaped decode through a stack of layers (equal d_model and dtype):
+ * every step runs each layer's sparse FFN followed by residual + LayerNorm,
+ * x_{l+1} = round(LN(x_l + y_l)), and the next step starts from the last
+ * layer's output.
+ *   x0      : [batch][d_model] dtype, first step's input
+ *   x_out   : [n_steps][batch][d_model] dtype, last layer's output per step
+ *   x_trace : NULL or [n_steps][n_layers][batch][d_model] dtype, the input of
+ *             every layer at every step
+ *   ln_gamma, ln_beta : NULL or [d_model] float32 shared by all layers */
+sffn_status sffn_forward_stack(const sffn_layer_t* layers, int32_t n_layers, const void* x0,
+                               int32_t batch, int32_t n_steps, void* x_out, void* x_trace,
+                               const float* ln_gamma, const float* ln_beta, float ln_eps,
+                               void* workspace, size_t workspace_bytes, void* stream);
+size_t sffn_stack_workspace_size(const sffn_layer_t* layers, int32_t n_layers, int32_t batch);
+
+/* Offline profile pass (hot/cold classification by activation frequency):
+ * counts[i] = number of the n_tokens rows of X (device, [n_tokens][d_model])
+ * for which neuron i is predicted active.  counts: [d_ff] int32, device,
+ * overwritten. */
+sffn_status sffn_profile_counts(sffn_layer_t layer, const void* X, int32_t n_tokens,
+                                int32_t* counts, void* workspace, size_t workspace_bytes,
+                                void* stream);
+
+/* Host-side: perm[new] = old, neurons by descending count, ties by ascending
+ * index.  counts and perm are host arrays of d_ff entries. */
+sffn_status sffn_hot_first_perm(const int32_t* counts, int32_t d_ff, int32_t* perm);
+
+/* dst row i = src row perm[i] (device pointers, 4-byte aligned, rows of
+ * row_bytes bytes, a multiple of 4; perm is a device int32 array of `rows`
+ * entries; src and dst must not overlap).  Used to apply the hot-first order
+ * to W_up, W_gate, W_down^T, U and b together. */
+sffn_status sffn_permute_rows(const void* src, void* dst, const int32_t* perm, int32_t rows,
+                              int64_t row_bytes, void* stream);
+
+/* Synchronises `stream`, copies the workspace status word to *status (an
+ * sffn_status value) and clears it. */
+sffn_status sffn_read_device_status(void* workspace, int32_t* status, void* stream);
+
+/* Test hook for the bounded waits: queues a one-block kernel that waits, with
+ * the library's grid-barrier code and a limit of timeout_ns nanoseconds, for
+ * an arrival that never comes; the status word then reads SFFN_ERR_TIMEOUT. */
+sffn_status sffn_debug_wait_timeout(void* workspace, size_t workspace_bytes, int64_t timeout_ns,
+                                    void* stream);
+
+/* Profiling hook: when both are non-NULL, every later gather launch (the
+ * fused row-gather FFN kernel of sffn_forward / sffn_dense_forward /
+ * sffn_forward_stack) is bracketed by cudaEventRecord(start_event) and
+ * cudaEventRecord(stop_event) on its stream (cudaEvent_t passed as void*).
+ * NULL, NULL switches it off.  Process-wide, not thread-safe: for timing. */
+sffn_status sffn_set_profile_events(void* start_event, void* stop_event);
+
+/* Limit of every device-side wait, in nanoseconds (default 1e9). */
+sffn_status sffn_set_wait_limit_ns(int64_t ns);
+
+const char* sffn_status_string(sffn_status status);
+/* Message of the last failed call on this host thread ("" if none). */
+const char* sffn_last_error(void);
+int32_t sffn_version(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* SFFN_H */

@@ -1,0 +1,304 @@
+"""GPU parity: the CUDA path through the C ABI against the CPU oracle on the
+same seeded inputs (single-layer workloads, edge cases, boundary errors,
+bounded-wait status)."""
+
+import numpy as np
+import pytest
+import torch
+
+import oracle
+from activation_sparse_decode_gb300 import workloads as W
+from activation_sparse_decode_gb300.workloads import to_numpy_stored as st
+from gpu_helpers import TOL, check_token, hot_first, mask_from_list, oracle_layer, rel_l2
+
+pytestmark = pytest.mark.gpu
+
+DEV = "cuda"
+
+
+@pytest.fixture(scope="module")
+def sffn():
+    if not torch.cuda.is_available():
+        pytest.skip("no CUDA device")
+    from activation_sparse_decode_gb300 import build
+    build.build()
+    from activation_sparse_decode_gb300 import sffn as mod
+    return mod
+
+
+def run_tokens(sffn, layer, X, want_idx=True):
+    """Decode the tokens X [T][B][d] one step at a time (batch B per step)."""
+    T, B, d = X.shape
+    f = layer.d_ff
+    ws = sffn.new_workspace(sffn.sffn_workspace_size(layer, B), DEV)
+    Y = torch.empty(T, B, d, dtype=torch.float32, device=DEV)
+    I = torch.empty(T, B, f, dtype=torch.int32, device=DEV) if want_idx else None
+    N = torch.empty(T, B, dtype=torch.int32, device=DEV) if want_idx else None
+    for t in range(T):
+        sffn.sffn_forward(layer, X[t], Y[t], ws, None if I is None else I[t], None if N is None else N[t])
+    torch.cuda.synchronize()
+    assert sffn.sffn_read_device_status(ws) == 0
+    return Y.cpu().numpy(), None if I is None else I.cpu().numpy(), None if N is None else N.cpu().numpy()
+
+
+# ---------------------------------------------------------------- ReLU FFN d1024 f4096 fp32 (64 tokens)
+
+def test_c1_every_token(sffn):
+    wl = W.get_workload("c1")
+    lw = W.make_layer(wl, device=DEV)
+    layer = sffn.Layer.from_weights(lw, tau=wl.tau)
+    ol = oracle_layer(lw, wl.tau)
+    X = W.make_tokens(wl, wl.steps, device=DEV)
+    Y, I, N = run_tokens(sffn, layer, X)
+    Xh = st(X)
+    band_total = 0
+    for t in range(wl.steps):
+        m = mask_from_list(I[t, 0], N[t, 0], wl.d_ff)
+        band, flipped, _ = check_token(ol, Xh[t, 0], m, Y[t, 0], TOL[wl.dtype])
+        band_total += band
+    assert 0.05 < N.mean() / wl.d_ff < 0.15
+
+
+def test_c1_predict_entry_points(sffn):
+    wl = W.get_workload("c1")
+    lw = W.make_layer(wl, device=DEV)
+    layer = sffn.Layer.from_weights(lw, tau=wl.tau, max_batch=8)
+    ol = oracle_layer(lw, wl.tau)
+    X = W.make_tokens(wl, 1, batch=8, device=DEV)[0]
+    ws = sffn.new_workspace(sffn.sffn_workspace_size(layer, 8), DEV)
+    S = torch.empty(8, wl.d_ff, dtype=torch.float32, device=DEV)
+    I = torch.empty(8, wl.d_ff, dtype=torch.int32, device=DEV)
+    N = torch.empty(8, dtype=torch.int32, device=DEV)
+    sffn.sffn_predict_scores(layer, X, S, ws)
+    sffn.sffn_predict(layer, X, I, N, ws)
+    torch.cuda.synchronize()
+    S, I, N = S.cpu().numpy(), I.cpu().numpy(), N.cpu().numpy()
+    so = oracle.predictor_scores(ol, st(X))
+    assert rel_l2(S, so) < 1e-6
+    for t in range(8):
+        m = mask_from_list(I[t], N[t], wl.d_ff)
+        band = np.abs(so[t]) <= 1e-4
+        assert not ((m != (so[t] > 0)) & ~band).any()
+        assert np.array_equal(m, S[t] > 0)  # the list is the GPU's own scores thresholded
+
+
+# ---------------------------------------------------------------- OPT-6.7B FFN, fp16, hot-first, 512 tokens
+
+def test_c2_full_size_sampled(sffn):
+    wl = W.get_workload("c2")
+    lw0 = W.make_layer(wl, device=DEV)
+    lw, perm, counts = hot_first(sffn, lw0, wl)
+    del lw0
+    c = counts.cpu().numpy()
+    assert np.all(np.diff(c[perm]) <= 0)
+    layer = sffn.Layer.from_weights(lw, tau=wl.tau)
+    X = W.make_tokens(wl, wl.steps, device=DEV)
+    Y, I, N = run_tokens(sffn, layer, X)
+    ol = oracle_layer(lw, wl.tau)
+    Xh = st(X)
+    rng = np.random.Generator(np.random.PCG64(7))
+    for t in sorted(rng.choice(wl.steps, 12, replace=False)):
+        m = mask_from_list(I[t, 0], N[t, 0], wl.d_ff)
+        check_token(ol, Xh[t, 0], m, Y[t, 0], TOL[wl.dtype])
+    # hot-first: the most frequent neurons come first, so the first rows are active far more often
+    first = (I[:, 0, :] < 400) & (np.arange(wl.d_ff)[None, :] < N[:, 0][:, None])
+    assert first.sum(1).mean() > 300
+
+
+# ---------------------------------------------------------------- Llama-7B ReGLU, bf16, batches 1/4/8/32
+
+@pytest.fixture(scope="module")
+def c3(sffn):
+    wl = W.get_workload("c3")
+    lw = W.make_layer(wl, device=DEV)
+    return wl, lw, oracle_layer(lw, wl.tau)
+
+
+@pytest.mark.parametrize("batch", [1, 4, 8, 32])
+def test_c3_reglu_batches(sffn, c3, batch):
+    wl, lw, ol = c3
+    layer = sffn.Layer.from_weights(lw, tau=wl.tau, max_batch=32)
+    steps = 2
+    X = W.make_tokens(wl, steps, batch=batch, device=DEV)
+    Y, I, N = run_tokens(sffn, layer, X)
+    Xh = st(X)
+    rng = np.random.Generator(np.random.PCG64(batch))
+    picks = [(s, b) for s in range(steps) for b in range(batch)]
+    if len(picks) > 8:
+        picks = [picks[i] for i in sorted(rng.choice(len(picks), 8, replace=False))]
+    for s, b in picks:
+        m = mask_from_list(I[s, b], N[s, b], wl.d_ff)
+        check_token(ol, Xh[s, b], m, Y[s, b], TOL[wl.dtype])
+    # batch invariance: each token alone gives the same output (up to summation order)
+    if batch > 1:
+        Y1, _, _ = run_tokens(sffn, layer, X[0, :4].reshape(4, 1, -1).contiguous(), want_idx=False)
+        for b in range(min(batch, 4)):
+            assert rel_l2(Y[0, b], Y1[b, 0]) < 1e-5
+
+
+# ---------------------------------------------------------------- dense contrast and degenerate masks
+
+def test_dense_forward_matches_oracle(sffn, c3):
+    wl, lw, ol = c3
+    layer = sffn.Layer.from_weights(lw, max_batch=4)
+    X = W.make_tokens(wl, 1, batch=4, device=DEV)[0]
+    ws = sffn.new_workspace(sffn.sffn_workspace_size(layer, 4), DEV)
+    Y = torch.empty(4, wl.d_model, dtype=torch.float32, device=DEV)
+    sffn.sffn_dense_forward(layer, X, Y, ws)
+    Y = Y.cpu().numpy()
+    Xh = st(X)
+    for b in range(4):
+        assert rel_l2(Y[b], oracle.dense_ffn(ol, Xh[b])) < TOL[wl.dtype]
+
+
+SMALL = [  # (d_model, d_ff, rank, dtype, act, batch)
+    (256, 1000, 32, "f16", "relu", 1),
+    (1000, 777, 8, "f16", "relu", 3),
+    (8, 64, 8, "bf16", "reglu", 2),
+    (64, 40, 4, "f32", "relu", 1),
+    (4096, 3000, 64, "bf16", "reglu", 4),
+    (512, 333, 16, "f32", "reglu", 5),
+]
+
+
+@pytest.mark.parametrize("shape", SMALL, ids=lambda s: "d%d_f%d_r%d_%s_%s_b%d" % s)
+def test_ragged_small_layers(sffn, shape):
+    d, f, r, dt, act, batch = shape
+    wl = W.tiny_workload(d_model=d, d_ff=f, rank=r, dtype=dt, act=act, mean_p=0.2, name=f"ragged{shape}")
+    lw = W.make_layer(wl, device=DEV)
+    ol = oracle_layer(lw)
+    layer = sffn.Layer.from_weights(lw, max_batch=batch)
+    X = W.make_tokens(wl, 3, batch=batch, device=DEV)
+    Y, I, N = run_tokens(sffn, layer, X)
+    Xh = st(X)
+    for s in range(3):
+        for b in range(batch):
+            m = mask_from_list(I[s, b], N[s, b], f)
+            check_token(ol, Xh[s, b], m, Y[s, b], TOL[dt])
+
+
+@pytest.mark.parametrize("tau,expect", [(1e30, "none"), (-1e30, "all")])
+def test_all_false_and_all_true_masks(sffn, tau, expect):
+    wl = W.tiny_workload(d_model=512, d_ff=1500, rank=32, dtype="f16", name="degenerate")
+    lw = W.make_layer(wl, device=DEV)
+    ol = oracle_layer(lw, tau)
+    layer = sffn.Layer.from_weights(lw, tau=tau, max_batch=2)
+    X = W.make_tokens(wl, 2, batch=2, device=DEV)
+    Y, I, N = run_tokens(sffn, layer, X)
+    if expect == "none":
+        assert (N == 0).all()
+        assert (Y == 0).all()
+    else:
+        assert (N == wl.d_ff).all()
+        Xh = st(X)
+        for s in range(2):
+            for b in range(2):
+                assert rel_l2(Y[s, b], oracle.dense_ffn(ol, Xh[s, b])) < TOL["f16"]
+
+
+def test_deterministic_run_to_run(sffn, c3):
+    wl, lw, _ = c3
+    layer = sffn.Layer.from_weights(lw, max_batch=4)
+    X = W.make_tokens(wl, 1, batch=4, device=DEV)
+    a, _, _ = run_tokens(sffn, layer, X, want_idx=False)
+    b, _, _ = run_tokens(sffn, layer, X, want_idx=False)
+    assert np.array_equal(a, b)
+
+
+# ---------------------------------------------------------------- LayerNorm, permutation, profile
+
+@pytest.mark.parametrize("dt", ["f32", "f16", "bf16"])
+def test_residual_layernorm(sffn, dt):
+    g = torch.Generator(device=DEV).manual_seed(3)
+    d, B = 5120, 3
+    x = (torch.randn(B, d, generator=g, device=DEV) * 2 + 0.5).to(W.TORCH_DTYPES[dt])
+    y = torch.randn(B, d, generator=g, device=DEV) * 0.3
+    gamma = torch.rand(d, generator=g, device=DEV) + 0.5
+    beta = torch.randn(d, generator=g, device=DEV) * 0.1
+    out = torch.empty_like(x)
+    for gm, bt in ((None, None), (gamma, beta)):
+        sffn.sffn_residual_layernorm(x, y, out, gm, bt, 1e-5)
+        torch.cuda.synchronize()
+        want = oracle.residual_layernorm(st(x), y.cpu().numpy(), dt,
+                                         None if gm is None else gm.cpu().numpy(),
+                                         None if bt is None else bt.cpu().numpy(), 1e-5)
+        got_v, want_v = oracle.decode(st(out), dt), oracle.decode(want, dt)
+        ulp = {"f32": 2.0 ** -23, "f16": 2.0 ** -10, "bf16": 2.0 ** -7}[dt]
+        err = np.abs(got_v - want_v) / np.maximum(np.abs(want_v), 1e-3)
+        assert err.max() <= 1.01 * ulp + 1e-6
+        assert (got_v != want_v).mean() < 0.05 if dt != "f32" else True
+    # in place
+    x2 = x.clone()
+    sffn.sffn_residual_layernorm(x2, y, x2)
+    sffn.sffn_residual_layernorm(x, y, out)
+    torch.cuda.synchronize()
+    assert torch.equal(x2, out)
+
+
+def test_permute_rows_and_profile_counts(sffn):
+    wl = W.get_workload("c1")
+    lw = W.make_layer(wl, device=DEV)
+    ol = oracle_layer(lw, wl.tau)
+    layer = sffn.Layer.from_weights(lw, tau=wl.tau, max_batch=8)
+    Xp = W.make_profile_tokens(wl, n_tokens=200, device=DEV)
+    ws = sffn.new_workspace(sffn.sffn_workspace_size(layer, 8), DEV)
+    perm, counts = sffn.hot_first_order(layer, Xp, ws)
+    counts = counts.cpu().numpy()
+    S = np.stack([oracle.predictor_scores(ol, x) for x in st(Xp)])
+    co = (S > 0).sum(0)
+    band = (np.abs(S) <= 1e-4).sum(0)
+    assert np.all(np.abs(counts - co) <= band)
+    assert np.array_equal(perm, oracle.hot_first_perm(counts))
+    pd = torch.from_numpy(perm).to(DEV)
+    plw = sffn.permute_layer_weights(lw, pd)
+    assert torch.equal(plw.w_up.cpu(), lw.w_up.cpu()[perm])
+    assert torch.equal(plw.U.cpu(), lw.U.cpu()[perm])
+    assert torch.equal(plw.b.cpu(), lw.b.cpu()[perm])
+    assert torch.equal(plw.w_downT.cpu(), lw.w_downT.cpu()[perm])
+
+
+# ---------------------------------------------------------------- boundary and status
+
+def test_bounded_wait_reports_timeout(sffn):
+    ws = sffn.new_workspace(4096, DEV)
+    sffn.sffn_debug_wait_timeout(ws, 2_000_000)
+    assert sffn.sffn_read_device_status(ws) == 5
+    assert sffn.sffn_read_device_status(ws) == 0  # reading clears it
+    # the context is still usable
+    wl = W.tiny_workload(d_model=64, d_ff=256, rank=8, dtype="f32", name="after-timeout")
+    lw = W.make_layer(wl, device=DEV)
+    layer = sffn.Layer.from_weights(lw)
+    X = W.make_tokens(wl, 1, device=DEV)
+    Y, I, N = run_tokens(sffn, layer, X)
+    check_token(oracle_layer(lw), st(X)[0, 0], mask_from_list(I[0, 0], N[0, 0], 256), Y[0, 0], 1e-5)
+
+
+def test_boundary_errors(sffn):
+    wl = W.tiny_workload(d_model=64, d_ff=256, rank=8, dtype="f16", name="boundary")
+    lw = W.make_layer(wl, device=DEV)
+    layer = sffn.Layer.from_weights(lw, max_batch=2)
+    need = sffn.sffn_workspace_size(layer, 2)
+    ws = sffn.new_workspace(need, DEV)
+    x = W.make_tokens(wl, 1, batch=2, device=DEV)[0]
+    y = torch.empty(2, 64, device=DEV)
+    with pytest.raises(sffn.SffnError) as e:
+        sffn.sffn_forward(layer, W.make_tokens(wl, 1, batch=3, device=DEV)[0], torch.empty(3, 64, device=DEV), ws)
+    assert e.value.status == 1
+    with pytest.raises(sffn.SffnError) as e:
+        sffn.sffn_forward(layer, x, y, ws[: need - 256])
+    assert e.value.status == 6
+    with pytest.raises(sffn.SffnError) as e:
+        sffn.sffn_forward(layer, x, y.view(-1)[1:129].view(2, 64), ws)
+    assert e.value.status == 1
+    with pytest.raises(sffn.SffnError) as e:
+        sffn.sffn_forward(layer, x.view(-1)[1:129].view(2, 64), y, ws)
+    assert e.value.status == 1
+    with pytest.raises(sffn.SffnError) as e:
+        sffn.Layer(lw.w_up.view(-1)[4:4 + 255 * 64].view(255, 64), lw.w_downT, lw.b, lw.U, lw.V)  # 8-byte offset
+    assert e.value.status == 1
+    with pytest.raises(sffn.SffnError) as e:
+        sffn.sffn_forward(layer, x, y, ws, idx=torch.empty(2, 256, dtype=torch.int32, device=DEV))
+    assert e.value.status == 1
+    sffn.sffn_forward(layer, x, y, ws)
+    torch.cuda.synchronize()
+    assert sffn.sffn_read_device_status(ws) == 0

@@ -223,10 +223,15 @@ def test_residual_layernorm(sffn, dt):
                                          None if gm is None else gm.cpu().numpy(),
                                          None if bt is None else bt.cpu().numpy(), 1e-5)
         got_v, want_v = oracle.decode(st(out), dt), oracle.decode(want, dt)
-        ulp = {"f32": 2.0 ** -23, "f16": 2.0 ** -10, "bf16": 2.0 ** -7}[dt]
-        err = np.abs(got_v - want_v) / np.maximum(np.abs(want_v), 1e-3)
-        assert err.max() <= 1.01 * ulp + 1e-6
-        assert (got_v != want_v).mean() < 0.05 if dt != "f32" else True
+        if dt == "f32":
+            # fp32 arithmetic on O(1) normalised values: absolute error ~1e-7
+            assert np.abs(got_v - want_v).max() <= 1e-5
+        else:
+            # one rounding step of the stored format at most, on few elements
+            ulp = {"f16": 2.0 ** -10, "bf16": 2.0 ** -7}[dt]
+            err = np.abs(got_v - want_v) / np.maximum(np.abs(want_v), 2.0 ** -6)
+            assert err.max() <= 1.01 * ulp + 1e-5
+            assert (got_v != want_v).mean() < 0.05
     # in place
     x2 = x.clone()
     sffn.sffn_residual_layernorm(x2, y, x2)
@@ -288,10 +293,10 @@ def test_boundary_errors(sffn):
         sffn.sffn_forward(layer, x, y, ws[: need - 256])
     assert e.value.status == 6
     with pytest.raises(sffn.SffnError) as e:
-        sffn.sffn_forward(layer, x, y.view(-1)[1:129].view(2, 64), ws)
+        sffn.sffn_forward(layer, x, torch.empty(136, device=DEV)[1:129].view(2, 64), ws)
     assert e.value.status == 1
     with pytest.raises(sffn.SffnError) as e:
-        sffn.sffn_forward(layer, x.view(-1)[1:129].view(2, 64), y, ws)
+        sffn.sffn_forward(layer, torch.empty(136, dtype=x.dtype, device=DEV)[1:129].view(2, 64), y, ws)
     assert e.value.status == 1
     with pytest.raises(sffn.SffnError) as e:
         sffn.Layer(lw.w_up.view(-1)[4:4 + 255 * 64].view(255, 64), lw.w_downT, lw.b, lw.U, lw.V)  # 8-byte offset

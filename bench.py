@@ -235,18 +235,20 @@ def bench_sffn(args):
         step_body(prof_events)
     launches_per_step = 3 * T  # predictor hidden, predictor scores, fused gather per token
 
-    # ---- device-timed steps (inputs resident in HBM)
-    for _ in range(args.warmup):
-        graph.replay()
+    # ---- device-timed steps (inputs resident in HBM); every replay and event on `stream`
+    with torch.cuda.stream(stream):
+        for _ in range(args.warmup):
+            graph.replay()
     torch.cuda.synchronize()
     e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     with ClockSampler(local) as clk:
         barrier(world)
         torch.cuda.synchronize()
-        e0.record(stream)
-        for _ in range(args.steps):
-            graph.replay()
-        e1.record(stream)
+        with torch.cuda.stream(stream):
+            e0.record(stream)
+            for _ in range(args.steps):
+                graph.replay()
+            e1.record(stream)
         torch.cuda.synchronize()
         barrier(world)
     clocks = clk.summary()
@@ -256,13 +258,15 @@ def bench_sffn(args):
     value = T * args.steps * world / (ms_max / 1e3)
 
     # ---- the dominant kernel (fused gather), its launches bracketed by events
-    for _ in range(3):
-        pgraph.replay()
+    with torch.cuda.stream(stream):
+        for _ in range(3):
+            pgraph.replay()
     torch.cuda.synchronize()
     reps_k = max(3, min(20, args.steps // 10))
     dur = np.zeros(T)
     for _ in range(reps_k):
-        pgraph.replay()
+        with torch.cuda.stream(stream):
+            pgraph.replay()
         torch.cuda.synchronize()
         dur += np.array([a.elapsed_time(b) for a, b in prof_events])
     dur /= reps_k  # ms per launch, per token
@@ -286,25 +290,23 @@ def bench_sffn(args):
     # ---- end to end: pinned host tokens in, host outputs back, every step
     Xh = X.cpu().pin_memory()
     Yh = torch.empty(Y.shape, dtype=Y.dtype).pin_memory()
-    for _ in range(2):
-        with torch.cuda.stream(stream):
+    with torch.cuda.stream(stream):
+        for _ in range(2):
             X.copy_(Xh, non_blocking=True)
-        graph.replay()
-        with torch.cuda.stream(stream):
+            graph.replay()
             Yh.copy_(Y, non_blocking=True)
     torch.cuda.synchronize()
     e_steps = max(3, args.steps // 4)
     barrier(world)
     torch.cuda.synchronize()
     t0 = time.perf_counter()
-    e0.record(stream)
-    for _ in range(e_steps):
-        with torch.cuda.stream(stream):
+    with torch.cuda.stream(stream):
+        e0.record(stream)
+        for _ in range(e_steps):
             X.copy_(Xh, non_blocking=True)
-        graph.replay()
-        with torch.cuda.stream(stream):
+            graph.replay()
             Yh.copy_(Y, non_blocking=True)
-    e1.record(stream)
+        e1.record(stream)
     torch.cuda.synchronize()
     wall = time.perf_counter() - t0
     barrier(world)

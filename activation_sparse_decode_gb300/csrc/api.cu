@@ -30,6 +30,9 @@ struct sffn_layer {
   int max_bt = 0;      // tokens per gather pass
   GatherConfig gcfg[3];  // tokens per pass 1, 2, 4
   bool gcfg_ok[3] = {false, false, false};
+  LayerConfig lcfg{};    // single-launch batch-1 layer kernel
+  bool lcfg_ok = false;
+  bool fused() const { return lcfg_ok && !(desc.flags & SFFN_FLAG_MULTI_KERNEL); }
 };
 
 namespace {
@@ -61,7 +64,7 @@ size_t align_up(size_t v, size_t a) { return (v + a - 1) / a * a; }
 int bt_slot(int bt) { return bt == 1 ? 0 : bt == 2 ? 1 : 2; }
 
 struct WsLayout {
-  size_t hdr, tickets, h_part, h, mask, y_part, total;
+  size_t hdr, tickets, h_part, h, mask, y_part, hl_part, total;
 };
 
 WsLayout layout(const sffn_layer* L, int batch) {
@@ -79,6 +82,7 @@ WsLayout layout(const sffn_layer* L, int batch) {
   w.h = take((size_t)batch * d.rank * sizeof(float));
   w.mask = take((size_t)batch * L->W * sizeof(uint32_t));
   w.y_part = take((size_t)L->gather_grid * std::min(batch, L->max_bt) * d.d_model * sizeof(float));
+  w.hl_part = take(L->lcfg_ok ? (size_t)L->lcfg.KS * d.rank * sizeof(float) : 0);
   w.total = off;
   return w;
 }
@@ -92,6 +96,7 @@ struct Ws {
   float* h() const { return reinterpret_cast<float*>(base + lay.h); }
   uint32_t* mask() const { return reinterpret_cast<uint32_t*>(base + lay.mask); }
   float* y_part() const { return reinterpret_cast<float*>(base + lay.y_part); }
+  float* hl_part() const { return reinterpret_cast<float*>(base + lay.hl_part); }
 };
 
 sffn_status check_ws(const sffn_layer* L, int batch, void* ws, size_t bytes, Ws* out) {
@@ -195,6 +200,47 @@ sffn_status run_gather(const sffn_layer* L, const void* x, int batch, float* y, 
 }
 
 sffn_status check_x(const sffn_layer* L, const void* x) { return check_dev_ptr(x, "x"); }
+
+// One token through the single-launch layer kernel.  With y_prev, the kernel
+// first forms x = round(LN(x_prev + y_prev)) and stores it at x_ln_out.
+sffn_status run_layer(const sffn_layer* L, const void* x, const float* y_prev, void* x_ln_out, const float* gamma,
+                      const float* beta, float eps, float* y, uint32_t* mask, const Ws& ws, cudaStream_t s) {
+  const auto& d = L->desc;
+  LayerArgs a{};
+  a.x = x;
+  a.y_prev = y_prev;
+  a.x_ln_out = x_ln_out;
+  a.ln_gamma = gamma;
+  a.ln_beta = beta;
+  a.ln_eps = eps;
+  a.V = d.pred_V;
+  a.U = d.pred_U;
+  a.pb = d.pred_b;
+  a.b = d.b;
+  a.tau = d.tau;
+  a.w_up = d.w_up;
+  a.w_gate = d.w_gate;
+  a.w_downT = d.w_downT;
+  a.y = y;
+  a.h_part = ws.hl_part();
+  a.mask = mask;
+  a.hdr = ws.hdr();
+  a.d = d.d_model;
+  a.f = d.d_ff;
+  a.r = d.rank;
+  a.KS = L->lcfg.KS;
+  a.kc = L->lcfg.kc;
+  a.RG = L->lcfg.RG;
+  a.act = d.act;
+  a.nstages = L->lcfg.nstages;
+  a.u_smem = L->lcfg.u_smem;
+  a.region_bytes = L->lcfg.region_bytes;
+  a.wait_ns = (uint64_t)g_wait_ns;
+  if (g_prof_start != nullptr) SFFN_TRY(record_profile_event(g_prof_start, s));
+  SFFN_CUDA(launch_layer(d.dtype, L->lcfg, a, L->gather_grid, s), "layer launch");
+  if (g_prof_stop != nullptr) SFFN_TRY(record_profile_event(g_prof_stop, s));
+  return SFFN_OK;
+}
 
 }  // namespace
 
@@ -301,6 +347,7 @@ sffn_status sffn_create_layer(const sffn_layer_desc* desc, sffn_layer_t* out) {
     return fail(SFFN_ERR_UNSUPPORTED, "rows of d_model %d do not fit two pipeline stages", d.d_model);
   }
   while (!L->gcfg_ok[bt_slot(L->max_bt)]) L->max_bt /= 2;
+  L->lcfg_ok = layer_config(d.dtype, d.act, d.d_model, d.d_ff, d.rank, L->gather_grid, L->smem_optin, &L->lcfg);
   *out = L;
   return SFFN_OK;
 }
@@ -360,6 +407,12 @@ sffn_status sffn_forward(sffn_layer_t L, const void* x, int32_t batch, float* y,
   Ws ws;
   SFFN_TRY(check_ws(L, batch, workspace, ws_bytes, &ws));
   cudaStream_t s = static_cast<cudaStream_t>(stream);
+  if (batch == 1 && L->fused()) {
+    SFFN_TRY(run_layer(L, x, nullptr, nullptr, nullptr, nullptr, 0.f, y, idx_out ? ws.mask() : nullptr, ws, s));
+    if (idx_out != nullptr)
+      SFFN_CUDA(launch_compact(ws.mask(), 1, L->desc.d_ff, L->W, idx_out, n_active_out, s), "compaction launch");
+    return SFFN_OK;
+  }
   SFFN_TRY(run_predictor(L, x, batch, ws, nullptr, s));
   if (idx_out != nullptr)
     SFFN_CUDA(launch_compact(ws.mask(), batch, L->desc.d_ff, L->W, idx_out, n_active_out, s), "compaction launch");
@@ -407,7 +460,7 @@ size_t sffn_stack_workspace_size(const sffn_layer_t* layers, int32_t n_layers, i
   const auto& d = layers[0]->desc;
   const size_t xb = align_up((size_t)batch * d.d_model * layers[0]->esize, 256);
   const size_t yb = align_up((size_t)batch * d.d_model * sizeof(float), 256);
-  return align_up(per, 256) + 2 * xb + yb;
+  return align_up(per, 256) + 2 * xb + 2 * yb;
 }
 
 sffn_status sffn_forward_stack(const sffn_layer_t* layers, int32_t n_layers, const void* x0, int32_t batch,
@@ -440,9 +493,56 @@ sffn_status sffn_forward_stack(const sffn_layer_t* layers, int32_t n_layers, con
   const size_t xbytes = (size_t)batch * d0.d_model * esize;
   const size_t xb = align_up(xbytes, 256);
   unsigned char* xbuf[2] = {base + per, base + per + xb};
-  float* ybuf = reinterpret_cast<float*>(base + per + 2 * xb);
+  const size_t yb = align_up((size_t)batch * d0.d_model * sizeof(float), 256);
+  float* ybufs[2] = {reinterpret_cast<float*>(base + per + 2 * xb), reinterpret_cast<float*>(base + per + 2 * xb + yb)};
+  float* ybuf = ybufs[0];
   unsigned char* trace = static_cast<unsigned char*>(x_trace);
   unsigned char* xo = static_cast<unsigned char*>(x_out);
+
+  bool all_fused = batch == 1;
+  for (int l = 0; l < n_layers; ++l) all_fused = all_fused && layers[l]->fused();
+  if (all_fused) {
+    // Residual + LayerNorm is formed at the start of the next layer's kernel:
+    // the kernel of (step t, layer l) reads the previous layer's input and
+    // output and writes this layer's input.  A last LayerNorm launch closes
+    // the final step.
+    const void* xprev = nullptr;  // input of the previous layer
+    const float* yprev = nullptr;  // output of the previous layer
+    int k = 0;                     // running layer counter (ping-pong index)
+    for (int t = 0; t < n_steps; ++t) {
+      for (int l = 0; l < n_layers; ++l, ++k) {
+        const sffn_layer* L = layers[l];
+        Ws ws;
+        SFFN_TRY(check_ws(L, batch, workspace, per, &ws));
+        float* ycur = ybufs[k & 1];
+        void* xin_store;  // where this layer's input lives
+        if (k == 0) {
+          xin_store = const_cast<void*>(x0);
+          if (trace != nullptr)
+            SFFN_CUDA(cudaMemcpyAsync(trace, x0, xbytes, cudaMemcpyDeviceToDevice, s), "trace copy");
+          SFFN_TRY(run_layer(L, x0, nullptr, nullptr, nullptr, nullptr, 0.f, ycur, nullptr, ws, s));
+        } else {
+          if (l == 0)
+            xin_store = xo + (size_t)(t - 1) * xbytes;  // last step's output is this step's input
+          else if (trace != nullptr)
+            xin_store = trace + ((size_t)t * n_layers + l) * xbytes;
+          else
+            xin_store = xbuf[k & 1];
+          SFFN_TRY(run_layer(L, xprev, yprev, xin_store, ln_gamma, ln_beta, ln_eps, ycur, nullptr, ws, s));
+          if (l == 0 && trace != nullptr)
+            SFFN_CUDA(cudaMemcpyAsync(trace + (size_t)t * n_layers * xbytes, xin_store, xbytes,
+                                      cudaMemcpyDeviceToDevice, s),
+                      "trace copy");
+        }
+        xprev = xin_store;
+        yprev = ycur;
+      }
+    }
+    SFFN_CUDA(launch_residual_layernorm(d0.dtype, xprev, yprev, batch, d0.d_model, ln_gamma, ln_beta, ln_eps,
+                                        xo + (size_t)(n_steps - 1) * xbytes, s),
+              "layernorm launch");
+    return SFFN_OK;
+  }
 
   const void* xin = x0;
   for (int t = 0; t < n_steps; ++t) {

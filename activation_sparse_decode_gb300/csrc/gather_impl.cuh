@@ -35,8 +35,8 @@ __device__ __forceinline__ uint32_t union_word(const GatherArgs& a, int w) {
     const int rem = a.f - w * 32;
     return rem >= 32 ? 0xffffffffu : ((1u << rem) - 1u);
   }
-  uint32_t u = 0;
-  for (int b = 0; b < a.B; ++b) u |= __ldcg(&a.mask[(size_t)b * a.W + w]);
+  uint32_t u = 0;  // the mask is read-only while this kernel runs: the non-coherent path is safe
+  for (int b = 0; b < a.B; ++b) u |= __ldg(&a.mask[(size_t)b * a.W + w]);
   return u;
 }
 
@@ -62,7 +62,8 @@ __global__ void __launch_bounds__(kGatherThreads, 1) k_gather(const GatherArgs a
   unsigned char* stages = smem;
   uint64_t* bars = reinterpret_cast<uint64_t*>(stages + (size_t)S * stage_bytes);
   int32_t* list = reinterpret_cast<int32_t*>(bars + S);
-  uint8_t* tokbits = reinterpret_cast<uint8_t*>(list + a.list_cap);
+  float* sbias = reinterpret_cast<float*>(list + a.list_cap);
+  uint8_t* tokbits = reinterpret_cast<uint8_t*>(sbias + a.list_cap);
 
   if (tid == 0) {
     for (int s = 0; s < S; ++s) mbar_init(&bars[s], 1);
@@ -105,17 +106,15 @@ __global__ void __launch_bounds__(kGatherThreads, 1) k_gather(const GatherArgs a
       uint32_t u = union_word(a, w);
       const int c = __popc(u);
       if (pos + c > k0) {
+        uint32_t tw[4] = {0u, 0u, 0u, 0u};  // this word of each token's mask (B <= 4)
+        for (int b = 0; b < B; ++b) tw[b] = a.dense ? 0xffffffffu : __ldg(&a.mask[(size_t)b * W + w]);
         while (u) {
           const int bit = __ffs(u) - 1;
           u &= u - 1;
           if (pos >= k0 && pos < k1) {
             list[pos - k0] = w * 32 + bit;
             uint32_t tb = 0;
-            if (a.dense) {
-              tb = (1u << B) - 1u;
-            } else {
-              for (int b = 0; b < B; ++b) tb |= ((__ldcg(&a.mask[(size_t)b * W + w]) >> bit) & 1u) << b;
-            }
+            for (int b = 0; b < B; ++b) tb |= ((tw[b] >> bit) & 1u) << b;
             tokbits[pos - k0] = (uint8_t)tb;
           }
           ++pos;
@@ -126,6 +125,7 @@ __global__ void __launch_bounds__(kGatherThreads, 1) k_gather(const GatherArgs a
     }
   }
   __syncthreads();
+  for (int j = tid; j < nloc; j += kGatherThreads) sbias[j] = a.b != nullptr ? __ldg(&a.b[list[j]]) : 0.f;
 
   // ---- start the row pipeline
   const unsigned char* gup = static_cast<const unsigned char*>(a.w_up);
@@ -212,9 +212,8 @@ __global__ void __launch_bounds__(kGatherThreads, 1) k_gather(const GatherArgs a
     // every thread has left iteration j-1, so its stage can be refilled
     if (tid == 0 && j >= 1 && j - 1 + S < nloc) issue(j - 1 + S);
 
-    const int neuron = list[j];
     const uint32_t tb = tokbits[j];
-    const float bias = a.b != nullptr ? __ldg(&a.b[neuron]) : 0.f;
+    const float bias = sbias[j];  // written before the first barrier of the loop
     float act[BT];
 #pragma unroll
     for (int bb = 0; bb < BT; ++bb) {

@@ -71,6 +71,37 @@ bool gather_config(int dtype, int act, int d, int f, int bt, int grid, size_t sm
 cudaError_t launch_gather(int dtype, const GatherConfig& cfg, const GatherArgs& a, int grid,
                           cudaStream_t s);
 
+// ---- one token through one layer in a single launch (predictor + gather)
+struct LayerArgs {
+  const void* x;          // [d] the token, or x_prev when y_prev is given
+  const float* y_prev;    // NULL, or the previous layer's output: x := round(LN(x_prev + y_prev))
+  void* x_ln_out;         // with y_prev: where the formed x is stored ([d], may be NULL)
+  const float* ln_gamma;  // NULL = 1
+  const float* ln_beta;   // NULL = 0
+  float ln_eps;
+  const void* V;          // [r][d]
+  const void* U;          // [f][r]
+  const float* pb;        // [f] predictor bias
+  const float* b;         // NULL or [f] gated bias
+  float tau;
+  const void* w_up;
+  const void* w_gate;
+  const void* w_downT;
+  float* y;               // [d] output, zeroed and accumulated here
+  float* h_part;          // [KS][r] workspace
+  uint32_t* mask;         // NULL or [ceil(f/32)] words, zeroed and set here
+  WsHeader* hdr;
+  int d, f, r, KS, kc, RG, act, nstages, u_smem;
+  size_t region_bytes;
+  uint64_t wait_ns;
+};
+struct LayerConfig {
+  int cpt, nstages, u_smem, KS, kc, RG;
+  size_t region_bytes, smem;
+};
+bool layer_config(int dtype, int act, int d, int f, int r, int grid, size_t smem_optin, LayerConfig* cfg);
+cudaError_t launch_layer(int dtype, const LayerConfig& cfg, const LayerArgs& a, int grid, cudaStream_t s);
+
 // ---- residual + LayerNorm: x_out = round(LN(x + y) * gamma + beta)
 cudaError_t launch_residual_layernorm(int dtype, const void* x, const float* y, int B, int d,
                                       const float* gamma, const float* beta, float eps, void* x_out,

@@ -1,0 +1,8 @@
+// Instantiations of the single-launch decode layer kernel for __nv_bfloat16 weights.
+#include "layer_impl.cuh"
+
+namespace sffn {
+cudaError_t launch_layer_bf16(const LayerConfig& cfg, const LayerArgs& a, int grid, cudaStream_t s) {
+  return layer_dispatch<__nv_bfloat16>(cfg, a, grid, s);
+}
+}  // namespace sffn

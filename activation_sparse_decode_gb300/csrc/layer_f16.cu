@@ -1,0 +1,8 @@
+// Instantiations of the single-launch decode layer kernel for __half weights.
+#include "layer_impl.cuh"
+
+namespace sffn {
+cudaError_t launch_layer_f16(const LayerConfig& cfg, const LayerArgs& a, int grid, cudaStream_t s) {
+  return layer_dispatch<__half>(cfg, a, grid, s);
+}
+}  // namespace sffn

@@ -1,0 +1,8 @@
+// Instantiations of the single-launch decode layer kernel for float weights.
+#include "layer_impl.cuh"
+
+namespace sffn {
+cudaError_t launch_layer_f32(const LayerConfig& cfg, const LayerArgs& a, int grid, cudaStream_t s) {
+  return layer_dispatch<float>(cfg, a, grid, s);
+}
+}  // namespace sffn

@@ -162,7 +162,7 @@ bool gather_config(int dtype, int act, int d, int f, int bt, int grid, size_t sm
   const size_t row_bytes = (size_t)d * esize;
   const size_t stage = (act == kReglu ? 3 : 2) * row_bytes;
   const int list_cap = (f + grid - 1) / grid + 1;
-  const size_t list_bytes = ((size_t)list_cap * 5 + 15) / 16 * 16;
+  const size_t list_bytes = ((size_t)list_cap * 9 + 15) / 16 * 16;  // neuron ids, biases, token bits
   const size_t static_smem = 8 * 1024;  // reduction scratch and scan words
   if (smem_optin < static_smem + list_bytes) return false;
   const size_t budget = smem_optin - static_smem - list_bytes;
@@ -175,6 +175,52 @@ bool gather_config(int dtype, int act, int d, int f, int bt, int grid, size_t sm
   cfg->list_cap = list_cap;
   cfg->smem = s * stage + s * 8 + list_bytes;
   return true;
+}
+
+bool layer_config(int dtype, int act, int d, int f, int r, int grid, size_t smem_optin, LayerConfig* cfg) {
+  const int esize = dtype == kF32 ? 4 : 2;
+  const int E = 16 / esize;
+  const int cpt = round_cpt((d / E + 255) / 256);
+  if (cpt == 0 || cpt * E > 48) return false;  // x and y accumulators live in registers
+  if (r / E > 4 * 32) return false;            // at most 4 chunks of a U row per lane
+  const int rg = (r + 15) / 16;
+  const int unit = 32 * E;
+  const int ks_target = std::max(1, (grid + rg - 1) / rg);
+  int kc = (d + ks_target - 1) / ks_target;
+  kc = (kc + unit - 1) / unit * unit;
+  const int own_cap = (f + grid - 1) / grid;
+  const int nwords = (own_cap + 31) / 32;
+  if (nwords > 256) return false;
+  const size_t stage = (size_t)(act == kReglu ? 3 : 2) * d * esize;
+  const size_t fixed = (size_t)d * esize + (size_t)((r + 3) & ~3) * 4 + 17 * 8 + (size_t)own_cap * 12 + nwords * 4;
+  const size_t reserve = 2048;  // static shared memory of the kernel
+  if (smem_optin < fixed + reserve + 2 * stage) return false;
+  const size_t budget = (smem_optin - fixed - reserve) / 16 * 16;
+  const size_t s = std::min<size_t>(16, budget / stage);
+  const size_t u_bytes = (size_t)own_cap * r * esize;
+  cfg->cpt = cpt;
+  cfg->nstages = (int)s;
+  cfg->u_smem = u_bytes <= budget ? 1 : 0;
+  cfg->RG = rg;
+  cfg->kc = kc;
+  cfg->KS = (d + kc - 1) / kc;
+  cfg->region_bytes = (std::max(s * stage, cfg->u_smem ? u_bytes : 0) + 15) / 16 * 16;
+  cfg->smem = cfg->region_bytes + (size_t)d * esize + (size_t)((r + 3) & ~3) * 4 + (s + 1) * 8 +
+              (size_t)own_cap * 12 + nwords * 4;
+  return cfg->smem + reserve <= smem_optin;
+}
+
+cudaError_t launch_layer_f32(const LayerConfig&, const LayerArgs&, int, cudaStream_t);
+cudaError_t launch_layer_f16(const LayerConfig&, const LayerArgs&, int, cudaStream_t);
+cudaError_t launch_layer_bf16(const LayerConfig&, const LayerArgs&, int, cudaStream_t);
+
+cudaError_t launch_layer(int dtype, const LayerConfig& cfg, const LayerArgs& a, int grid, cudaStream_t s) {
+  switch (dtype) {
+    case kF32: return launch_layer_f32(cfg, a, grid, s);
+    case kF16: return launch_layer_f16(cfg, a, grid, s);
+    case kBF16: return launch_layer_bf16(cfg, a, grid, s);
+  }
+  return cudaErrorInvalidValue;
 }
 
 cudaError_t launch_gather(int dtype, const GatherConfig& cfg, const GatherArgs& a, int grid, cudaStream_t s) {

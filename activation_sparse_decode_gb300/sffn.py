@@ -39,7 +39,9 @@ class sffn_layer_desc(ctypes.Structure):
     _fields_ = [("d_model", _i32), ("d_ff", _i32), ("rank", _i32), ("max_batch", _i32),
                 ("dtype", _i32), ("act", _i32),
                 ("w_up", _vp), ("w_gate", _vp), ("w_downT", _vp), ("b", _vp),
-                ("pred_U", _vp), ("pred_V", _vp), ("pred_b", _vp), ("tau", ctypes.c_float)]
+                ("pred_U", _vp), ("pred_V", _vp), ("pred_b", _vp), ("tau", ctypes.c_float), ("flags", _i32)]
+
+SFFN_FLAG_MULTI_KERNEL = 1
 
 
 def _sig(name, res, *args):
@@ -106,7 +108,8 @@ def _stream(stream) -> ctypes.c_void_p:
 class Layer:
     """A layer handle plus references to the tensors it borrows."""
 
-    def __init__(self, w_up, w_downT, b, U, V, pred_b=None, w_gate=None, tau: float = 0.0, max_batch: int = 1):
+    def __init__(self, w_up, w_downT, b, U, V, pred_b=None, w_gate=None, tau: float = 0.0, max_batch: int = 1,
+                 flags: int = 0):
         self.tensors = [w_up, w_downT, b, U, V, pred_b, w_gate]
         self.act = "reglu" if w_gate is not None else "relu"
         self.dtype = w_up.dtype
@@ -114,7 +117,8 @@ class Layer:
             d_model=w_up.shape[1], d_ff=w_up.shape[0], rank=U.shape[1], max_batch=max_batch,
             dtype=DTYPE_CODES[w_up.dtype], act=ACT_CODES[self.act],
             w_up=_ptr(w_up), w_gate=_ptr(w_gate), w_downT=_ptr(w_downT), b=_ptr(b),
-            pred_U=_ptr(U), pred_V=_ptr(V), pred_b=_ptr(pred_b if pred_b is not None else b), tau=tau)
+            pred_U=_ptr(U), pred_V=_ptr(V), pred_b=_ptr(pred_b if pred_b is not None else b), tau=tau,
+            flags=flags)
         self.desc = desc
         h = ctypes.c_void_p()
         _check(_c["create"](ctypes.byref(desc), ctypes.byref(h)))
@@ -122,10 +126,10 @@ class Layer:
         self.d_model, self.d_ff, self.rank, self.max_batch = desc.d_model, desc.d_ff, desc.rank, max_batch
 
     @classmethod
-    def from_weights(cls, lw, tau: float = 0.0, max_batch: int = 1) -> "Layer":
+    def from_weights(cls, lw, tau: float = 0.0, max_batch: int = 1, flags: int = 0) -> "Layer":
         """From a workloads.LayerWeights already on the GPU."""
         return cls(lw.w_up, lw.w_downT, lw.b, lw.U, lw.V, pred_b=lw.b, w_gate=lw.w_gate, tau=tau,
-                   max_batch=max_batch)
+                   max_batch=max_batch, flags=flags)
 
     def close(self):
         if getattr(self, "handle", None):

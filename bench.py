@@ -233,7 +233,7 @@ def bench_sffn(args):
     pgraph = torch.cuda.CUDAGraph()
     with torch.cuda.graph(pgraph, stream=stream):
         step_body(prof_events)
-    launches_per_step = 3 * T  # predictor hidden, predictor scores, fused gather per token
+    launches_per_step = T  # one single-launch layer kernel per token
 
     # ---- device-timed steps (inputs resident in HBM); every replay and event on `stream`
     with torch.cuda.stream(stream):
@@ -272,9 +272,11 @@ def bench_sffn(args):
     dur /= reps_k  # ms per launch, per token
     esz = 2
     gathered = n_tok * wl.d_model * esz * 2  # rows of W_up and W_down^T
-    algo = gathered + wl.d_model * esz + wl.d_model * 4  # + x read + y written
+    pred_bytes = (wl.rank * wl.d_model + wl.d_ff * wl.rank) * esz + 2 * wl.d_ff * 4  # V, U, both biases
+    algo = gathered + pred_bytes + wl.d_model * esz + wl.d_model * 4  # + x read + y written
     k_avg_ms = float(dur.mean())
     achieved_gbs = float(algo.mean()) / (k_avg_ms / 1e3) / 1e9
+    gathered_gbs = float(gathered.mean()) / (k_avg_ms / 1e3) / 1e9
     peaks = measured_peaks()
     peak = peaks["hbm_gbs"] if peaks else 6800.0
     traffic = None
@@ -284,8 +286,6 @@ def bench_sffn(args):
         if tj.get("kernel_source_hash") == kernel_source_hash():
             traffic = tj.get("bytes_per_launch")
 
-    # per-token predictor bytes (reported, not in the roofline figure)
-    pred_bytes = (wl.rank * wl.d_model + wl.d_ff * wl.rank) * esz + wl.d_ff * 4
 
     # ---- end to end: pinned host tokens in, host outputs back, every step
     Xh = X.cpu().pin_memory()
@@ -335,12 +335,14 @@ def bench_sffn(args):
                   f"reuse distance ~{R * 37} MB per token vs {L2_BYTES // 2**20} MB L2",
             "mean_active": round(float(n_tok.mean()), 1),
             "us_per_layer": round(ms_per_step * 1e3 / T, 3),
-            "gather_us_per_launch": round(k_avg_ms * 1e3, 3),
+            "layer_kernel_us_per_launch": round(k_avg_ms * 1e3, 3),
             "predictor_bytes_per_token": int(pred_bytes),
+            "gathered_bytes_per_token": round(float(gathered.mean())),
+            "gathered_gbs_over_launch": round(gathered_gbs, 1),
             "parallelism": f"replicas x{world}" if world > 1 else "single GPU",
         },
         "roofline": {
-            "kernel": "k_gather (fused row gather + ReLU + down projection)",
+            "kernel": "k_layer (predictor, threshold, row gather, ReLU, down projection: one launch per token)",
             "bound": "hbm",
             "achieved": round(achieved_gbs, 1),
             "peak": peak,
@@ -370,7 +372,7 @@ def kernel_source_hash():
     import hashlib
     h = hashlib.sha256()
     csrc = os.path.join(ROOT, "activation_sparse_decode_gb300", "csrc")
-    for name in ("gather_impl.cuh", "common.cuh", "kernels.cuh"):
+    for name in ("layer_impl.cuh", "common.cuh", "kernels.cuh"):
         h.update(open(os.path.join(csrc, name), "rb").read())
     return h.hexdigest()[:16]
 

@@ -92,7 +92,14 @@ typedef struct {
   const void* pred_V;   /* [rank][d_model]                                  */
   const float* pred_b;  /* [d_ff] predictor bias                            */
   float tau;            /* threshold: neuron i is active iff s_i > tau      */
+  int32_t flags;        /* SFFN_FLAG_* bits, 0 for the defaults            */
 } sffn_layer_desc;
+
+/* Batch-1 calls normally run the whole layer (predictor, threshold, gather,
+ * activation, down projection) as one kernel launch; this flag selects the
+ * multi-kernel path (separate predictor, score and gather kernels) that larger
+ * batches use, with its deterministic cross-block reduction. */
+#define SFFN_FLAG_MULTI_KERNEL 1
 
 /* Validates the descriptor and records it with launch settings chosen for the
  * current device.  Allocates only host memory.  Returns INVALID_ARG for bad

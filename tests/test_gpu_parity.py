@@ -43,10 +43,14 @@ def run_tokens(sffn, layer, X, want_idx=True):
 
 # ---------------------------------------------------------------- ReLU FFN d1024 f4096 fp32 (64 tokens)
 
-def test_c1_every_token(sffn):
+PATHS = {"fused": 0, "multi": 1}  # single-launch layer kernel vs separate predictor/score/gather kernels
+
+
+@pytest.mark.parametrize("path", list(PATHS))
+def test_c1_every_token(sffn, path):
     wl = W.get_workload("c1")
     lw = W.make_layer(wl, device=DEV)
-    layer = sffn.Layer.from_weights(lw, tau=wl.tau)
+    layer = sffn.Layer.from_weights(lw, tau=wl.tau, flags=PATHS[path])
     ol = oracle_layer(lw, wl.tau)
     X = W.make_tokens(wl, wl.steps, device=DEV)
     Y, I, N = run_tokens(sffn, layer, X)
@@ -94,6 +98,13 @@ def test_c2_full_size_sampled(sffn):
     layer = sffn.Layer.from_weights(lw, tau=wl.tau)
     X = W.make_tokens(wl, wl.steps, device=DEV)
     Y, I, N = run_tokens(sffn, layer, X)
+    # the multi-kernel path on the first tokens agrees with the fused one
+    multi = sffn.Layer.from_weights(lw, tau=wl.tau, flags=PATHS["multi"])
+    Ym, Im, Nm = run_tokens(sffn, multi, X[:16])
+    assert np.array_equal(Nm, N[:16])
+    for t in range(16):
+        assert np.array_equal(Im[t, 0, :Nm[t, 0]], I[t, 0, :N[t, 0]])
+        assert rel_l2(Ym[t, 0], Y[t, 0]) < 1e-5
     ol = oracle_layer(lw, wl.tau)
     Xh = st(X)
     rng = np.random.Generator(np.random.PCG64(7))
@@ -151,8 +162,13 @@ def test_dense_forward_matches_oracle(sffn, c3):
         assert rel_l2(Y[b], oracle.dense_ffn(ol, Xh[b])) < TOL[wl.dtype]
 
 
-SMALL = [  # (d_model, d_ff, rank, dtype, act, batch)
+SMALL = [  # (d_model, d_ff, rank, dtype, act, batch); batch-1 shapes run both paths
     (256, 1000, 32, "f16", "relu", 1),
+    (1000, 777, 8, "f16", "relu", 1),
+    (8, 64, 8, "bf16", "reglu", 1),
+    (512, 333, 16, "f32", "reglu", 1),
+    (12288, 500, 1024, "f16", "relu", 1),
+    (2048, 6000, 384, "bf16", "reglu", 1),
     (1000, 777, 8, "f16", "relu", 3),
     (8, 64, 8, "bf16", "reglu", 2),
     (64, 40, 4, "f32", "relu", 1),
@@ -161,13 +177,16 @@ SMALL = [  # (d_model, d_ff, rank, dtype, act, batch)
 ]
 
 
+@pytest.mark.parametrize("path", list(PATHS))
 @pytest.mark.parametrize("shape", SMALL, ids=lambda s: "d%d_f%d_r%d_%s_%s_b%d" % s)
-def test_ragged_small_layers(sffn, shape):
+def test_ragged_small_layers(sffn, shape, path):
     d, f, r, dt, act, batch = shape
+    if path == "fused" and batch > 1:
+        pytest.skip("the single-launch layer kernel serves batch 1")
     wl = W.tiny_workload(d_model=d, d_ff=f, rank=r, dtype=dt, act=act, mean_p=0.2, name=f"ragged{shape}")
     lw = W.make_layer(wl, device=DEV)
     ol = oracle_layer(lw)
-    layer = sffn.Layer.from_weights(lw, max_batch=batch)
+    layer = sffn.Layer.from_weights(lw, max_batch=batch, flags=PATHS[path])
     X = W.make_tokens(wl, 3, batch=batch, device=DEV)
     Y, I, N = run_tokens(sffn, layer, X)
     Xh = st(X)
@@ -177,13 +196,14 @@ def test_ragged_small_layers(sffn, shape):
             check_token(ol, Xh[s, b], m, Y[s, b], TOL[dt])
 
 
+@pytest.mark.parametrize("batch", [1, 2])
 @pytest.mark.parametrize("tau,expect", [(1e30, "none"), (-1e30, "all")])
-def test_all_false_and_all_true_masks(sffn, tau, expect):
+def test_all_false_and_all_true_masks(sffn, tau, expect, batch):
     wl = W.tiny_workload(d_model=512, d_ff=1500, rank=32, dtype="f16", name="degenerate")
     lw = W.make_layer(wl, device=DEV)
     ol = oracle_layer(lw, tau)
     layer = sffn.Layer.from_weights(lw, tau=tau, max_batch=2)
-    X = W.make_tokens(wl, 2, batch=2, device=DEV)
+    X = W.make_tokens(wl, 2, batch=batch, device=DEV)
     Y, I, N = run_tokens(sffn, layer, X)
     if expect == "none":
         assert (N == 0).all()
@@ -192,11 +212,13 @@ def test_all_false_and_all_true_masks(sffn, tau, expect):
         assert (N == wl.d_ff).all()
         Xh = st(X)
         for s in range(2):
-            for b in range(2):
+            for b in range(batch):
                 assert rel_l2(Y[s, b], oracle.dense_ffn(ol, Xh[s, b])) < TOL["f16"]
 
 
 def test_deterministic_run_to_run(sffn, c3):
+    """The multi-kernel path reduces block partials in a fixed order (the
+    single-launch kernel adds them with float atomics instead)."""
     wl, lw, _ = c3
     layer = sffn.Layer.from_weights(lw, max_batch=4)
     X = W.make_tokens(wl, 1, batch=4, device=DEV)

@@ -72,6 +72,20 @@ def teacher_forced(sffn, wl, lws, layers, x_out, trace, pairs, tokens):
             check_next_input(nh_next[b], want, wl.dtype)
 
 
+@pytest.mark.parametrize("flags", [0, 1], ids=["fused", "multi"])
+def test_small_stack_both_paths(sffn, flags):
+    wl = W.tiny_workload(d_model=512, d_ff=2048, rank=64, dtype="bf16", name="small-stack").with_(n_layers=3)
+    lws = [W.make_layer(wl, layer=l, device=DEV) for l in range(3)]
+    layers = [sffn.Layer.from_weights(lw, max_batch=1, flags=flags) for lw in lws]
+    x0 = W.make_tokens(wl, 1, device=DEV)[0]
+    x_out, trace = run_stack(sffn, layers, x0, 4)
+    assert torch.equal(trace[0, 0], x0)
+    for t in range(1, 4):
+        assert torch.equal(trace[t, 0], x_out[t - 1])
+    pairs = [(t, l) for t in range(4) for l in range(3)]
+    teacher_forced(sffn, wl, lws, layers, x_out, trace, pairs, [0])
+
+
 def test_opt13b_stack40_fp16(sffn):
     wl = W.get_workload("c4")
     lws, layers = build_stack(sffn, wl, wl.n_layers, 1)

@@ -201,4 +201,14 @@ __device__ __forceinline__ uint64_t policy_evict_normal() {
   return p;
 }
 
+// Raises a kernel's dynamic shared-memory limit when a launch needs more than
+// any earlier launch of it did (`cur` is that kernel's high-water mark).
+template <typename F>
+inline cudaError_t ensure_dyn_smem(F* func, size_t bytes, int* cur) {
+  if ((int)bytes <= *cur) return cudaSuccess;
+  const cudaError_t e = cudaFuncSetAttribute(func, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)bytes);
+  if (e == cudaSuccess) *cur = (int)bytes;
+  return e;
+}
+
 }  // namespace sffn

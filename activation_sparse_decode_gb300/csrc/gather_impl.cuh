@@ -299,13 +299,9 @@ __global__ void __launch_bounds__(kGatherThreads, 1) k_gather(const GatherArgs a
 
 template <typename T, int BT, int CPT>
 cudaError_t gather_launch(const GatherConfig& cfg, const GatherArgs& a, int grid, cudaStream_t s) {
-  static bool attr = false;
-  if (!attr) {
-    cudaError_t e = cudaFuncSetAttribute(k_gather<T, BT, CPT>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                         (int)cfg.smem);
-    if (e != cudaSuccess) return e;
-    attr = true;
-  }
+  static int cur = 48 * 1024;
+  const cudaError_t e = ensure_dyn_smem(k_gather<T, BT, CPT>, cfg.smem, &cur);
+  if (e != cudaSuccess) return e;
   k_gather<T, BT, CPT><<<grid, kGatherThreads, cfg.smem, s>>>(a);
   return cudaGetLastError();
 }

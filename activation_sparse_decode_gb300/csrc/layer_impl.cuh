@@ -430,12 +430,9 @@ __global__ void __launch_bounds__(kLayerThreads, 1) k_layer(const LayerArgs a) {
 
 template <typename T, int CPT>
 cudaError_t layer_launch(const LayerConfig& cfg, const LayerArgs& a, int grid, cudaStream_t s) {
-  static bool attr = false;
-  if (!attr) {
-    cudaError_t e = cudaFuncSetAttribute(k_layer<T, CPT>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)cfg.smem);
-    if (e != cudaSuccess) return e;
-    attr = true;
-  }
+  static int cur = 48 * 1024;
+  const cudaError_t e = ensure_dyn_smem(k_layer<T, CPT>, cfg.smem, &cur);
+  if (e != cudaSuccess) return e;
   k_layer<T, CPT><<<grid, kLayerThreads, cfg.smem, s>>>(a);
   return cudaGetLastError();
 }

@@ -259,11 +259,9 @@ template <typename T, int BT>
 cudaError_t hidden_launch(const PredHiddenArgs& a, cudaStream_t s) {
   const dim3 grid(a.KS, pred_hidden_row_groups(a.r), (a.B + BT - 1) / BT);
   const size_t smem = (size_t)BT * a.kc_elems * sizeof(T);
-  static bool attr = false;
-  if (!attr) {
-    cudaFuncSetAttribute(k_pred_hidden<T, BT>, cudaFuncAttributeMaxDynamicSharedMemorySize, 200 * 1024);
-    attr = true;
-  }
+  static int cur = 48 * 1024;
+  const cudaError_t e = ensure_dyn_smem(k_pred_hidden<T, BT>, smem, &cur);
+  if (e != cudaSuccess) return e;
   k_pred_hidden<T, BT><<<grid, kHiddenWarps * 32, smem, s>>>(
       static_cast<const T*>(a.V), static_cast<const T*>(a.x), a.B, a.r, a.d, a.kc_elems, a.KS,
       a.h_part, a.h, a.tickets);
@@ -282,11 +280,9 @@ template <typename T, int CPL, int BT>
 cudaError_t score_launch(const PredScoreArgs& a, cudaStream_t s) {
   const dim3 grid(a.grid, (a.B + BT - 1) / BT);
   const size_t smem = (size_t)BT * a.r * sizeof(float);
-  static bool attr = false;
-  if (!attr) {
-    cudaFuncSetAttribute(k_pred_score<T, CPL, BT>, cudaFuncAttributeMaxDynamicSharedMemorySize, 200 * 1024);
-    attr = true;
-  }
+  static int cur = 48 * 1024;
+  const cudaError_t e = ensure_dyn_smem(k_pred_score<T, CPL, BT>, smem, &cur);
+  if (e != cudaSuccess) return e;
   k_pred_score<T, CPL, BT><<<grid, kScoreWarps * 32, smem, s>>>(
       static_cast<const T*>(a.U), a.h, a.pb, a.tau, a.B, a.f, a.r, a.W, a.mask, a.scores);
   return cudaGetLastError();

@@ -64,7 +64,7 @@ size_t align_up(size_t v, size_t a) { return (v + a - 1) / a * a; }
 int bt_slot(int bt) { return bt == 1 ? 0 : bt == 2 ? 1 : 2; }
 
 struct WsLayout {
-  size_t hdr, tickets, h_part, h, mask, y_part, hl_part, total;
+  size_t hdr, flags, tickets, h_part, h, mask, y_part, hl_part, total;
 };
 
 WsLayout layout(const sffn_layer* L, int batch) {
@@ -77,6 +77,7 @@ WsLayout layout(const sffn_layer* L, int batch) {
     return o;
   };
   w.hdr = take(sizeof(WsHeader));
+  w.flags = take(barrier_flag_bytes((uint32_t)L->gather_grid));
   w.tickets = take((size_t)L->RG * batch * sizeof(uint32_t));
   w.h_part = take((size_t)L->KS * batch * d.rank * sizeof(float));
   w.h = take((size_t)batch * d.rank * sizeof(float));
@@ -91,6 +92,7 @@ struct Ws {
   WsLayout lay;
   unsigned char* base;
   WsHeader* hdr() const { return reinterpret_cast<WsHeader*>(base + lay.hdr); }
+  uint32_t* flags() const { return reinterpret_cast<uint32_t*>(base + lay.flags); }
   uint32_t* tickets() const { return reinterpret_cast<uint32_t*>(base + lay.tickets); }
   float* h_part() const { return reinterpret_cast<float*>(base + lay.h_part); }
   float* h() const { return reinterpret_cast<float*>(base + lay.h); }
@@ -183,6 +185,7 @@ sffn_status run_gather(const sffn_layer* L, const void* x, int batch, float* y, 
     a.y = y + (size_t)b0 * d.d_model;
     a.y_part = ws.y_part();
     a.hdr = ws.hdr();
+    a.bar_flags = ws.flags();
     a.B = nb;
     a.d = d.d_model;
     a.f = d.d_ff;
@@ -225,6 +228,7 @@ sffn_status run_layer(const sffn_layer* L, const void* x, const float* y_prev, v
   a.h_part = ws.hl_part();
   a.mask = mask;
   a.hdr = ws.hdr();
+  a.bar_flags = ws.flags();
   a.d = d.d_model;
   a.f = d.d_ff;
   a.r = d.rank;
@@ -235,6 +239,9 @@ sffn_status run_layer(const sffn_layer* L, const void* x, const float* y_prev, v
   a.nstages = L->lcfg.nstages;
   a.u_smem = L->lcfg.u_smem;
   a.region_bytes = L->lcfg.region_bytes;
+  a.u_off = L->lcfg.u_off;
+  a.hot_rows = d.hot_rows;
+  a.hot_stages = L->lcfg.hot_stages;
   a.wait_ns = (uint64_t)g_wait_ns;
   if (g_prof_start != nullptr) SFFN_TRY(record_profile_event(g_prof_start, s));
   SFFN_CUDA(launch_layer(d.dtype, L->lcfg, a, L->gather_grid, s), "layer launch");
@@ -302,6 +309,7 @@ sffn_status sffn_create_layer(const sffn_layer_desc* desc, sffn_layer_t* out) {
     return fail(SFFN_ERR_INVALID_ARG, "w_gate must be NULL for ReLU layers");
   }
   if (d.rank / (16 / esize) > 256) return fail(SFFN_ERR_UNSUPPORTED, "rank too large for the score kernel");
+  if (d.hot_rows < 0 || d.hot_rows > d.d_ff) return fail(SFFN_ERR_INVALID_ARG, "hot_rows outside [0, d_ff]");
 
   sffn_layer* L = new (std::nothrow) sffn_layer();
   if (L == nullptr) return fail(SFFN_ERR_INVALID_ARG, "out of host memory");
@@ -622,7 +630,7 @@ sffn_status sffn_read_device_status(void* workspace, int32_t* status, void* stre
     // clear the status; after a timeout the barrier words may be mid-generation
     WsHeader z;
     std::memset(&z, 0, sizeof(z));
-    z.bar_gen = h.bar_gen;
+
     SFFN_CUDA(cudaMemcpyAsync(workspace, &z, sizeof(z), cudaMemcpyHostToDevice, s), "status clear");
     SFFN_CUDA(cudaStreamSynchronize(s), "status clear sync");
   }
@@ -631,9 +639,12 @@ sffn_status sffn_read_device_status(void* workspace, int32_t* status, void* stre
 
 sffn_status sffn_debug_wait_timeout(void* workspace, size_t ws_bytes, int64_t timeout_ns, void* stream) {
   g_err.clear();
-  if (workspace == nullptr || ws_bytes < sizeof(WsHeader)) return fail(SFFN_ERR_WORKSPACE, "workspace too small");
+  if (workspace == nullptr || ws_bytes < sizeof(WsHeader) + barrier_flag_bytes(2))
+    return fail(SFFN_ERR_WORKSPACE, "workspace too small");
   if (timeout_ns <= 0 || timeout_ns > 10000000000LL) return fail(SFFN_ERR_INVALID_ARG, "timeout out of range");
-  SFFN_CUDA(launch_wait_timeout(static_cast<WsHeader*>(workspace), (uint64_t)timeout_ns,
+  SFFN_CUDA(launch_wait_timeout(static_cast<WsHeader*>(workspace),
+                                reinterpret_cast<uint32_t*>(static_cast<unsigned char*>(workspace) + sizeof(WsHeader)),
+                                (uint64_t)timeout_ns,
                                 static_cast<cudaStream_t>(stream)),
             "wait launch");
   return SFFN_OK;

@@ -16,7 +16,7 @@ struct WsHeader {
   uint32_t status;     // first device-side error (sticky until read)
   uint32_t detail;     // where it happened (kernel-specific code)
   uint32_t bar_count;  // grid barrier: arrivals in the current generation
-  uint32_t bar_gen;    // grid barrier: generation counter
+  uint32_t reserved;
   uint32_t pad[60];
 };
 static_assert(sizeof(WsHeader) == 256, "workspace header is 256 bytes");
@@ -101,36 +101,69 @@ __device__ __forceinline__ void st_release_gpu(uint32_t* p, uint32_t v) {
   asm volatile("st.release.gpu.global.u32 [%0], %1;" ::"l"(p), "r"(v) : "memory");
 }
 
-// Grid-wide barrier over `expected` resident blocks (sense reversal through a
-// generation word, so it needs no reset between uses).  Every wait is bounded:
-// after limit_ns the block records kStTimeout and returns false instead of
-// spinning on.  All threads of the block must call it.
-__device__ __forceinline__ bool grid_barrier(WsHeader* h, uint32_t expected, uint64_t limit_ns,
+// Grid-wide barrier over `expected` resident blocks.
+//
+// Arrival is two-level: blocks arrive on the counter of their group of
+// kBarGroup blocks, and the last block of each group arrives on the top
+// counter (h->bar_count), so no counter takes more than ~20 same-address
+// atomics.  Release is per block: every block waits on its own flag word, one
+// 128-byte line each, and the last block to arrive stores the next generation
+// into all of them, so no two blocks poll the same line and the release store
+// does not queue behind pollers.  All flags hold the same generation, so a
+// block reads its own flag before arriving to learn the value it waits to
+// change.  Layout of `flags` (32-word stride): [expected] release flags, then
+// [ceil(expected / kBarGroup)] group counters.
+//
+// Every wait is bounded: after limit_ns the block records kStTimeout and
+// returns false (the counters are then left mid-count; zero the workspace
+// before reusing it).  All threads of the block must call it.
+constexpr uint32_t kBarGroup = 8;
+
+__host__ __device__ constexpr size_t barrier_flag_bytes(uint32_t blocks) {
+  return ((size_t)blocks + (blocks + kBarGroup - 1) / kBarGroup) * 128;
+}
+
+__device__ __forceinline__ bool grid_barrier(WsHeader* h, uint32_t* flags, uint32_t expected, uint64_t limit_ns,
                                              uint32_t detail) {
-  __shared__ int s_ok;
+  __shared__ int s_ok, s_last;
+  __shared__ uint32_t s_gen;
+  uint32_t* mine = flags + (size_t)blockIdx.x * 32;
   __syncthreads();
   if (threadIdx.x == 0) {
-    int ok = 1;
-    const uint32_t gen = ld_acquire_gpu(&h->bar_gen);  // read before arriving
-    __threadfence();                                     // publish this block's writes
-    const uint32_t old = atomicAdd(&h->bar_count, 1u);
-    if (old == expected - 1) {
-      atomicExch(&h->bar_count, 0u);
+    const uint32_t gen = ld_acquire_gpu(mine);  // read before arriving
+    __threadfence();                             // publish this block's writes
+    const uint32_t grp = blockIdx.x / kBarGroup;
+    const uint32_t ngroups = (expected + kBarGroup - 1) / kBarGroup;
+    const uint32_t in_grp = min(kBarGroup, expected - grp * kBarGroup);
+    uint32_t* gcount = flags + ((size_t)expected + grp) * 32;
+    int last = 0;
+    if (atomicAdd(gcount, 1u) == in_grp - 1) {
+      atomicExch(gcount, 0u);
       __threadfence();
-      st_release_gpu(&h->bar_gen, gen + 1u);
-    } else {
-      const uint64_t t0 = globaltimer_ns();
-      while (ld_acquire_gpu(&h->bar_gen) == gen) {
-        __nanosleep(32);
-        if (globaltimer_ns() - t0 > limit_ns) {
-          set_status(h, kStTimeout, detail);
-          ok = 0;
-          break;
-        }
+      if (atomicAdd(&h->bar_count, 1u) == ngroups - 1) {
+        atomicExch(&h->bar_count, 0u);  // reset before any block can be released
+        __threadfence();
+        last = 1;
+      }
+    }
+    s_gen = gen;
+    s_last = last;
+    s_ok = 1;
+  }
+  __syncthreads();
+  if (s_last) {
+    __threadfence();
+    for (uint32_t b = threadIdx.x; b < expected; b += blockDim.x) st_release_gpu(flags + (size_t)b * 32, s_gen + 1u);
+  } else if (threadIdx.x == 0) {
+    const uint64_t t0 = globaltimer_ns();
+    while (ld_acquire_gpu(mine) == s_gen) {
+      if (globaltimer_ns() - t0 > limit_ns) {
+        set_status(h, kStTimeout, detail);
+        s_ok = 0;
+        break;
       }
     }
     __threadfence();
-    s_ok = ok;
   }
   __syncthreads();
   return s_ok != 0;
@@ -188,6 +221,24 @@ __device__ __forceinline__ void bulk_g2s(void* dst, const void* src, uint32_t by
       "[%0], [%1], %2, [%3], %4;" ::"r"(smem_addr(dst)),
       "l"(src), "r"(bytes), "r"(smem_addr(bar)), "l"(policy)
       : "memory");
+}
+
+// Per-thread 16-byte asynchronous copy global -> shared (L1 bypassed), many in
+// flight per thread without registers; completion per thread via wait_all.
+__device__ __forceinline__ void cp_async16(void* smem_dst, const void* src) {
+  asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(smem_addr(smem_dst)), "l"(src) : "memory");
+}
+__device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commit_group;" ::: "memory"); }
+__device__ __forceinline__ void cp_async_wait_all() { asm volatile("cp.async.wait_all;" ::: "memory"); }
+
+// The mbarrier receives one arrival once every cp.async this thread issued
+// before it has landed (the barrier's expected count includes the arrival).
+__device__ __forceinline__ void cp_async_arrive_noinc(uint64_t* bar) {
+  asm volatile("cp.async.mbarrier.arrive.noinc.shared::cta.b64 [%0];" ::"r"(smem_addr(bar)) : "memory");
+}
+
+__device__ __forceinline__ void prefetch_l2(const void* p) {
+  asm volatile("prefetch.global.L2 [%0];" ::"l"(p));
 }
 
 __device__ __forceinline__ uint64_t policy_evict_first() {

@@ -266,7 +266,7 @@ __global__ void __launch_bounds__(kGatherThreads, 1) k_gather(const GatherArgs a
       }
     }
   if (G == 1) return;
-  if (!grid_barrier(a.hdr, (uint32_t)G, a.wait_ns, 0x200u)) return;
+  if (!grid_barrier(a.hdr, a.bar_flags, (uint32_t)G, a.wait_ns, 0x200u)) return;
 
   const int N4 = B * d / 4;
   const float4* yp4 = reinterpret_cast<const float4*>(a.y_part);

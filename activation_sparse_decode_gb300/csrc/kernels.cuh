@@ -53,6 +53,7 @@ struct GatherArgs {
   float* y;             // [B][d]
   float* y_part;        // [grid][B][d] per-block partial outputs (workspace)
   WsHeader* hdr;
+  uint32_t* bar_flags;  // [grid] grid-barrier release flags, 128 bytes apart (workspace)
   int B, d, f, W;
   int act;              // Act
   int dense;            // 1: every neuron (no predictor)
@@ -91,13 +92,17 @@ struct LayerArgs {
   float* h_part;          // [KS][r] workspace
   uint32_t* mask;         // NULL or [ceil(f/32)] words, zeroed and set here
   WsHeader* hdr;
+  uint32_t* bar_flags;    // [grid] grid-barrier release flags, 128 bytes apart
   int d, f, r, KS, kc, RG, act, nstages, u_smem;
+  int hot_rows;           // neurons [0, hot_rows) are prefetched before the predictor decides
+  int hot_stages;         // ring stages free of the U rows, usable for that prefetch
   size_t region_bytes;
+  size_t u_off;           // offset of the staged U rows inside the region
   uint64_t wait_ns;
 };
 struct LayerConfig {
-  int cpt, nstages, u_smem, KS, kc, RG;
-  size_t region_bytes, smem;
+  int cpt, nstages, u_smem, KS, kc, RG, hot_stages;
+  size_t region_bytes, u_off, smem;
 };
 bool layer_config(int dtype, int act, int d, int f, int r, int grid, size_t smem_optin, LayerConfig* cfg);
 cudaError_t launch_layer(int dtype, const LayerConfig& cfg, const LayerArgs& a, int grid, cudaStream_t s);
@@ -112,6 +117,6 @@ cudaError_t launch_permute_rows(const void* src, void* dst, const int32_t* perm,
                                 int64_t row_bytes, cudaStream_t s);
 
 // ---- test hook: a barrier wait that cannot complete
-cudaError_t launch_wait_timeout(WsHeader* hdr, uint64_t limit_ns, cudaStream_t s);
+cudaError_t launch_wait_timeout(WsHeader* hdr, uint32_t* flags, uint64_t limit_ns, cudaStream_t s);
 
 }  // namespace sffn

@@ -34,8 +34,19 @@
 
 namespace sffn {
 
+// Phase timestamps for profiling builds (compiled out unless SFFN_PHASE_TRACE
+// is defined, in which case the including file provides sffn_phase_trace()).
+#ifdef SFFN_PHASE_TRACE
+#define SFFN_TRACE(k) sffn_phase_trace(k)
+#define SFFN_TRACE_VAL(k, v) sffn_phase_value(k, v)
+#else
+#define SFFN_TRACE(k) ((void)0)
+#define SFFN_TRACE_VAL(k, v) ((void)0)
+#endif
+
 constexpr int kLayerThreads = 256;
 constexpr int kLayerWarps = kLayerThreads / 32;
+constexpr int kGroup = 4;  // neurons per block-wide reduction in the row ring
 
 __device__ __forceinline__ void bulk_prefetch_l2(const void* src, uint32_t bytes) {
   asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(src), "r"(bytes) : "memory");
@@ -79,7 +90,7 @@ __global__ void __launch_bounds__(kLayerThreads, 1) k_layer(const LayerArgs a) {
   constexpr int E = Chunk<T>::N;
   constexpr int ES = sizeof(T);
   extern __shared__ __align__(128) unsigned char smem[];
-  __shared__ float s_red[2][kLayerWarps][2];
+  __shared__ float s_red[2][kLayerWarps][kGroup][2];
   __shared__ float s_warp[kLayerWarps];
   __shared__ int s_nloc;
 
@@ -107,19 +118,57 @@ __global__ void __launch_bounds__(kLayerThreads, 1) k_layer(const LayerArgs a) {
   float* ownpb = ownb + own_cap;
   uint32_t* words = reinterpret_cast<uint32_t*>(ownpb + own_cap);
   int32_t* list = reinterpret_cast<int32_t*>(words + nwords);
-  uint64_t* ubar = bars + S;
+  SFFN_TRACE(0);
 
   // ---- phase 0: start every independent stream, zero the outputs
-  if (tid == 0) {
-    for (int s = 0; s <= S; ++s) mbar_init(&bars[s], 1);
-    fence_mbar_init();
-    if (a.u_smem && n_own > 0) {
-      const uint64_t pol = policy_evict_first();
-      mbar_arrive_expect_tx(ubar, (uint32_t)n_own * urow_bytes);
-      const unsigned char* U = static_cast<const unsigned char*>(a.U);
-      for (int j = 0; j < n_own; ++j)
-        bulk_g2s(region + (size_t)j * urow_bytes, U + (size_t)(c + (size_t)j * G) * urow_bytes, urow_bytes, ubar, pol);
+  if (a.y_prev == nullptr) {  // the token itself first: everything in phase 1 waits on it
+    const uint4* xg = static_cast<const uint4*>(a.x);
+    for (int ch = tid; ch < NCH; ch += kLayerThreads) cp_async16(reinterpret_cast<uint4*>(xs) + ch, xg + ch);
+  }
+  cp_async_commit();  // group 1: x
+  const unsigned char* Ub = static_cast<const unsigned char*>(a.U);
+  if (a.u_smem) {  // owned U rows -> shared memory, 16 bytes per copy over all threads
+    const int total = n_own * NC;
+    for (int q = tid; q < total; q += kLayerThreads) {
+      const int j = q / NC, ch = q - j * NC;
+      cp_async16(region + a.u_off + (size_t)j * urow_bytes + ch * 16,
+                 Ub + (size_t)(c + (size_t)j * G) * urow_bytes + ch * 16);
     }
+  } else {  // too large to stage: warm L2 with the owned rows instead
+    const int lines = (urow_bytes + 127) / 128;
+    for (int q = tid; q < n_own * lines; q += kLayerThreads) {
+      const int j = q / lines, l = q - j * lines;
+      prefetch_l2(Ub + (size_t)(c + (size_t)j * G) * urow_bytes + l * 128);
+    }
+  }
+  cp_async_commit();  // group 2: U rows
+  // hot rows: the first owned neurons under the hot-first order are almost
+  // always active, so their rows start streaming before the predictor decides
+  const int n_hot = c < a.hot_rows ? min(a.hot_stages, min(n_own, (a.hot_rows - c + G - 1) / G)) : 0;
+  const unsigned char* gup = static_cast<const unsigned char*>(a.w_up);
+  const unsigned char* ggt = static_cast<const unsigned char*>(a.w_gate);
+  const unsigned char* gdn = static_cast<const unsigned char*>(a.w_downT);
+  // Owned row j into stage s: every thread copies its own 16-byte chunks (the
+  // same chunks it later reads, so no thread waits on another's data) and
+  // arrives on the stage barrier when they have landed.  Expected arrivals per
+  // phase: one per thread.
+  auto fill = [&](int s, int j) {
+    const size_t off = (size_t)(c + (size_t)j * G) * row_bytes;
+    unsigned char* dst = region + (size_t)s * stage_bytes;
+#pragma unroll
+    for (int cq = 0; cq < CPT; ++cq) {
+      const int ch = tid + cq * kLayerThreads;
+      if (ch < NCH) {
+        cp_async16(dst + (size_t)ch * 16, gup + off + (size_t)ch * 16);
+        if (reglu) cp_async16(dst + row_bytes + (size_t)ch * 16, ggt + off + (size_t)ch * 16);
+        cp_async16(dst + (size_t)(nrows - 1) * row_bytes + (size_t)ch * 16, gdn + off + (size_t)ch * 16);
+      }
+    }
+    cp_async_arrive_noinc(&bars[s]);
+  };
+  if (tid == 0) {
+    for (int s = 0; s < S; ++s) mbar_init(&bars[s], kLayerThreads);
+    fence_mbar_init();
   }
   {  // L2 prefetch of this block's V tiles (one row segment per thread)
     const int tiles = a.RG * a.KS;
@@ -149,8 +198,7 @@ __global__ void __launch_bounds__(kLayerThreads, 1) k_layer(const LayerArgs a) {
   }
   // the token: loaded, or formed from the previous layer by residual + LayerNorm
   if (a.y_prev == nullptr) {
-    const uint4* xg = static_cast<const uint4*>(a.x);
-    for (int ch = tid; ch < NCH; ch += kLayerThreads) reinterpret_cast<uint4*>(xs)[ch] = xg[ch];
+    asm volatile("cp.async.wait_group 1;" ::: "memory");  // this thread's copies of x have landed
   } else {
     const T* xp = static_cast<const T*>(a.x);
     auto load = [&](int ch, float* v) {
@@ -193,12 +241,14 @@ __global__ void __launch_bounds__(kLayerThreads, 1) k_layer(const LayerArgs a) {
     }
   }
   __syncthreads();
+  for (int j = 0; j < n_hot; ++j) fill(j, j);  // barriers are initialised (the barrier above)
   if (a.y_prev != nullptr && a.x_ln_out != nullptr) {  // each block stores its slice of the new x
     uint4* xo = static_cast<uint4*>(a.x_ln_out);
     for (int ch = (int)((int64_t)NCH * c / G) + tid; ch < (int)((int64_t)NCH * (c + 1) / G); ch += kLayerThreads)
       xo[ch] = reinterpret_cast<const uint4*>(xs)[ch];
   }
 
+  SFFN_TRACE(1);
   // ---- phase 1: partial h over this block's (16-row, K-chunk) tiles of V
   {
     const T* V = static_cast<const T*>(a.V);
@@ -232,12 +282,14 @@ __global__ void __launch_bounds__(kLayerThreads, 1) k_layer(const LayerArgs a) {
     }
   }
 
+  SFFN_TRACE(2);
   // ---- phase 2: every block's partials are in place
-  if (!grid_barrier(a.hdr, (uint32_t)G, a.wait_ns, 0x300u)) {
-    if (tid == 0 && a.u_smem && n_own > 0) mbar_wait(ubar, 0, a.hdr, a.wait_ns, 0x301u);
+  if (!grid_barrier(a.hdr, a.bar_flags, (uint32_t)G, a.wait_ns, 0x300u)) {
+    cp_async_wait_all();  // nothing of this block is left in flight
     return;
   }
 
+  SFFN_TRACE(3);
   // ---- phase 3: h = sum of the K-chunk partials (fixed order)
   for (int k = tid; k < r; k += kLayerThreads) {
     float s = 0.f;
@@ -246,11 +298,14 @@ __global__ void __launch_bounds__(kLayerThreads, 1) k_layer(const LayerArgs a) {
   }
   __syncthreads();
 
-  // ---- phase 4: scores of the owned neurons, 32 rows per warp task; lane k
-  // ends up with row k's full dot product (reduce-scatter over the lanes)
-  bool u_ok = true;
-  if (a.u_smem && n_own > 0) u_ok = mbar_wait(ubar, 0, a.hdr, a.wait_ns, 0x302u);
-  if (__syncthreads_or(!u_ok)) return;
+  // ---- phase 4: scores of the owned neurons.  One warp per 32-row word: lane
+  // l holds 16-byte chunks l, l+32, ... of every row, rows are summed with a
+  // warp all-reduce, and lane k keeps row k's score.  A compact loop: fully
+  // unrolled variants of it overflow the instruction cache.
+  SFFN_TRACE(4);
+  cp_async_wait_all();  // this thread's U-row copies have landed; the barrier below publishes all
+  __syncthreads();
+  SFFN_TRACE(8);
   {
     float hreg[CPL][E];
 #pragma unroll
@@ -261,39 +316,29 @@ __global__ void __launch_bounds__(kLayerThreads, 1) k_layer(const LayerArgs a) {
     }
     const T* Ug = static_cast<const T*>(a.U);
     for (int q = warp; q < nwords; q += kLayerWarps) {
-      float v[32];
-#pragma unroll
-      for (int k = 0; k < 32; ++k) {
+      const int kn = min(32, n_own - q * 32);
+      float mine = 0.f;
+#pragma unroll 2
+      for (int k = 0; k < kn; ++k) {
         const int j = q * 32 + k;
         float acc = 0.f;
-        if (j < n_own) {
 #pragma unroll
-          for (int cc = 0; cc < CPL; ++cc) {
-            const int ch = lane + 32 * cc;
-            if (ch < NC) {
-              const uint4 raw = a.u_smem ? reinterpret_cast<const uint4*>(region + (size_t)j * urow_bytes)[ch]
-                                         : ldg_stream(Ug + (size_t)(c + (size_t)j * G) * r + ch * E);
-              float w[E];
-              unpack<T>(raw, w);
+        for (int cc = 0; cc < CPL; ++cc) {
+          const int ch = lane + 32 * cc;
+          if (ch < NC) {
+            const uint4 raw = a.u_smem ? reinterpret_cast<const uint4*>(region + a.u_off + (size_t)j * urow_bytes)[ch]
+                                       : ldg_stream(Ug + (size_t)(c + (size_t)j * G) * r + ch * E);
+            float w[E];
+            unpack<T>(raw, w);
 #pragma unroll
-              for (int e = 0; e < E; ++e) acc = fmaf(w[e], hreg[cc][e], acc);
-            }
+            for (int e = 0; e < E; ++e) acc = fmaf(w[e], hreg[cc][e], acc);
           }
         }
-        v[k] = acc;
-      }
-#pragma unroll
-      for (int o = 16; o >= 1; o >>= 1) {
-        const bool upper = (lane & o) != 0;
-#pragma unroll
-        for (int k = 0; k < o; ++k) {
-          const float send = upper ? v[k] : v[k + o];
-          const float keep = upper ? v[k + o] : v[k];
-          v[k] = keep + __shfl_xor_sync(0xffffffffu, send, o);
-        }
+        acc = warp_sum(acc);
+        if (lane == k) mine = acc;
       }
       const int j = q * 32 + lane;
-      const bool act = j < n_own && (v[0] + ownpb[j < n_own ? j : 0]) > a.tau;
+      const bool act = lane < kn && (mine + ownpb[lane < kn ? j : 0]) > a.tau;
       const uint32_t bits = __ballot_sync(0xffffffffu, act);
       if (lane == 0) words[q] = bits;
       if (act && a.mask != nullptr) {
@@ -303,39 +348,55 @@ __global__ void __launch_bounds__(kLayerThreads, 1) k_layer(const LayerArgs a) {
     }
   }
   __syncthreads();
-  // ascending list of active owned rows
-  if (tid < nwords) {
-    int pre = 0;
-    for (int w = 0; w < tid; ++w) pre += __popc(words[w]);
-    uint32_t bits = words[tid];
-    while (bits) {
-      const int k = __ffs(bits) - 1;
-      bits &= bits - 1;
-      list[pre++] = tid * 32 + k;
+  SFFN_TRACE(9);
+  // ascending list of active owned rows: warp 0 scans the word popcounts
+  if (warp == 0) {
+    int base = 0;
+    for (int q0 = 0; q0 < nwords; q0 += 32) {
+      const int q = q0 + lane;
+      uint32_t bits = q < nwords ? words[q] : 0u;
+      const int cnt = __popc(bits);
+      int incl = cnt;
+#pragma unroll
+      for (int o = 1; o < 32; o <<= 1) {
+        const int v = __shfl_up_sync(0xffffffffu, incl, o);
+        if (lane >= o) incl += v;
+      }
+      int pos = base + incl - cnt;
+      while (bits) {
+        const int k = __ffs(bits) - 1;
+        bits &= bits - 1;
+        list[pos++] = q * 32 + k;
+      }
+      base += __shfl_sync(0xffffffffu, incl, 31);
     }
-    if (tid == nwords - 1) s_nloc = pre;
+    if (lane == 0) s_nloc = base;
   }
-  if (nwords == 0 && tid == 0) s_nloc = 0;
   __syncthreads();
   const int nloc = s_nloc;
+  SFFN_TRACE_VAL(11, nloc);
 
-  // ---- phase 5: stream the active rows through the ring, accumulate
-  const unsigned char* gup = static_cast<const unsigned char*>(a.w_up);
-  const unsigned char* ggt = static_cast<const unsigned char*>(a.w_gate);
-  const unsigned char* gdn = static_cast<const unsigned char*>(a.w_downT);
-  uint64_t policy = 0;
-  if (tid == 0) policy = policy_evict_first();
-  auto issue = [&](int j) {
-    const int s = j % S;
-    const size_t off = (size_t)(c + (size_t)list[j] * G) * row_bytes;
-    unsigned char* dst = region + (size_t)s * stage_bytes;
-    mbar_arrive_expect_tx(&bars[s], stage_bytes);
-    bulk_g2s(dst, gup + off, row_bytes, &bars[s], policy);
-    if (reglu) bulk_g2s(dst + row_bytes, ggt + off, row_bytes, &bars[s], policy);
-    bulk_g2s(dst + (size_t)(nrows - 1) * row_bytes, gdn + off, row_bytes, &bars[s], policy);
+  // ---- phase 5: the active rows stream through a ring of S one-neuron stages,
+  // consumed in groups of up to kGroup neurons per block-wide reduction.
+  SFFN_TRACE(5);
+  // If the hot rows fetched in phase 0 are exactly the first list entries (the
+  // usual case) their stages already hold positions 0..n_hot-1; otherwise
+  // those copies are waited out and discarded, and each such stage is one
+  // phase ahead.  List position p uses stage p % S.
+  bool hot_ok = n_hot <= nloc;
+  for (int k = 0; k < n_hot && hot_ok; ++k) hot_ok = list[k] == k;
+  auto parity = [&](int p) -> uint32_t {
+    const int st = p % S;
+    return (uint32_t)((p / S) + ((!hot_ok && st < n_hot) ? 1 : 0)) & 1u;
   };
-  if (tid == 0)
-    for (int j = 0; j < min(S, nloc); ++j) issue(j);
+  bool failed = false;
+  if (!hot_ok)
+    for (int k = 0; k < n_hot; ++k) failed |= !mbar_wait(&bars[k], 0, a.hdr, a.wait_ns, 0x305u);
+  if (__syncthreads_or(failed)) {
+    cp_async_wait_all();
+    return;
+  }
+  for (int p = hot_ok ? n_hot : 0; p < min(S, nloc); ++p) fill(p % S, list[p]);
 
   float xr[CPT][E], yacc[CPT][E];
 #pragma unroll
@@ -347,73 +408,94 @@ __global__ void __launch_bounds__(kLayerThreads, 1) k_layer(const LayerArgs a) {
 #pragma unroll
     for (int e = 0; e < E; ++e) yacc[cq][e] = 0.f;
   }
-  int consumed = 0;
-  bool failed = false;
-  for (int j = 0; j < nloc; ++j) {
-    const int s = j % S;
-    const bool ok = mbar_wait(&bars[s], (uint32_t)(j / S) & 1u, a.hdr, a.wait_ns, 0x303u);
-    const uint4* up = reinterpret_cast<const uint4*>(region + (size_t)s * stage_bytes);
-    const uint4* gt = up + NCH;
-    const uint4* dn = up + (size_t)(nrows - 1) * NCH;
-    float pu = 0.f, pg = 0.f;
+  const int ng_max = max(1, min(kGroup, S / 2));
+  int grp = 0;
+  for (int p0 = 0; p0 < nloc; p0 += ng_max, ++grp) {
+    const int ng = min(ng_max, nloc - p0);
+    bool ok = true;
+    float pu[kGroup], pg[kGroup];
 #pragma unroll
-    for (int cq = 0; cq < CPT; ++cq) {
-      const int ch = tid + cq * kLayerThreads;
-      if (ch < NCH) {
-        float w[E];
-        unpack<T>(up[ch], w);
+    for (int g = 0; g < kGroup; ++g) {
+      pu[g] = pg[g] = 0.f;
+      if (g < ng) {
+        const int st = (p0 + g) % S;
+        ok &= mbar_wait(&bars[st], parity(p0 + g), a.hdr, a.wait_ns, 0x303u);
+        const uint4* up = reinterpret_cast<const uint4*>(region + (size_t)st * stage_bytes);
 #pragma unroll
-        for (int e = 0; e < E; ++e) pu = fmaf(w[e], xr[cq][e], pu);
-        if (reglu) {
-          unpack<T>(gt[ch], w);
+        for (int cq = 0; cq < CPT; ++cq) {
+          const int ch = tid + cq * kLayerThreads;
+          if (ch < NCH) {
+            float w[E];
+            unpack<T>(up[ch], w);
 #pragma unroll
-          for (int e = 0; e < E; ++e) pg = fmaf(w[e], xr[cq][e], pg);
+            for (int e = 0; e < E; ++e) pu[g] = fmaf(w[e], xr[cq][e], pu[g]);
+            if (reglu) {
+              unpack<T>(up[NCH + ch], w);
+#pragma unroll
+              for (int e = 0; e < E; ++e) pg[g] = fmaf(w[e], xr[cq][e], pg[g]);
+            }
+          }
         }
       }
     }
-    pu = warp_sum(pu);
-    if (reglu) pg = warp_sum(pg);
+    if (grp == 0) SFFN_TRACE(10);
+#pragma unroll
+    for (int g = 0; g < kGroup; ++g) {
+      pu[g] = warp_sum(pu[g]);
+      if (reglu) pg[g] = warp_sum(pg[g]);
+    }
     if (lane == 0) {
-      s_red[j & 1][warp][0] = pu;
-      s_red[j & 1][warp][1] = pg;
+#pragma unroll
+      for (int g = 0; g < kGroup; ++g) {
+        s_red[grp & 1][warp][g][0] = pu[g];
+        s_red[grp & 1][warp][g][1] = pg[g];
+      }
     }
     if (__syncthreads_or(!ok)) {
       failed = true;
       break;
     }
-    consumed = j + 1;
-    if (tid == 0 && j >= 1 && j - 1 + S < nloc) issue(j - 1 + S);
-    float u = 0.f, g = 0.f;
+    float act[kGroup];
 #pragma unroll
-    for (int w = 0; w < kLayerWarps; ++w) {
-      u += s_red[j & 1][w][0];
-      g += s_red[j & 1][w][1];
+    for (int g = 0; g < kGroup; ++g) {
+      float u = 0.f, gt = 0.f;
+#pragma unroll
+      for (int w = 0; w < kLayerWarps; ++w) {
+        u += s_red[grp & 1][w][g][0];
+        gt += s_red[grp & 1][w][g][1];
+      }
+      const float bias = g < ng ? ownb[list[p0 + g]] : 0.f;
+      act[g] = g < ng ? (reglu ? fmaxf(gt + bias, 0.f) * u : fmaxf(u + bias, 0.f)) : 0.f;
     }
-    const float bias = ownb[list[j]];
-    const float act = reglu ? fmaxf(g + bias, 0.f) * u : fmaxf(u + bias, 0.f);
-    if (act != 0.f) {
 #pragma unroll
-      for (int cq = 0; cq < CPT; ++cq) {
-        const int ch = tid + cq * kLayerThreads;
-        if (ch < NCH) {
-          float w[E];
-          unpack<T>(dn[ch], w);
+    for (int g = 0; g < kGroup; ++g) {
+      if (g < ng) {
+        const int st = (p0 + g) % S;
+        if (act[g] != 0.f) {
+          const uint4* dn = reinterpret_cast<const uint4*>(region + (size_t)st * stage_bytes) + (size_t)(nrows - 1) * NCH;
 #pragma unroll
-          for (int e = 0; e < E; ++e) yacc[cq][e] = fmaf(act, w[e], yacc[cq][e]);
+          for (int cq = 0; cq < CPT; ++cq) {
+            const int ch = tid + cq * kLayerThreads;
+            if (ch < NCH) {
+              float w[E];
+              unpack<T>(dn[ch], w);
+#pragma unroll
+              for (int e = 0; e < E; ++e) yacc[cq][e] = fmaf(act[g], w[e], yacc[cq][e]);
+            }
+          }
         }
+        // this thread is done with its chunks of the stage: refill them
+        if (p0 + g + S < nloc) fill(st, list[p0 + g + S]);
       }
     }
   }
   if (failed) {
-    if (tid == 0) {
-      const int issued = consumed == 0 ? min(S, nloc) : min(nloc, consumed - 1 + S);
-      for (int j = consumed; j < issued; ++j)
-        mbar_wait(&bars[j % S], (uint32_t)(j / S) & 1u, a.hdr, a.wait_ns, 0x304u);
-    }
+    cp_async_wait_all();
     return;
   }
 
   // ---- phase 6: add this block's contribution into y
+  SFFN_TRACE(6);
   if (nloc > 0) {
 #pragma unroll
     for (int cq = 0; cq < CPT; ++cq) {
@@ -426,6 +508,7 @@ __global__ void __launch_bounds__(kLayerThreads, 1) k_layer(const LayerArgs a) {
       }
     }
   }
+  SFFN_TRACE(7);
 }
 
 template <typename T, int CPT>

@@ -95,8 +95,8 @@ __global__ void k_permute_rows(const V* __restrict__ src, V* __restrict__ dst, c
 
 // Waits at the grid barrier for one more block than the grid has: the arrival
 // never comes, so the wait must end by its limit with kStTimeout recorded.
-__global__ void k_wait_timeout(WsHeader* hdr, uint64_t limit_ns) {
-  grid_barrier(hdr, gridDim.x + 1u, limit_ns, 0x900u);
+__global__ void k_wait_timeout(WsHeader* hdr, uint32_t* flags, uint64_t limit_ns) {
+  grid_barrier(hdr, flags, gridDim.x + 1u, limit_ns, 0x900u);
 }
 
 template <typename T>
@@ -140,8 +140,8 @@ cudaError_t launch_permute_rows(const void* src, void* dst, const int32_t* perm,
   return cudaGetLastError();
 }
 
-cudaError_t launch_wait_timeout(WsHeader* hdr, uint64_t limit_ns, cudaStream_t s) {
-  k_wait_timeout<<<1, 32, 0, s>>>(hdr, limit_ns);
+cudaError_t launch_wait_timeout(WsHeader* hdr, uint32_t* flags, uint64_t limit_ns, cudaStream_t s) {
+  k_wait_timeout<<<1, 32, 0, s>>>(hdr, flags, limit_ns);
   return cudaGetLastError();
 }
 
@@ -205,6 +205,9 @@ bool layer_config(int dtype, int act, int d, int f, int r, int grid, size_t smem
   cfg->kc = kc;
   cfg->KS = (d + kc - 1) / kc;
   cfg->region_bytes = (std::max(s * stage, cfg->u_smem ? u_bytes : 0) + 15) / 16 * 16;
+  const size_t u_round = (u_bytes + 15) / 16 * 16;
+  cfg->u_off = cfg->u_smem ? cfg->region_bytes - u_round : 0;  // U rows sit at the end of the region
+  cfg->hot_stages = (int)std::min<size_t>(4, cfg->u_smem ? cfg->u_off / stage : s);
   cfg->smem = cfg->region_bytes + (size_t)d * esize + (size_t)((r + 3) & ~3) * 4 + (s + 1) * 8 +
               (size_t)own_cap * 12 + nwords * 4;
   return cfg->smem + reserve <= smem_optin;

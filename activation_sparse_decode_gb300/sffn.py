@@ -39,7 +39,8 @@ class sffn_layer_desc(ctypes.Structure):
     _fields_ = [("d_model", _i32), ("d_ff", _i32), ("rank", _i32), ("max_batch", _i32),
                 ("dtype", _i32), ("act", _i32),
                 ("w_up", _vp), ("w_gate", _vp), ("w_downT", _vp), ("b", _vp),
-                ("pred_U", _vp), ("pred_V", _vp), ("pred_b", _vp), ("tau", ctypes.c_float), ("flags", _i32)]
+                ("pred_U", _vp), ("pred_V", _vp), ("pred_b", _vp), ("tau", ctypes.c_float), ("flags", _i32),
+                ("hot_rows", _i32)]
 
 SFFN_FLAG_MULTI_KERNEL = 1
 
@@ -109,7 +110,7 @@ class Layer:
     """A layer handle plus references to the tensors it borrows."""
 
     def __init__(self, w_up, w_downT, b, U, V, pred_b=None, w_gate=None, tau: float = 0.0, max_batch: int = 1,
-                 flags: int = 0):
+                 flags: int = 0, hot_rows: int = 0):
         self.tensors = [w_up, w_downT, b, U, V, pred_b, w_gate]
         self.act = "reglu" if w_gate is not None else "relu"
         self.dtype = w_up.dtype
@@ -118,7 +119,7 @@ class Layer:
             dtype=DTYPE_CODES[w_up.dtype], act=ACT_CODES[self.act],
             w_up=_ptr(w_up), w_gate=_ptr(w_gate), w_downT=_ptr(w_downT), b=_ptr(b),
             pred_U=_ptr(U), pred_V=_ptr(V), pred_b=_ptr(pred_b if pred_b is not None else b), tau=tau,
-            flags=flags)
+            flags=flags, hot_rows=hot_rows)
         self.desc = desc
         h = ctypes.c_void_p()
         _check(_c["create"](ctypes.byref(desc), ctypes.byref(h)))
@@ -126,10 +127,10 @@ class Layer:
         self.d_model, self.d_ff, self.rank, self.max_batch = desc.d_model, desc.d_ff, desc.rank, max_batch
 
     @classmethod
-    def from_weights(cls, lw, tau: float = 0.0, max_batch: int = 1, flags: int = 0) -> "Layer":
+    def from_weights(cls, lw, tau: float = 0.0, max_batch: int = 1, flags: int = 0, hot_rows: int = 0) -> "Layer":
         """From a workloads.LayerWeights already on the GPU."""
         return cls(lw.w_up, lw.w_downT, lw.b, lw.U, lw.V, pred_b=lw.b, w_gate=lw.w_gate, tau=tau,
-                   max_batch=max_batch, flags=flags)
+                   max_batch=max_batch, flags=flags, hot_rows=hot_rows)
 
     def close(self):
         if getattr(self, "handle", None):
@@ -276,3 +277,10 @@ def hot_first_order(layer: Layer, X: torch.Tensor, ws: torch.Tensor) -> np.ndarr
     counts = torch.empty(layer.d_ff, dtype=torch.int32, device=X.device)
     sffn_profile_counts(layer, X, counts, ws)
     return sffn_hot_first_perm(counts.cpu().numpy()), counts
+
+
+def hot_row_count(counts, n_tokens: int, frac: float = 0.99) -> int:
+    """Neurons predicted active for at least `frac` of the profile tokens: under
+    the hot-first order they are the first rows."""
+    c = np.asarray(counts.cpu() if hasattr(counts, "cpu") else counts)
+    return int((c >= frac * n_tokens).sum())

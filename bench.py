@@ -187,14 +187,15 @@ def bench_sffn(args):
     lw = W.make_layer(wl, seed=0, layer=0, device=dev)
     prof_layer = sffn.Layer.from_weights(lw, tau=wl.tau, max_batch=8)
     ws8 = sffn.new_workspace(sffn.sffn_workspace_size(prof_layer, 8), dev)
-    perm, _ = sffn.hot_first_order(prof_layer, W.make_profile_tokens(wl, device=dev), ws8)
+    perm, counts = sffn.hot_first_order(prof_layer, W.make_profile_tokens(wl, device=dev), ws8)
+    hot_rows = sffn.hot_row_count(counts, wl.profile_tokens)
     prof_layer.close()
     lw = sffn.permute_layer_weights(lw, torch.from_numpy(perm).to(dev))
     R = max(1, args.replicas)
     reps = [lw] + [W.LayerWeights(w_up=lw.w_up.clone(), w_gate=None, w_downT=lw.w_downT.clone(), b=lw.b.clone(),
                                   U=lw.U.clone(), V=lw.V.clone(), p=lw.p, dtype=lw.dtype, act=lw.act)
                    for _ in range(R - 1)]
-    layers = [sffn.Layer.from_weights(r, tau=wl.tau, max_batch=1) for r in reps]
+    layers = [sffn.Layer.from_weights(r, tau=wl.tau, max_batch=1, hot_rows=hot_rows) for r in reps]
     ws = sffn.new_workspace(sffn.sffn_workspace_size(layers[0], 1), dev)
 
     X = W.make_tokens(wl, T, batch=1, seed=rank, device=dev)  # [T][1][d] fp16
@@ -334,6 +335,7 @@ def bench_sffn(args):
                   f"({R * (lw.w_up.numel() * 4 + (lw.U.numel() + lw.V.numel()) * 2) / 2**30:.2f} GiB), "
                   f"reuse distance ~{R * 37} MB per token vs {L2_BYTES // 2**20} MB L2",
             "mean_active": round(float(n_tok.mean()), 1),
+            "hot_rows": hot_rows,
             "us_per_layer": round(ms_per_step * 1e3 / T, 3),
             "layer_kernel_us_per_launch": round(k_avg_ms * 1e3, 3),
             "predictor_bytes_per_token": int(pred_bytes),

@@ -48,8 +48,10 @@
  *     recorded in a status word inside the workspace and read with
  *     sffn_read_device_status.  Kernels never trap.
  *   - The workspace must be zero-filled once before its first use
- *     (sffn_workspace_init does it); every call leaves it reusable.  Two calls
- *     that share a workspace must be ordered (same stream, or synchronised).
+ *     (sffn_workspace_init does it); every call leaves it reusable, except
+ *     after a device status of SFFN_ERR_TIMEOUT, when it must be zero-filled
+ *     again.  Two calls that share a workspace must be ordered (same stream,
+ *     or synchronised): calls that overlap on the GPU race.
  */
 #ifndef SFFN_H
 #define SFFN_H
@@ -93,6 +95,12 @@ typedef struct {
   const float* pred_b;  /* [d_ff] predictor bias                            */
   float tau;            /* threshold: neuron i is active iff s_i > tau      */
   int32_t flags;        /* SFFN_FLAG_* bits, 0 for the defaults            */
+  int32_t hot_rows;     /* neurons [0, hot_rows) are "hot": under a hot-first
+                           order (sffn_hot_first_perm) the neurons active for
+                           nearly every token.  Their rows may be fetched
+                           before the predictor has decided; results do not
+                           depend on it (only the predicted set is used).
+                           0 = no such prefetch.                            */
 } sffn_layer_desc;
 
 /* Batch-1 calls normally run the whole layer (predictor, threshold, gather,

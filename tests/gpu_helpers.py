@@ -42,7 +42,7 @@ def hot_first(sffn, lw, wl, layer_idx=0, device="cuda"):
     perm, counts = sffn.hot_first_order(layer, X, ws)
     layer.close()
     perm_dev = torch.from_numpy(perm).to(device)
-    return sffn.permute_layer_weights(lw, perm_dev), perm, counts
+    return sffn.permute_layer_weights(lw, perm_dev), perm, counts[torch.from_numpy(perm).to(device).long()]
 
 
 def mask_from_list(idx_row, n, f):

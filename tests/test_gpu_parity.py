@@ -93,9 +93,11 @@ def test_c2_full_size_sampled(sffn):
     lw0 = W.make_layer(wl, device=DEV)
     lw, perm, counts = hot_first(sffn, lw0, wl)
     del lw0
-    c = counts.cpu().numpy()
-    assert np.all(np.diff(c[perm]) <= 0)
-    layer = sffn.Layer.from_weights(lw, tau=wl.tau)
+    c = counts.cpu().numpy()  # in the new (hot-first) order
+    assert np.all(np.diff(c) <= 0)
+    hot = sffn.hot_row_count(c, wl.profile_tokens)
+    assert 200 < hot < 800
+    layer = sffn.Layer.from_weights(lw, tau=wl.tau, hot_rows=hot)
     X = W.make_tokens(wl, wl.steps, device=DEV)
     Y, I, N = run_tokens(sffn, layer, X)
     # the multi-kernel path on the first tokens agrees with the fused one
@@ -214,6 +216,22 @@ def test_all_false_and_all_true_masks(sffn, tau, expect, batch):
         for s in range(2):
             for b in range(batch):
                 assert rel_l2(Y[s, b], oracle.dense_ffn(ol, Xh[s, b])) < TOL["f16"]
+
+
+@pytest.mark.parametrize("hot_rows", [0, 10, 100, 1500])
+def test_hot_row_prefetch_any_setting(sffn, hot_rows):
+    """Rows of "hot" neurons are fetched before the predictor decides; when a
+    prefetched neuron turns out inactive the copy is discarded.  With every
+    neuron declared hot most prefetches are wasted, and the result is the same."""
+    wl = W.tiny_workload(d_model=1024, d_ff=1500, rank=32, dtype="f16", mean_p=0.1, name="hot-prefetch")
+    lw = W.make_layer(wl, device=DEV)
+    ol = oracle_layer(lw)
+    layer = sffn.Layer.from_weights(lw, hot_rows=hot_rows)
+    X = W.make_tokens(wl, 4, device=DEV)
+    Y, I, N = run_tokens(sffn, layer, X)
+    Xh = st(X)
+    for t in range(4):
+        check_token(ol, Xh[t, 0], mask_from_list(I[t, 0], N[t, 0], wl.d_ff), Y[t, 0], TOL["f16"])
 
 
 def test_deterministic_run_to_run(sffn, c3):

@@ -33,10 +33,12 @@ def build_stack(sffn, wl, n_layers, max_batch):
     lws, layers = [], []
     for l in range(n_layers):
         lw = W.make_layer(wl, layer=l, device=DEV)
+        hot = 0
         if wl.reorder:
-            lw, _, _ = hot_first(sffn, lw, wl, layer_idx=l)
+            lw, _, counts = hot_first(sffn, lw, wl, layer_idx=l)
+            hot = sffn.hot_row_count(counts, wl.profile_tokens)
         lws.append(lw)
-        layers.append(sffn.Layer.from_weights(lw, tau=wl.tau, max_batch=max_batch))
+        layers.append(sffn.Layer.from_weights(lw, tau=wl.tau, max_batch=max_batch, hot_rows=hot))
     torch.cuda.synchronize()
     return lws, layers
 

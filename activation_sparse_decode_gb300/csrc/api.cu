@@ -64,7 +64,7 @@ size_t align_up(size_t v, size_t a) { return (v + a - 1) / a * a; }
 int bt_slot(int bt) { return bt == 1 ? 0 : bt == 2 ? 1 : 2; }
 
 struct WsLayout {
-  size_t hdr, flags, tickets, h_part, h, mask, y_part, hl_part, total;
+  size_t hdr, flags, tickets, h_part, h, mask, y_part, hl_part, bal_counts, bal_lists, total;
 };
 
 WsLayout layout(const sffn_layer* L, int batch) {
@@ -84,6 +84,9 @@ WsLayout layout(const sffn_layer* L, int batch) {
   w.mask = take((size_t)batch * L->W * sizeof(uint32_t));
   w.y_part = take((size_t)L->gather_grid * std::min(batch, L->max_bt) * d.d_model * sizeof(float));
   w.hl_part = take(L->lcfg_ok ? (size_t)L->lcfg.KS * d.rank * sizeof(float) : 0);
+  const size_t own_cap = (size_t)(d.d_ff + L->gather_grid - 1) / L->gather_grid;
+  w.bal_counts = take(L->lcfg_ok ? (size_t)L->gather_grid * sizeof(uint64_t) : 0);
+  w.bal_lists = take(L->lcfg_ok ? (size_t)L->gather_grid * own_cap * 2 * sizeof(int32_t) : 0);
   w.total = off;
   return w;
 }
@@ -99,6 +102,8 @@ struct Ws {
   uint32_t* mask() const { return reinterpret_cast<uint32_t*>(base + lay.mask); }
   float* y_part() const { return reinterpret_cast<float*>(base + lay.y_part); }
   float* hl_part() const { return reinterpret_cast<float*>(base + lay.hl_part); }
+  uint64_t* bal_counts() const { return reinterpret_cast<uint64_t*>(base + lay.bal_counts); }
+  int32_t* bal_lists() const { return reinterpret_cast<int32_t*>(base + lay.bal_lists); }
 };
 
 sffn_status check_ws(const sffn_layer* L, int batch, void* ws, size_t bytes, Ws* out) {
@@ -242,6 +247,14 @@ sffn_status run_layer(const sffn_layer* L, const void* x, const float* y_prev, v
   a.u_off = L->lcfg.u_off;
   a.hot_rows = d.hot_rows;
   a.hot_stages = L->lcfg.hot_stages;
+  const int own_cap = (d.d_ff + L->gather_grid - 1) / L->gather_grid;
+  a.balance = (d.flags & SFFN_FLAG_BALANCE) != 0 && own_cap >= 8 ? 1 : 0;
+  int prefill = L->lcfg.hot_stages;
+  if (d.expected_active > 0.f)
+    prefill = std::max(prefill, std::min(L->lcfg.nstages, (int)(0.85f * d.expected_active / L->gather_grid)));
+  a.prefill = prefill;
+  a.bal_counts = ws.bal_counts();
+  a.bal_lists = ws.bal_lists();
   a.wait_ns = (uint64_t)g_wait_ns;
   if (g_prof_start != nullptr) SFFN_TRY(record_profile_event(g_prof_start, s));
   SFFN_CUDA(launch_layer(d.dtype, L->lcfg, a, L->gather_grid, s), "layer launch");
@@ -310,6 +323,7 @@ sffn_status sffn_create_layer(const sffn_layer_desc* desc, sffn_layer_t* out) {
   }
   if (d.rank / (16 / esize) > 256) return fail(SFFN_ERR_UNSUPPORTED, "rank too large for the score kernel");
   if (d.hot_rows < 0 || d.hot_rows > d.d_ff) return fail(SFFN_ERR_INVALID_ARG, "hot_rows outside [0, d_ff]");
+  if (!(d.expected_active >= 0.f)) return fail(SFFN_ERR_INVALID_ARG, "expected_active must be >= 0");
 
   sffn_layer* L = new (std::nothrow) sffn_layer();
   if (L == nullptr) return fail(SFFN_ERR_INVALID_ARG, "out of host memory");

@@ -103,67 +103,71 @@ __device__ __forceinline__ void st_release_gpu(uint32_t* p, uint32_t v) {
 
 // Grid-wide barrier over `expected` resident blocks.
 //
-// Arrival is two-level: blocks arrive on the counter of their group of
-// kBarGroup blocks, and the last block of each group arrives on the top
-// counter (h->bar_count), so no counter takes more than ~20 same-address
-// atomics.  Release is per block: every block waits on its own flag word, one
-// 128-byte line each, and the last block to arrive stores the next generation
-// into all of them, so no two blocks poll the same line and the release store
-// does not queue behind pollers.  All flags hold the same generation, so a
-// block reads its own flag before arriving to learn the value it waits to
-// change.  Layout of `flags` (32-word stride): [expected] release flags, then
-// [ceil(expected / kBarGroup)] group counters.
+// Every block has its own release flag, flags[b * 32] (one 128-byte line
+// each); all flags hold the same generation.  A block learns that generation
+// before it can change -- at kernel start, barrier_generation() -- so arriving
+// costs one round trip: an acq_rel atomic add on the shared counter.  The last
+// block to arrive resets the counter, fences once, and stores generation + 1
+// into every flag; the others poll only their own line, so no two blocks poll
+// the same line and the release stores do not queue behind pollers.  `gen` is
+// the generation this barrier waits to leave (the next barrier of the same
+// launch waits on gen + 1).
 //
-// Every wait is bounded: after limit_ns the block records kStTimeout and
-// returns false (the counters are then left mid-count; zero the workspace
+// One thread of the block (`bthread`) does the arrival, the release and the
+// wait.  Every wait is bounded: after limit_ns the block records kStTimeout
+// and returns false (the counter is then left mid-count; zero the workspace
 // before reusing it).  All threads of the block must call it.
-constexpr uint32_t kBarGroup = 8;
+__host__ __device__ constexpr size_t barrier_flag_bytes(uint32_t blocks) { return (size_t)blocks * 128; }
 
-__host__ __device__ constexpr size_t barrier_flag_bytes(uint32_t blocks) {
-  return ((size_t)blocks + (blocks + kBarGroup - 1) / kBarGroup) * 128;
+__device__ __forceinline__ uint32_t barrier_generation(const uint32_t* flags) {
+  uint32_t v;
+  asm volatile("ld.relaxed.gpu.global.u32 %0, [%1];" : "=r"(v) : "l"(flags + (size_t)blockIdx.x * 32) : "memory");
+  return v;
 }
 
-__device__ __forceinline__ bool grid_barrier(WsHeader* h, uint32_t* flags, uint32_t expected, uint64_t limit_ns,
-                                             uint32_t detail) {
-  __shared__ int s_ok, s_last;
-  __shared__ uint32_t s_gen;
-  uint32_t* mine = flags + (size_t)blockIdx.x * 32;
-  __syncthreads();
-  if (threadIdx.x == 0) {
-    const uint32_t gen = ld_acquire_gpu(mine);  // read before arriving
-    __threadfence();                             // publish this block's writes
-    const uint32_t grp = blockIdx.x / kBarGroup;
-    const uint32_t ngroups = (expected + kBarGroup - 1) / kBarGroup;
-    const uint32_t in_grp = min(kBarGroup, expected - grp * kBarGroup);
-    uint32_t* gcount = flags + ((size_t)expected + grp) * 32;
-    int last = 0;
-    if (atomicAdd(gcount, 1u) == in_grp - 1) {
-      atomicExch(gcount, 0u);
-      __threadfence();
-      if (atomicAdd(&h->bar_count, 1u) == ngroups - 1) {
-        atomicExch(&h->bar_count, 0u);  // reset before any block can be released
-        __threadfence();
-        last = 1;
-      }
-    }
-    s_gen = gen;
-    s_last = last;
-    s_ok = 1;
+// The warp-level part, called by all 32 lanes of one warp: lane 0 arrives;
+// if it was the last block, the counter is reset and the 32 lanes store the
+// next generation into the flags (a few stores each, each lane fencing first);
+// otherwise lane 0 waits on its own flag.  Returns the same value on all lanes.
+__device__ __forceinline__ bool barrier_arrive_wait_warp(WsHeader* h, uint32_t* flags, uint32_t expected,
+                                                         uint32_t gen, uint64_t limit_ns, uint32_t detail) {
+  const uint32_t lane = threadIdx.x & 31u;
+  uint32_t old = 0;
+  if (lane == 0)
+    asm volatile("atom.add.acq_rel.gpu.global.u32 %0, [%1], 1;" : "=r"(old) : "l"(&h->bar_count) : "memory");
+  old = __shfl_sync(0xffffffffu, old, 0);
+  if (old == expected - 1) {
+    if (lane == 0)  // nobody touches the counter again before the release below
+      asm volatile("st.relaxed.gpu.global.u32 [%0], 0;" ::"l"(&h->bar_count) : "memory");
+    __syncwarp();
+    __threadfence();  // the reset and everything this block saw precede the release
+    for (uint32_t b = lane; b < expected; b += 32)
+      asm volatile("st.relaxed.gpu.global.u32 [%0], %1;" ::"l"(flags + (size_t)b * 32), "r"(gen + 1u) : "memory");
+    return true;
   }
-  __syncthreads();
-  if (s_last) {
-    __threadfence();
-    for (uint32_t b = threadIdx.x; b < expected; b += blockDim.x) st_release_gpu(flags + (size_t)b * 32, s_gen + 1u);
-  } else if (threadIdx.x == 0) {
+  int ok = 1;
+  if (lane == 0) {
+    const uint32_t* mine = flags + (size_t)blockIdx.x * 32;
     const uint64_t t0 = globaltimer_ns();
-    while (ld_acquire_gpu(mine) == s_gen) {
+    while (ld_acquire_gpu(mine) == gen) {
       if (globaltimer_ns() - t0 > limit_ns) {
         set_status(h, kStTimeout, detail);
-        s_ok = 0;
+        ok = 0;
         break;
       }
     }
-    __threadfence();
+  }
+  return __shfl_sync(0xffffffffu, ok, 0) != 0;
+}
+
+// Whole-block form; warp `bwarp` does the barrier work.
+__device__ __forceinline__ bool grid_barrier(WsHeader* h, uint32_t* flags, uint32_t expected, uint32_t gen,
+                                             uint64_t limit_ns, uint32_t detail, uint32_t bwarp = 0) {
+  __shared__ int s_ok;
+  __syncthreads();
+  if ((threadIdx.x >> 5) == bwarp) {
+    const bool ok = barrier_arrive_wait_warp(h, flags, expected, gen, limit_ns, detail);
+    if ((threadIdx.x & 31) == 0) s_ok = ok ? 1 : 0;
   }
   __syncthreads();
   return s_ok != 0;
@@ -227,6 +231,9 @@ __device__ __forceinline__ void bulk_g2s(void* dst, const void* src, uint32_t by
 // flight per thread without registers; completion per thread via wait_all.
 __device__ __forceinline__ void cp_async16(void* smem_dst, const void* src) {
   asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(smem_addr(smem_dst)), "l"(src) : "memory");
+}
+__device__ __forceinline__ void cp_async4(void* smem_dst, const void* src) {
+  asm volatile("cp.async.ca.shared.global [%0], [%1], 4;" ::"r"(smem_addr(smem_dst)), "l"(src) : "memory");
 }
 __device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commit_group;" ::: "memory"); }
 __device__ __forceinline__ void cp_async_wait_all() { asm volatile("cp.async.wait_all;" ::: "memory"); }

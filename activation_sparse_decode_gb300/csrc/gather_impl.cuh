@@ -65,6 +65,8 @@ __global__ void __launch_bounds__(kGatherThreads, 1) k_gather(const GatherArgs a
   float* sbias = reinterpret_cast<float*>(list + a.list_cap);
   uint8_t* tokbits = reinterpret_cast<uint8_t*>(sbias + a.list_cap);
 
+  // generation of this block's barrier flag, read before anyone can change it
+  const uint32_t bar_gen = warp == 0 ? barrier_generation(a.bar_flags) : 0u;
   if (tid == 0) {
     for (int s = 0; s < S; ++s) mbar_init(&bars[s], 1);
     fence_mbar_init();
@@ -266,7 +268,7 @@ __global__ void __launch_bounds__(kGatherThreads, 1) k_gather(const GatherArgs a
       }
     }
   if (G == 1) return;
-  if (!grid_barrier(a.hdr, a.bar_flags, (uint32_t)G, a.wait_ns, 0x200u)) return;
+  if (!grid_barrier(a.hdr, a.bar_flags, (uint32_t)G, bar_gen, a.wait_ns, 0x200u)) return;
 
   const int N4 = B * d / 4;
   const float4* yp4 = reinterpret_cast<const float4*>(a.y_part);

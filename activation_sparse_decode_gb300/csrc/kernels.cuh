@@ -96,6 +96,10 @@ struct LayerArgs {
   int d, f, r, KS, kc, RG, act, nstages, u_smem;
   int hot_rows;           // neurons [0, hot_rows) are prefetched before the predictor decides
   int hot_stages;         // ring stages free of the U rows, usable for that prefetch
+  int balance;            // 1: even out the active rows over the blocks (second barrier)
+  int prefill;            // own rows each block starts streaming before the balancing
+  uint64_t* bal_counts;   // [grid] {epoch, active rows} per block (workspace)
+  int32_t* bal_lists;     // [grid][own_cap] {neuron, bias bits} pairs per block (workspace)
   size_t region_bytes;
   size_t u_off;           // offset of the staged U rows inside the region
   uint64_t wait_ns;

@@ -39,7 +39,9 @@ namespace sffn {
 #ifdef SFFN_PHASE_TRACE
 #define SFFN_TRACE(k) sffn_phase_trace(k)
 #define SFFN_TRACE_VAL(k, v) sffn_phase_value(k, v)
+#define SFFN_TRACE_AT(k, t) sffn_phase_trace_at(k, t)
 #else
+#define SFFN_TRACE_AT(k, t) ((void)0)
 #define SFFN_TRACE(k) ((void)0)
 #define SFFN_TRACE_VAL(k, v) ((void)0)
 #endif
@@ -47,6 +49,10 @@ namespace sffn {
 constexpr int kLayerThreads = 256;
 constexpr int kLayerWarps = kLayerThreads / 32;
 constexpr int kGroup = 4;  // neurons per block-wide reduction in the row ring
+// Warps 0..6 do the copying of phase 0; lane 0 of warp 7 runs the grid
+// barrier, so that no copies of its warp are in flight when it fences.
+constexpr int kCopyThreads = kLayerThreads - 32;
+constexpr int kBarrierThread = kLayerThreads - 32;
 
 __device__ __forceinline__ void bulk_prefetch_l2(const void* src, uint32_t bytes) {
   asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(src), "r"(bytes) : "memory");
@@ -117,31 +123,25 @@ __global__ void __launch_bounds__(kLayerThreads, 1) k_layer(const LayerArgs a) {
   float* ownb = reinterpret_cast<float*>(bars + S + 1);
   float* ownpb = ownb + own_cap;
   uint32_t* words = reinterpret_cast<uint32_t*>(ownpb + own_cap);
-  int32_t* list = reinterpret_cast<int32_t*>(words + nwords);
+  int32_t* list = reinterpret_cast<int32_t*>(words + nwords);  // active neurons (global index) per ring position
+  float* lbias = reinterpret_cast<float*>(list + own_cap);       // their biases
+  int32_t* bal_cnt = reinterpret_cast<int32_t*>(lbias + own_cap);  // balancing: rows per block,
+  int32_t* bal_keep = bal_cnt + G;                                 // rows each block keeps,
+  int32_t* bal_einc = bal_keep + G;                                // inclusive prefix of given-away rows
+  uint8_t* s_act = reinterpret_cast<uint8_t*>(bal_einc + G);      // predicted-active flag per owned row
   SFFN_TRACE(0);
 
   // ---- phase 0: start every independent stream, zero the outputs
+  // generation of this block's barrier flag: it cannot change before this block arrives
+  const uint32_t bar_gen = warp == kBarrierThread / 32 ? barrier_generation(a.bar_flags) : 0u;
+  // tag of this launch's published balancing counts: the generation the barrier moves to
+  const uint32_t bar_epoch = barrier_generation(a.bar_flags) + 1u;
   if (a.y_prev == nullptr) {  // the token itself first: everything in phase 1 waits on it
     const uint4* xg = static_cast<const uint4*>(a.x);
-    for (int ch = tid; ch < NCH; ch += kLayerThreads) cp_async16(reinterpret_cast<uint4*>(xs) + ch, xg + ch);
+    if (tid < kCopyThreads)
+      for (int ch = tid; ch < NCH; ch += kCopyThreads) cp_async16(reinterpret_cast<uint4*>(xs) + ch, xg + ch);
   }
   cp_async_commit();  // group 1: x
-  const unsigned char* Ub = static_cast<const unsigned char*>(a.U);
-  if (a.u_smem) {  // owned U rows -> shared memory, 16 bytes per copy over all threads
-    const int total = n_own * NC;
-    for (int q = tid; q < total; q += kLayerThreads) {
-      const int j = q / NC, ch = q - j * NC;
-      cp_async16(region + a.u_off + (size_t)j * urow_bytes + ch * 16,
-                 Ub + (size_t)(c + (size_t)j * G) * urow_bytes + ch * 16);
-    }
-  } else {  // too large to stage: warm L2 with the owned rows instead
-    const int lines = (urow_bytes + 127) / 128;
-    for (int q = tid; q < n_own * lines; q += kLayerThreads) {
-      const int j = q / lines, l = q - j * lines;
-      prefetch_l2(Ub + (size_t)(c + (size_t)j * G) * urow_bytes + l * 128);
-    }
-  }
-  cp_async_commit();  // group 2: U rows
   // hot rows: the first owned neurons under the hot-first order are almost
   // always active, so their rows start streaming before the predictor decides
   const int n_hot = c < a.hot_rows ? min(a.hot_stages, min(n_own, (a.hot_rows - c + G - 1) / G)) : 0;
@@ -152,8 +152,8 @@ __global__ void __launch_bounds__(kLayerThreads, 1) k_layer(const LayerArgs a) {
   // same chunks it later reads, so no thread waits on another's data) and
   // arrives on the stage barrier when they have landed.  Expected arrivals per
   // phase: one per thread.
-  auto fill = [&](int s, int j) {
-    const size_t off = (size_t)(c + (size_t)j * G) * row_bytes;
+  auto fill = [&](int s, int neuron) {
+    const size_t off = (size_t)neuron * row_bytes;
     unsigned char* dst = region + (size_t)s * stage_bytes;
 #pragma unroll
     for (int cq = 0; cq < CPT; ++cq) {
@@ -164,6 +164,20 @@ __global__ void __launch_bounds__(kLayerThreads, 1) k_layer(const LayerArgs a) {
         cp_async16(dst + (size_t)(nrows - 1) * row_bytes + (size_t)ch * 16, gdn + off + (size_t)ch * 16);
       }
     }
+    cp_async_arrive_noinc(&bars[s]);
+  };
+  // Hot rows, fetched before the predictor decides: warps 0..6 copy every
+  // chunk (the barrier warp has nothing in flight when it fences) and all
+  // threads arrive, so the stage completes when the copies have landed.
+  auto fill_hot = [&](int s) {
+    const size_t off = (size_t)(c + (size_t)s * G) * row_bytes;
+    unsigned char* dst = region + (size_t)s * stage_bytes;
+    if (tid < kCopyThreads)
+      for (int ch = tid; ch < NCH; ch += kCopyThreads) {
+        cp_async16(dst + (size_t)ch * 16, gup + off + (size_t)ch * 16);
+        if (reglu) cp_async16(dst + row_bytes + (size_t)ch * 16, ggt + off + (size_t)ch * 16);
+        cp_async16(dst + (size_t)(nrows - 1) * row_bytes + (size_t)ch * 16, gdn + off + (size_t)ch * 16);
+      }
     cp_async_arrive_noinc(&bars[s]);
   };
   if (tid == 0) {
@@ -180,25 +194,28 @@ __global__ void __launch_bounds__(kLayerThreads, 1) k_layer(const LayerArgs a) {
       if (tid < 16 && row < r) bulk_prefetch_l2(V + ((size_t)row * d + k0) * ES, (uint32_t)kn * ES);
     }
   }
-  for (int j = tid; j < n_own; j += kLayerThreads) {
+  for (int j = tid; j < (tid < kCopyThreads ? n_own : 0); j += kCopyThreads) {
     const int i = c + j * G;
-    ownb[j] = a.b != nullptr ? __ldg(&a.b[i]) : 0.f;
-    ownpb[j] = __ldg(&a.pb[i]);
+    if (a.b != nullptr)
+      cp_async4(&ownb[j], &a.b[i]);
+    else
+      ownb[j] = 0.f;
+    cp_async4(&ownpb[j], &a.pb[i]);
   }
   {
     float4* y4 = reinterpret_cast<float4*>(a.y);
     const int N4 = d / 4;
-    for (int q = (int)((int64_t)N4 * c / G) + tid; q < (int)((int64_t)N4 * (c + 1) / G); q += kLayerThreads)
-      y4[q] = make_float4(0.f, 0.f, 0.f, 0.f);
+    const int q1 = tid < kCopyThreads ? (int)((int64_t)N4 * (c + 1) / G) : 0;
+    for (int q = (int)((int64_t)N4 * c / G) + tid; q < q1; q += kCopyThreads) y4[q] = make_float4(0.f, 0.f, 0.f, 0.f);
     if (a.mask != nullptr) {
       const int W = (f + 31) / 32;
-      for (int w = (int)((int64_t)W * c / G) + tid; w < (int)((int64_t)W * (c + 1) / G); w += kLayerThreads)
-        a.mask[w] = 0u;
+      const int w1 = tid < kCopyThreads ? (int)((int64_t)W * (c + 1) / G) : 0;
+      for (int w = (int)((int64_t)W * c / G) + tid; w < w1; w += kCopyThreads) a.mask[w] = 0u;
     }
   }
   // the token: loaded, or formed from the previous layer by residual + LayerNorm
   if (a.y_prev == nullptr) {
-    asm volatile("cp.async.wait_group 1;" ::: "memory");  // this thread's copies of x have landed
+    cp_async_wait_all();  // this thread's copies of x have landed
   } else {
     const T* xp = static_cast<const T*>(a.x);
     auto load = [&](int ch, float* v) {
@@ -241,7 +258,6 @@ __global__ void __launch_bounds__(kLayerThreads, 1) k_layer(const LayerArgs a) {
     }
   }
   __syncthreads();
-  for (int j = 0; j < n_hot; ++j) fill(j, j);  // barriers are initialised (the barrier above)
   if (a.y_prev != nullptr && a.x_ln_out != nullptr) {  // each block stores its slice of the new x
     uint4* xo = static_cast<uint4*>(a.x_ln_out);
     for (int ch = (int)((int64_t)NCH * c / G) + tid; ch < (int)((int64_t)NCH * (c + 1) / G); ch += kLayerThreads)
@@ -282,9 +298,41 @@ __global__ void __launch_bounds__(kLayerThreads, 1) k_layer(const LayerArgs a) {
     }
   }
 
+  // ---- phase 2: grid barrier (every block's h partials are in place).  The
+  // barrier thread arrives and waits while the other warps issue the copies
+  // needed after it: the owned U rows, then the hot rows.  Issued here, behind
+  // the V tiles, they do not delay the token and V loads in the request queues.
   SFFN_TRACE(2);
-  // ---- phase 2: every block's partials are in place
-  if (!grid_barrier(a.hdr, a.bar_flags, (uint32_t)G, a.wait_ns, 0x300u)) {
+  __shared__ int s_passed;
+  __syncthreads();  // all h partials of this block are written
+  if (warp == kBarrierThread / 32) {
+    SFFN_TRACE_AT(12, kBarrierThread);
+    const bool ok = barrier_arrive_wait_warp(a.hdr, a.bar_flags, (uint32_t)G, bar_gen, a.wait_ns, 0x300u);
+    SFFN_TRACE_AT(13, kBarrierThread);
+    if (tid == kBarrierThread) s_passed = ok ? 1 : 0;
+  } else {
+    const unsigned char* Ub = static_cast<const unsigned char*>(a.U);
+    if (a.u_smem) {  // owned U rows -> shared memory, 16 bytes per copy
+      for (int q = tid; q < n_own * NC; q += kCopyThreads) {
+        const int j = q / NC, ch = q - j * NC;
+        cp_async16(region + a.u_off + (size_t)j * urow_bytes + ch * 16,
+                   Ub + (size_t)(c + (size_t)j * G) * urow_bytes + ch * 16);
+      }
+    } else {  // too large to stage: warm L2 with the owned rows instead
+      const int lines = (urow_bytes + 127) / 128;
+      for (int q = tid; q < n_own * lines; q += kCopyThreads) {
+        const int j = q / lines, l = q - j * lines;
+        prefetch_l2(Ub + (size_t)(c + (size_t)j * G) * urow_bytes + l * 128);
+      }
+    }
+    cp_async_commit();
+  }
+  __syncthreads();
+  const bool passed = s_passed != 0;
+  // hot rows next: issued after the barrier so that its round trips do not
+  // queue behind them; they still land before the predictor has decided
+  for (int j = 0; j < n_hot; ++j) fill_hot(j);
+  if (!passed) {
     cp_async_wait_all();  // nothing of this block is left in flight
     return;
   }
@@ -306,7 +354,56 @@ __global__ void __launch_bounds__(kLayerThreads, 1) k_layer(const LayerArgs a) {
   cp_async_wait_all();  // this thread's U-row copies have landed; the barrier below publishes all
   __syncthreads();
   SFFN_TRACE(8);
-  {
+  if (a.u_smem) {
+    // Lr lanes per row from shared memory (a power of two, as many as keep all
+    // threads busy); each group starts at a row-dependent chunk so the lanes of
+    // one shared-memory phase hit distinct banks.
+    int Lr = 1;
+    while (Lr < 32 && 2 * Lr <= NC && n_own * 2 * Lr <= kLayerThreads) Lr *= 2;
+    const int rows_per_pass = kLayerThreads / Lr;
+    const int sub = tid % Lr;
+    for (int j0 = 0; j0 < n_own; j0 += rows_per_pass) {
+      const int j = j0 + tid / Lr;
+      float acc0 = 0.f, acc1 = 0.f;
+      if (j < n_own) {
+        const uint4* row = reinterpret_cast<const uint4*>(region + a.u_off + (size_t)j * urow_bytes);
+        const int rot = (j * Lr) & 7;
+        for (int k = sub; k < NC; k += Lr) {
+          int ch = k + rot;
+          if (ch >= NC) ch -= NC;
+          if (ch >= NC) ch %= NC;
+          float w[E];
+          unpack<T>(row[ch], w);
+          const float4* hp = reinterpret_cast<const float4*>(hs + ch * E);
+          const float4 h0 = hp[0];
+          acc0 = fmaf(w[0], h0.x, acc0);
+          acc1 = fmaf(w[1], h0.y, acc1);
+          acc0 = fmaf(w[2], h0.z, acc0);
+          acc1 = fmaf(w[3], h0.w, acc1);
+          if (E > 4) {
+            const float4 h1 = hp[1];
+            acc0 = fmaf(w[E > 4 ? 4 : 0], h1.x, acc0);
+            acc1 = fmaf(w[E > 4 ? 5 : 0], h1.y, acc1);
+            acc0 = fmaf(w[E > 4 ? 6 : 0], h1.z, acc0);
+            acc1 = fmaf(w[E > 4 ? 7 : 0], h1.w, acc1);
+          }
+        }
+      }
+      float acc = acc0 + acc1;
+      for (int o = Lr >> 1; o > 0; o >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, o);
+      if (sub == 0 && j < n_own) {
+        const bool act = acc + ownpb[j] > a.tau;
+        s_act[j] = act ? 1 : 0;
+        if (act && a.mask != nullptr) {
+          const int i = c + j * G;
+          atomicOr(&a.mask[i >> 5], 1u << (i & 31));
+        }
+      }
+    }
+  } else {
+    // Rows too many to stage: one warp per 32-row word reads each row from
+    // L2 (warmed in phase 0), lane l holding chunks l, l+32, ...; rows are
+    // summed with a warp all-reduce and lane k keeps row k's score.
     float hreg[CPL][E];
 #pragma unroll
     for (int cc = 0; cc < CPL; ++cc) {
@@ -326,10 +423,8 @@ __global__ void __launch_bounds__(kLayerThreads, 1) k_layer(const LayerArgs a) {
         for (int cc = 0; cc < CPL; ++cc) {
           const int ch = lane + 32 * cc;
           if (ch < NC) {
-            const uint4 raw = a.u_smem ? reinterpret_cast<const uint4*>(region + a.u_off + (size_t)j * urow_bytes)[ch]
-                                       : ldg_stream(Ug + (size_t)(c + (size_t)j * G) * r + ch * E);
             float w[E];
-            unpack<T>(raw, w);
+            unpack<T>(ldg_stream(Ug + (size_t)(c + (size_t)j * G) * r + ch * E), w);
 #pragma unroll
             for (int e = 0; e < E; ++e) acc = fmaf(w[e], hreg[cc][e], acc);
           }
@@ -339,8 +434,7 @@ __global__ void __launch_bounds__(kLayerThreads, 1) k_layer(const LayerArgs a) {
       }
       const int j = q * 32 + lane;
       const bool act = lane < kn && (mine + ownpb[lane < kn ? j : 0]) > a.tau;
-      const uint32_t bits = __ballot_sync(0xffffffffu, act);
-      if (lane == 0) words[q] = bits;
+      if (lane < kn) s_act[j] = act ? 1 : 0;
       if (act && a.mask != nullptr) {
         const int i = c + j * G;
         atomicOr(&a.mask[i >> 5], 1u << (i & 31));
@@ -354,7 +448,11 @@ __global__ void __launch_bounds__(kLayerThreads, 1) k_layer(const LayerArgs a) {
     int base = 0;
     for (int q0 = 0; q0 < nwords; q0 += 32) {
       const int q = q0 + lane;
-      uint32_t bits = q < nwords ? words[q] : 0u;
+      uint32_t bits = 0u;  // word q of the activity flags
+      for (int k = 0; k < 32; ++k) {
+        const int j = q * 32 + k;
+        if (q < nwords && j < n_own && s_act[j]) bits |= 1u << k;
+      }
       const int cnt = __popc(bits);
       int incl = cnt;
 #pragma unroll
@@ -366,14 +464,16 @@ __global__ void __launch_bounds__(kLayerThreads, 1) k_layer(const LayerArgs a) {
       while (bits) {
         const int k = __ffs(bits) - 1;
         bits &= bits - 1;
-        list[pos++] = q * 32 + k;
+        const int j = q * 32 + k;
+        list[pos] = c + j * G;
+        lbias[pos++] = ownb[j];
       }
       base += __shfl_sync(0xffffffffu, incl, 31);
     }
     if (lane == 0) s_nloc = base;
   }
   __syncthreads();
-  const int nloc = s_nloc;
+  int nloc = s_nloc;
   SFFN_TRACE_VAL(11, nloc);
 
   // ---- phase 5: the active rows stream through a ring of S one-neuron stages,
@@ -384,7 +484,7 @@ __global__ void __launch_bounds__(kLayerThreads, 1) k_layer(const LayerArgs a) {
   // those copies are waited out and discarded, and each such stage is one
   // phase ahead.  List position p uses stage p % S.
   bool hot_ok = n_hot <= nloc;
-  for (int k = 0; k < n_hot && hot_ok; ++k) hot_ok = list[k] == k;
+  for (int k = 0; k < n_hot && hot_ok; ++k) hot_ok = list[k] == c + k * G;
   auto parity = [&](int p) -> uint32_t {
     const int st = p % S;
     return (uint32_t)((p / S) + ((!hot_ok && st < n_hot) ? 1 : 0)) & 1u;
@@ -396,7 +496,144 @@ __global__ void __launch_bounds__(kLayerThreads, 1) k_layer(const LayerArgs a) {
     cp_async_wait_all();
     return;
   }
-  for (int p = hot_ok ? n_hot : 0; p < min(S, nloc); ++p) fill(p % S, list[p]);
+  // Own rows start streaming now, up to the prefill count when the rows are
+  // balanced afterwards (every block keeps at least that many of its own).
+  // Rows every block keeps and streams before the balancing: only the hot
+  // ones.  Traffic in flight lengthens the exchange's round trips (requests
+  // queue behind it), so the exchange runs with the request queues short.
+  const int P = a.hot_stages;
+  const int pre = a.balance ? min(nloc, P) : nloc;
+  for (int p = hot_ok ? n_hot : 0; p < min(S, pre); ++p) fill(p % S, list[p]);
+
+  // ---- balancing: each token's active rows fall unevenly on the blocks (a
+  // sum of independent Bernoulli draws per block), and the block with the
+  // most rows sets the kernel's length.  Every block publishes its count and
+  // list; after a second grid barrier every block computes the same
+  // assignment: the total N gives capacities K or K + 1, each block keeps its
+  // own rows up to max(capacity, prefill) -- its hot rows stay local -- and
+  // the rows above that, in block order, fill the other blocks' free
+  // capacity in block order.
+  if (a.balance) {
+    // publish: the list as {neuron, bias} pairs, then the count tagged with
+    // this launch's epoch (the barrier generation), released after the pairs
+    int2* pub = reinterpret_cast<int2*>(a.bal_lists) + (size_t)c * own_cap;
+    for (int p = tid; p < nloc; p += kLayerThreads) pub[p] = make_int2(list[p], __float_as_int(lbias[p]));
+    __syncthreads();
+    if (tid == kBarrierThread) {  // its warp has no copies in flight, so the fence is short
+      __threadfence();
+      const uint64_t word = ((uint64_t)bar_epoch << 32) | (uint32_t)nloc;
+      asm volatile("st.relaxed.gpu.global.u64 [%0], %1;" ::"l"(a.bal_counts + c), "l"(word) : "memory");
+      SFFN_TRACE_AT(15, kBarrierThread);
+    }
+    if (warp == 0) {
+      // every block's count, all loads in flight together, re-polling
+      // (bounded) only the ones not yet published
+      constexpr int kCnt = 8;  // counts per lane: up to 256 blocks
+      uint64_t v[kCnt];
+#pragma unroll
+      for (int k = 0; k < kCnt; ++k) {
+        const int cc = lane + 32 * k;
+        v[k] = 0;
+        if (cc < G) asm volatile("ld.acquire.gpu.global.u64 %0, [%1];" : "=l"(v[k]) : "l"(a.bal_counts + cc) : "memory");
+      }
+      bool ok = true;
+      const uint64_t t0 = globaltimer_ns();
+      while (true) {
+        bool all = true;
+#pragma unroll
+        for (int k = 0; k < kCnt; ++k) {
+          const int cc = lane + 32 * k;
+          if (cc < G && (uint32_t)(v[k] >> 32) != bar_epoch) {
+            all = false;
+            asm volatile("ld.acquire.gpu.global.u64 %0, [%1];" : "=l"(v[k]) : "l"(a.bal_counts + cc) : "memory");
+          }
+        }
+        if (all) break;
+        if (globaltimer_ns() - t0 > a.wait_ns) {
+          set_status(a.hdr, kStTimeout, 0x306u);
+          ok = false;
+          break;
+        }
+      }
+      int N = 0;
+#pragma unroll
+      for (int k = 0; k < kCnt; ++k) {
+        const int cc = lane + 32 * k;
+        const int n = cc < G ? (int)(uint32_t)v[k] : 0;
+        if (cc < G) bal_cnt[cc] = n;
+        N += n;
+      }
+      N = __reduce_add_sync(0xffffffffu, N);
+      __syncwarp();
+      SFFN_TRACE(16);
+      ok = __all_sync(0xffffffffu, ok);
+      if (ok) {
+        const int K = N / G, R = N - K * G;
+        int run_e = 0, run_d = 0, my_d = 0, my_def = 0, my_keep = 0;
+        for (int q0 = 0; q0 < G; q0 += 32) {
+          const int cc = q0 + lane;
+          const int n = cc < G ? bal_cnt[cc] : 0;
+          const int cap = K + (cc < R ? 1 : 0);
+          const int keep = min(n, max(cap, P));
+          const int exc = cc < G ? n - keep : 0;
+          const int def = cc < G ? max(0, cap - keep) : 0;
+          int ie = exc, id = def;  // inclusive warp scans
+#pragma unroll
+          for (int o = 1; o < 32; o <<= 1) {
+            const int ve = __shfl_up_sync(0xffffffffu, ie, o), vd = __shfl_up_sync(0xffffffffu, id, o);
+            if (lane >= o) {
+              ie += ve;
+              id += vd;
+            }
+          }
+          if (cc < G) {
+            bal_keep[cc] = keep;
+            bal_einc[cc] = run_e + ie;
+          }
+          if (cc == c) {
+            my_d = run_d + id - def;
+            my_def = def;
+            my_keep = keep;
+          }
+          run_e += __shfl_sync(0xffffffffu, ie, 31);
+          run_d += __shfl_sync(0xffffffffu, id, 31);
+        }
+        my_d = __reduce_add_sync(0xffffffffu, my_d);  // only the lane holding block c contributes
+        my_def = __reduce_add_sync(0xffffffffu, my_def);
+        my_keep = __reduce_add_sync(0xffffffffu, my_keep);
+        __syncwarp();
+        const int X = run_e;  // rows given away in total
+        const int nsteal = max(0, min(my_d + my_def, X) - my_d);
+        for (int t = lane; t < nsteal; t += 32) {
+          const int x = my_d + t;
+          int lo = 0, hi = G - 1;  // first block whose inclusive prefix exceeds x
+          while (lo < hi) {
+            const int mid = (lo + hi) >> 1;
+            if (bal_einc[mid] > x)
+              hi = mid;
+            else
+              lo = mid + 1;
+          }
+          const int owner_exc = bal_cnt[lo] - bal_keep[lo];
+          const int pos = bal_keep[lo] + (x - (bal_einc[lo] - owner_exc));
+          const int2 e = __ldcg(reinterpret_cast<const int2*>(a.bal_lists) + (size_t)lo * own_cap + pos);
+          list[my_keep + t] = e.x;
+          lbias[my_keep + t] = __int_as_float(e.y);
+        }
+        if (lane == 0) s_nloc = my_keep + nsteal;
+        SFFN_TRACE(17);
+      }
+      if (lane == 0) s_passed = ok ? 1 : 0;
+    }
+    __syncthreads();
+    if (!s_passed) {
+      cp_async_wait_all();
+      return;
+    }
+    nloc = s_nloc;
+    SFFN_TRACE(14);
+    for (int p = pre; p < min(S, nloc); ++p) fill(p % S, list[p]);
+  }
 
   float xr[CPT][E], yacc[CPT][E];
 #pragma unroll
@@ -410,8 +647,9 @@ __global__ void __launch_bounds__(kLayerThreads, 1) k_layer(const LayerArgs a) {
   }
   const int ng_max = max(1, min(kGroup, S / 2));
   int grp = 0;
-  for (int p0 = 0; p0 < nloc; p0 += ng_max, ++grp) {
-    const int ng = min(ng_max, nloc - p0);
+  for (int p0 = 0, ng = 0; p0 < nloc; p0 += ng, ++grp) {
+    // the first group is the prefetched hot rows alone, so it need not wait for a cold row
+    ng = (grp == 0 && hot_ok && n_hot > 0) ? min(n_hot, ng_max) : min(ng_max, nloc - p0);
     bool ok = true;
     float pu[kGroup], pg[kGroup];
 #pragma unroll
@@ -464,7 +702,7 @@ __global__ void __launch_bounds__(kLayerThreads, 1) k_layer(const LayerArgs a) {
         u += s_red[grp & 1][w][g][0];
         gt += s_red[grp & 1][w][g][1];
       }
-      const float bias = g < ng ? ownb[list[p0 + g]] : 0.f;
+      const float bias = g < ng ? lbias[p0 + g] : 0.f;
       act[g] = g < ng ? (reglu ? fmaxf(gt + bias, 0.f) * u : fmaxf(u + bias, 0.f)) : 0.f;
     }
 #pragma unroll

@@ -96,7 +96,7 @@ __global__ void k_permute_rows(const V* __restrict__ src, V* __restrict__ dst, c
 // Waits at the grid barrier for one more block than the grid has: the arrival
 // never comes, so the wait must end by its limit with kStTimeout recorded.
 __global__ void k_wait_timeout(WsHeader* hdr, uint32_t* flags, uint64_t limit_ns) {
-  grid_barrier(hdr, flags, gridDim.x + 1u, limit_ns, 0x900u);
+  grid_barrier(hdr, flags, gridDim.x + 1u, barrier_generation(flags), limit_ns, 0x900u);
 }
 
 template <typename T>
@@ -190,9 +190,11 @@ bool layer_config(int dtype, int act, int d, int f, int r, int grid, size_t smem
   kc = (kc + unit - 1) / unit * unit;
   const int own_cap = (f + grid - 1) / grid;
   const int nwords = (own_cap + 31) / 32;
-  if (nwords > 256) return false;
+  if (nwords > 256 || grid > 256) return false;  // the balancing holds 8 block counts per lane
   const size_t stage = (size_t)(act == kReglu ? 3 : 2) * d * esize;
-  const size_t fixed = (size_t)d * esize + (size_t)((r + 3) & ~3) * 4 + 17 * 8 + (size_t)own_cap * 12 + nwords * 4;
+  // x, h, stage barriers, own biases (2), list + list biases, words, balancing scratch (3 x grid)
+  const size_t fixed = (size_t)d * esize + (size_t)((r + 3) & ~3) * 4 + 17 * 8 + (size_t)own_cap * 16 + nwords * 4 +
+                       (size_t)grid * 12 + (size_t)own_cap + 80;
   const size_t reserve = 2048;  // static shared memory of the kernel
   if (smem_optin < fixed + reserve + 2 * stage) return false;
   const size_t budget = (smem_optin - fixed - reserve) / 16 * 16;
@@ -209,7 +211,7 @@ bool layer_config(int dtype, int act, int d, int f, int r, int grid, size_t smem
   cfg->u_off = cfg->u_smem ? cfg->region_bytes - u_round : 0;  // U rows sit at the end of the region
   cfg->hot_stages = (int)std::min<size_t>(4, cfg->u_smem ? cfg->u_off / stage : s);
   cfg->smem = cfg->region_bytes + (size_t)d * esize + (size_t)((r + 3) & ~3) * 4 + (s + 1) * 8 +
-              (size_t)own_cap * 12 + nwords * 4;
+              (size_t)own_cap * 16 + nwords * 4 + (size_t)grid * 12 + (size_t)own_cap + 80;
   return cfg->smem + reserve <= smem_optin;
 }
 

@@ -40,9 +40,10 @@ class sffn_layer_desc(ctypes.Structure):
                 ("dtype", _i32), ("act", _i32),
                 ("w_up", _vp), ("w_gate", _vp), ("w_downT", _vp), ("b", _vp),
                 ("pred_U", _vp), ("pred_V", _vp), ("pred_b", _vp), ("tau", ctypes.c_float), ("flags", _i32),
-                ("hot_rows", _i32)]
+                ("hot_rows", _i32), ("expected_active", ctypes.c_float)]
 
 SFFN_FLAG_MULTI_KERNEL = 1
+SFFN_FLAG_BALANCE = 2
 
 
 def _sig(name, res, *args):
@@ -110,7 +111,7 @@ class Layer:
     """A layer handle plus references to the tensors it borrows."""
 
     def __init__(self, w_up, w_downT, b, U, V, pred_b=None, w_gate=None, tau: float = 0.0, max_batch: int = 1,
-                 flags: int = 0, hot_rows: int = 0):
+                 flags: int = 0, hot_rows: int = 0, expected_active: float = 0.0):
         self.tensors = [w_up, w_downT, b, U, V, pred_b, w_gate]
         self.act = "reglu" if w_gate is not None else "relu"
         self.dtype = w_up.dtype
@@ -119,7 +120,7 @@ class Layer:
             dtype=DTYPE_CODES[w_up.dtype], act=ACT_CODES[self.act],
             w_up=_ptr(w_up), w_gate=_ptr(w_gate), w_downT=_ptr(w_downT), b=_ptr(b),
             pred_U=_ptr(U), pred_V=_ptr(V), pred_b=_ptr(pred_b if pred_b is not None else b), tau=tau,
-            flags=flags, hot_rows=hot_rows)
+            flags=flags, hot_rows=hot_rows, expected_active=expected_active)
         self.desc = desc
         h = ctypes.c_void_p()
         _check(_c["create"](ctypes.byref(desc), ctypes.byref(h)))
@@ -127,10 +128,11 @@ class Layer:
         self.d_model, self.d_ff, self.rank, self.max_batch = desc.d_model, desc.d_ff, desc.rank, max_batch
 
     @classmethod
-    def from_weights(cls, lw, tau: float = 0.0, max_batch: int = 1, flags: int = 0, hot_rows: int = 0) -> "Layer":
+    def from_weights(cls, lw, tau: float = 0.0, max_batch: int = 1, flags: int = 0, hot_rows: int = 0,
+                     expected_active: float = 0.0) -> "Layer":
         """From a workloads.LayerWeights already on the GPU."""
         return cls(lw.w_up, lw.w_downT, lw.b, lw.U, lw.V, pred_b=lw.b, w_gate=lw.w_gate, tau=tau,
-                   max_batch=max_batch, flags=flags, hot_rows=hot_rows)
+                   max_batch=max_batch, flags=flags, hot_rows=hot_rows, expected_active=expected_active)
 
     def close(self):
         if getattr(self, "handle", None):

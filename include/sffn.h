@@ -101,6 +101,10 @@ typedef struct {
                            before the predictor has decided; results do not
                            depend on it (only the predicted set is used).
                            0 = no such prefetch.                            */
+  float expected_active; /* expected number of predicted-active neurons per
+                           token (e.g. from the profile counts), 0 = unknown;
+                           a hint for how much work to start before the
+                           active rows are balanced over the SMs.           */
 } sffn_layer_desc;
 
 /* Batch-1 calls normally run the whole layer (predictor, threshold, gather,
@@ -108,6 +112,13 @@ typedef struct {
  * multi-kernel path (separate predictor, score and gather kernels) that larger
  * batches use, with its deterministic cross-block reduction. */
 #define SFFN_FLAG_MULTI_KERNEL 1
+/* Batch-1 kernel: after the predictor, even out the token's active rows over
+ * the SMs (each block publishes its count and list; every block computes the
+ * same assignment, keeping its own rows up to its share and taking the surplus
+ * of others).  Costs about four global round trips; pays off when the uneven
+ * split of active rows costs more (wide rows, many rows per SM).  Needs d_ff
+ * of at least 8 rows per SM, otherwise ignored. */
+#define SFFN_FLAG_BALANCE 2
 
 /* Validates the descriptor and records it with launch settings chosen for the
  * current device.  Allocates only host memory.  Returns INVALID_ARG for bad

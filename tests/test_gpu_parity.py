@@ -234,6 +234,25 @@ def test_hot_row_prefetch_any_setting(sffn, hot_rows):
         check_token(ol, Xh[t, 0], mask_from_list(I[t, 0], N[t, 0], wl.d_ff), Y[t, 0], TOL["f16"])
 
 
+@pytest.mark.parametrize("flags,expected", [(2, 0.0), (2, 1.0), (2, 10.0), (0, 0.0)],
+                         ids=["balanced", "balanced-hint", "balanced-overhint", "unbalanced"])
+def test_row_balancing(sffn, flags, expected):
+    """Active rows are evened out over the SMs after the predictor; every
+    setting of the balancing must give the oracle's result."""
+    wl = W.tiny_workload(d_model=512, d_ff=8192, rank=64, dtype="f16", mean_p=0.1, name="balance")
+    lw0 = W.make_layer(wl, device=DEV)
+    lw, _, counts = hot_first(sffn, lw0, wl.with_(profile_tokens=200))
+    hot = sffn.hot_row_count(counts, 200)
+    ea = expected * float(counts.sum().item()) / 200
+    ol = oracle_layer(lw)
+    layer = sffn.Layer.from_weights(lw, hot_rows=hot, flags=flags, expected_active=ea)
+    X = W.make_tokens(wl, 6, device=DEV)
+    Y, I, N = run_tokens(sffn, layer, X)
+    Xh = st(X)
+    for t in range(6):
+        check_token(ol, Xh[t, 0], mask_from_list(I[t, 0], N[t, 0], wl.d_ff), Y[t, 0], TOL["f16"])
+
+
 def test_deterministic_run_to_run(sffn, c3):
     """The multi-kernel path reduces block partials in a fixed order (the
     single-launch kernel adds them with float atomics instead)."""

@@ -33,12 +33,13 @@ def build_stack(sffn, wl, n_layers, max_batch):
     lws, layers = [], []
     for l in range(n_layers):
         lw = W.make_layer(wl, layer=l, device=DEV)
-        hot = 0
+        hot, ea = 0, 0.0
         if wl.reorder:
             lw, _, counts = hot_first(sffn, lw, wl, layer_idx=l)
             hot = sffn.hot_row_count(counts, wl.profile_tokens)
+            ea = float(counts.sum().item()) / wl.profile_tokens
         lws.append(lw)
-        layers.append(sffn.Layer.from_weights(lw, tau=wl.tau, max_batch=max_batch, hot_rows=hot))
+        layers.append(sffn.Layer.from_weights(lw, tau=wl.tau, max_batch=max_batch, hot_rows=hot, expected_active=ea))
     torch.cuda.synchronize()
     return lws, layers
 
@@ -74,7 +75,7 @@ def teacher_forced(sffn, wl, lws, layers, x_out, trace, pairs, tokens):
             check_next_input(nh_next[b], want, wl.dtype)
 
 
-@pytest.mark.parametrize("flags", [0, 1], ids=["fused", "multi"])
+@pytest.mark.parametrize("flags", [0, 1, 2], ids=["fused", "multi", "fused-balanced"])
 def test_small_stack_both_paths(sffn, flags):
     wl = W.tiny_workload(d_model=512, d_ff=2048, rank=64, dtype="bf16", name="small-stack").with_(n_layers=3)
     lws = [W.make_layer(wl, layer=l, device=DEV) for l in range(3)]

@@ -262,7 +262,7 @@ def bench_sffn(args):
     peaks = measured_peaks()
     peak = peaks["hbm_gbs"] if peaks else 6800.0
     traffic = None
-    tpath = os.path.join(ROOT, "profiles", "gather_traffic.json")
+    tpath = os.path.join(ROOT, "profiles", "k_layer_traffic.json")
     if os.path.exists(tpath):
         tj = json.load(open(tpath))
         if tj.get("kernel_source_hash") == kernel_source_hash():

@@ -665,3 +665,69 @@ sffn_status sffn_debug_wait_timeout(void* workspace, size_t ws_bytes, int64_t ti
 }
 
 }  // extern "C"
+
+// ---- internals of sffn_forward_noalloc (noalloc.cu): the single-launch layer
+// kernel on a fixed scratch array instead of a workspace.
+
+sffn_status sffn_internal_fail(sffn_status status, const char* message) { return fail(status, "%s", message); }
+
+sffn_status sffn_internal_layer_device(sffn_layer_t L, int* device) {
+  g_err.clear();
+  if (L == nullptr) return fail(SFFN_ERR_INVALID_ARG, "layer is NULL");
+  *device = L->device;
+  return SFFN_OK;
+}
+
+sffn_status sffn_internal_layer_on_scratch(sffn_layer_t L, const void* x, float* y, void* scratch,
+                                           size_t scratch_bytes, void* stream) {
+  if (!L->fused())
+    return fail(SFFN_ERR_UNSUPPORTED, "the layer has no single-launch kernel configuration (or asks for the "
+                                      "multi-kernel path)");
+  SFFN_TRY(check_dev_ptr(x, "x"));
+  SFFN_TRY(check_dev_ptr(y, "y"));
+  const auto& d = L->desc;
+  // header, barrier flags, predictor partial sums -- the workspace layout's order
+  const size_t flags_off = align_up(sizeof(WsHeader), 256);
+  const size_t part_off = flags_off + align_up(barrier_flag_bytes((uint32_t)L->gather_grid), 256);
+  const size_t need = part_off + align_up((size_t)L->lcfg.KS * d.rank * sizeof(float), 256);
+  if (need > scratch_bytes)
+    return fail(SFFN_ERR_UNSUPPORTED, "this layer needs %zu bytes of scratch, the fixed array holds %zu", need,
+                scratch_bytes);
+  unsigned char* base = static_cast<unsigned char*>(scratch);
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  // the barrier counter and flags must start at zero: the array keeps whatever the last call left
+  SFFN_CUDA(cudaMemsetAsync(base, 0, part_off, s), "scratch clear");
+  LayerArgs a{};
+  a.x = x;
+  a.V = d.pred_V;
+  a.U = d.pred_U;
+  a.pb = d.pred_b;
+  a.b = d.b;
+  a.tau = d.tau;
+  a.w_up = d.w_up;
+  a.w_gate = d.w_gate;
+  a.w_downT = d.w_downT;
+  a.y = y;
+  a.h_part = reinterpret_cast<float*>(base + part_off);
+  a.hdr = reinterpret_cast<WsHeader*>(base);
+  a.bar_flags = reinterpret_cast<uint32_t*>(base + flags_off);
+  a.d = d.d_model;
+  a.f = d.d_ff;
+  a.r = d.rank;
+  a.KS = L->lcfg.KS;
+  a.kc = L->lcfg.kc;
+  a.RG = L->lcfg.RG;
+  a.act = d.act;
+  a.nstages = L->lcfg.nstages;
+  a.u_smem = L->lcfg.u_smem;
+  a.region_bytes = L->lcfg.region_bytes;
+  a.u_off = L->lcfg.u_off;
+  a.hot_rows = d.hot_rows;
+  a.hot_stages = L->lcfg.hot_stages;
+  a.balance = 0;
+  a.prefill = 0;
+  a.wait_ns = (uint64_t)g_wait_ns;
+  SFFN_CUDA(launch_layer(d.dtype, L->lcfg, a, L->gather_grid, s), "layer launch");
+  return SFFN_OK;
+}
+

@@ -73,6 +73,7 @@ _c = {
     "debug_wait": _sig("sffn_debug_wait_timeout", _i32, _vp, _sz, _i64, _vp),
     "wait_limit": _sig("sffn_set_wait_limit_ns", _i32, _i64),
     "prof_events": _sig("sffn_set_profile_events", _i32, _vp, _vp),
+    "noalloc": _sig("sffn_forward_noalloc", _i32, _vp, _vp, _vp, _vp),
     "status_string": _sig("sffn_status_string", ctypes.c_char_p, _i32),
     "last_error": _sig("sffn_last_error", ctypes.c_char_p),
     "version": _sig("sffn_version", _i32),
@@ -82,7 +83,7 @@ EXPORTED = ["sffn_create_layer", "sffn_destroy_layer", "sffn_workspace_size", "s
             "sffn_predict", "sffn_predict_scores", "sffn_forward", "sffn_dense_forward",
             "sffn_residual_layernorm", "sffn_forward_stack", "sffn_stack_workspace_size",
             "sffn_profile_counts", "sffn_hot_first_perm", "sffn_permute_rows", "sffn_read_device_status",
-            "sffn_debug_wait_timeout", "sffn_set_wait_limit_ns", "sffn_set_profile_events", "sffn_status_string", "sffn_last_error",
+            "sffn_debug_wait_timeout", "sffn_set_wait_limit_ns", "sffn_set_profile_events", "sffn_forward_noalloc", "sffn_status_string", "sffn_last_error",
             "sffn_version"]
 
 
@@ -187,6 +188,12 @@ def sffn_forward(layer: Layer, x: torch.Tensor, y: torch.Tensor, ws: torch.Tenso
                  stream=None):
     _check(_c["forward"](layer.handle, _ptr(x), x.shape[0], _ptr(y), _ptr(idx), _ptr(n_active), _ptr(ws),
                          ws.numel(), _stream(stream)))
+
+
+def sffn_forward_noalloc(layer: Layer, x: torch.Tensor, y: torch.Tensor, stream=None):
+    """Batch-1 forward whose scratch is the library's own fixed array (no
+    workspace, no device allocation); see sffn.h for who needs it."""
+    _check(_c["noalloc"](layer.handle, _ptr(x), _ptr(y), _stream(stream)))
 
 
 def sffn_dense_forward(layer: Layer, x: torch.Tensor, y: torch.Tensor, ws: torch.Tensor, stream=None):

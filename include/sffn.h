@@ -141,6 +141,29 @@ sffn_status sffn_predict(sffn_layer_t layer, const void* x, int32_t batch, int32
                          int32_t* n_active, void* workspace, size_t workspace_bytes,
                          void* stream);
 
+/* No counterpart in the paper: a library convenience.
+ *
+ * The batch-1 sparse FFN (as sffn_forward with batch 1, no index outputs) for
+ * callers that cannot allocate device memory: serving loops and embedded
+ * runtimes that own all device memory up front in a fixed pool and forbid
+ * cudaMalloc while running (it may synchronise the device, and it fragments a
+ * pool sized to the byte), and programs whose device memory belongs to another
+ * framework's allocator.  The caller passes x ([d_model], dtype, device) and
+ * y ([d_model] float32, device); the kernel's scratch is a fixed 256 KiB array
+ * inside the library, held on every device that loads the library until the
+ * process exits.  Nothing here calls cudaMalloc or cudaFree.
+ *   - Layers needing more scratch than that (header + 128 bytes per SM + the
+ *     predictor's split-K partial sums) are rejected with SFFN_ERR_UNSUPPORTED
+ *     and a message giving both sizes; so are layers created with
+ *     SFFN_FLAG_MULTI_KERNEL or outside the single-launch kernel's limits.
+ *   - The layer's device must be current.  The first call on a device looks up
+ *     the array's device address there (cudaGetSymbolAddress); make that first
+ *     call before any stream capture.
+ *   - Every call shares the one array and clears its barrier words first, so
+ *     calls that overlap on the GPU (other streams, other threads) race; order
+ *     them.  Device-side wait timeouts are not reported by this entry point. */
+sffn_status sffn_forward_noalloc(sffn_layer_t layer, const void* x, float* y, void* stream);
+
 /* Predictor scores s = U (V x) + pb as float32 [batch][d_ff] (diagnostics:
  * the same kernels as sffn_predict, scores written out). */
 sffn_status sffn_predict_scores(sffn_layer_t layer, const void* x, int32_t batch, float* scores,

@@ -15,7 +15,7 @@ CSRC = os.path.join(HERE, "csrc")
 OUT_DIR = os.path.join(HERE, "_build")
 LIB = os.path.join(HERE, "libsffn.so")
 SOURCES = ["api.cu", "predict.cu", "misc.cu", "gather_f32.cu", "gather_f16.cu", "gather_bf16.cu",
-           "layer_f32.cu", "layer_f16.cu", "layer_bf16.cu", "noalloc.cu"]
+           "layer_f32.cu", "layer_f16.cu", "layer_bf16.cu", "union_f16.cu", "union_bf16.cu", "noalloc.cu"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 FLAGS = ["-O3", "-std=c++17", "-lineinfo", "-Xcompiler", "-fPIC", "--expt-relaxed-constexpr",
          "-I", os.path.join(os.path.dirname(HERE), "include")]

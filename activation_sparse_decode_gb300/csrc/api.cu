@@ -207,6 +207,44 @@ sffn_status run_gather(const sffn_layer* L, const void* x, int batch, float* y, 
   return SFFN_OK;
 }
 
+// Batches this large (and 16-bit weights) go to the tensor-core union path.
+constexpr int kUnionMinBatch = 8;
+
+bool use_union(const sffn_layer* L, int batch, UnionConfig* cfg) {
+  const auto& d = L->desc;
+  if (batch < kUnionMinBatch || (d.flags & SFFN_FLAG_ROW_GATHER)) return false;
+  return union_config(d.dtype, d.act, d.d_model, d.d_ff, batch, L->gather_grid, L->smem_optin, cfg);
+}
+
+// The sparse products of a batch whose mask words are in the workspace.
+sffn_status run_sparse_ffn(const sffn_layer* L, const void* x, int batch, float* y, const Ws& ws, cudaStream_t s) {
+  UnionConfig uc{};
+  if (!use_union(L, batch, &uc)) return run_gather(L, x, batch, y, ws, false, s);
+  const auto& d = L->desc;
+  SFFN_CUDA(cudaMemsetAsync(y, 0, (size_t)batch * d.d_model * sizeof(float), s), "output clear");
+  UnionArgs a{};
+  a.x = x;
+  a.w_up = d.w_up;
+  a.w_gate = d.w_gate;
+  a.w_downT = d.w_downT;
+  a.b = d.b;
+  a.mask = ws.mask();
+  a.y = y;
+  a.hdr = ws.hdr();
+  a.B = batch;
+  a.d = d.d_model;
+  a.f = d.d_ff;
+  a.W = L->W;
+  a.act = d.act;
+  a.list_cap = uc.list_cap;
+  a.ring_bytes = uc.ring_bytes;
+  a.wait_ns = (uint64_t)g_wait_ns;
+  if (g_prof_start != nullptr) SFFN_TRY(record_profile_event(g_prof_start, s));
+  SFFN_CUDA(launch_union(d.dtype, uc, a, L->gather_grid, s), "union launch");
+  if (g_prof_stop != nullptr) SFFN_TRY(record_profile_event(g_prof_stop, s));
+  return SFFN_OK;
+}
+
 sffn_status check_x(const sffn_layer* L, const void* x) { return check_dev_ptr(x, "x"); }
 
 // One token through the single-launch layer kernel.  With y_prev, the kernel
@@ -306,6 +344,8 @@ sffn_status sffn_create_layer(const sffn_layer_desc* desc, sffn_layer_t* out) {
   if (d.d_model <= 0 || d.d_ff <= 0 || d.rank <= 0)
     return fail(SFFN_ERR_INVALID_ARG, "d_model, d_ff and rank must be positive");
   if (d.max_batch < 1 || d.max_batch > 32) return fail(SFFN_ERR_INVALID_ARG, "max_batch must be in [1, 32]");
+  if (d.flags & ~(SFFN_FLAG_MULTI_KERNEL | SFFN_FLAG_BALANCE | SFFN_FLAG_ROW_GATHER))
+    return fail(SFFN_ERR_INVALID_ARG, "unknown flag bits 0x%x", (unsigned)d.flags);
   const int esize = d.dtype == SFFN_F32 ? 4 : 2;
   if (((size_t)d.d_model * esize) % 16 != 0)
     return fail(SFFN_ERR_INVALID_ARG, "d_model * sizeof(dtype) must be a multiple of 16");
@@ -438,7 +478,7 @@ sffn_status sffn_forward(sffn_layer_t L, const void* x, int32_t batch, float* y,
   SFFN_TRY(run_predictor(L, x, batch, ws, nullptr, s));
   if (idx_out != nullptr)
     SFFN_CUDA(launch_compact(ws.mask(), batch, L->desc.d_ff, L->W, idx_out, n_active_out, s), "compaction launch");
-  return run_gather(L, x, batch, y, ws, false, s);
+  return run_sparse_ffn(L, x, batch, y, ws, s);
 }
 
 sffn_status sffn_dense_forward(sffn_layer_t L, const void* x, int32_t batch, float* y, void* workspace,
@@ -577,7 +617,7 @@ sffn_status sffn_forward_stack(const sffn_layer_t* layers, int32_t n_layers, con
       Ws ws;
       SFFN_TRY(check_ws(L, batch, workspace, per, &ws));
       SFFN_TRY(run_predictor(L, xin, batch, ws, nullptr, s));
-      SFFN_TRY(run_gather(L, xin, batch, ybuf, ws, false, s));
+      SFFN_TRY(run_sparse_ffn(L, xin, batch, ybuf, ws, s));
       void* xnext = (l == n_layers - 1) ? static_cast<void*>(xo + (size_t)t * xbytes) : xbuf[l & 1];
       SFFN_CUDA(launch_residual_layernorm(d0.dtype, xin, ybuf, batch, d0.d_model, ln_gamma, ln_beta, ln_eps,
                                           xnext, s),

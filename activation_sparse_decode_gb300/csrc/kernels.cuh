@@ -111,6 +111,33 @@ struct LayerConfig {
 bool layer_config(int dtype, int act, int d, int f, int r, int grid, size_t smem_optin, LayerConfig* cfg);
 cudaError_t launch_layer(int dtype, const LayerConfig& cfg, const LayerArgs& a, int grid, cudaStream_t s);
 
+// ---- batched decode over the union of the tokens' active rows (tensor cores)
+struct UnionArgs {
+  const void* x;          // [B][d] tokens
+  const void* w_up;
+  const void* w_gate;     // ReGLU only
+  const void* w_downT;
+  const float* b;         // NULL or [f]
+  const uint32_t* mask;   // [B][W] predicted bits
+  float* y;               // [B][d]: zero on entry, accumulated with float atomics
+  WsHeader* hdr;
+  int B, d, f, W, act;
+  int list_cap;           // >= the most union members one block can get
+  size_t ring_bytes;      // shared memory of the copy ring
+  uint64_t wait_ns;
+};
+constexpr int kUnionThreads = 416;       // 4 epilogue warps, 1 MMA warp, 8 copy warps
+constexpr int kUnionMaxWpt = 4;          // mask words per thread in the union scan
+constexpr int kUnionMaxSlots = 16;
+constexpr size_t kUnionAtBytes = 16384;  // GEMM2 B operand (128 neurons x 64 columns x 2 bytes)
+struct UnionConfig {
+  int bt;                 // token columns of the tiles: 8, 16 or 32
+  int list_cap;
+  size_t ring_bytes, smem;
+};
+bool union_config(int dtype, int act, int d, int f, int B, int grid, size_t smem_optin, UnionConfig* cfg);
+cudaError_t launch_union(int dtype, const UnionConfig& cfg, const UnionArgs& a, int grid, cudaStream_t s);
+
 // ---- residual + LayerNorm: x_out = round(LN(x + y) * gamma + beta)
 cudaError_t launch_residual_layernorm(int dtype, const void* x, const float* y, int B, int d,
                                       const float* gamma, const float* beta, float eps, void* x_out,

@@ -215,6 +215,40 @@ bool layer_config(int dtype, int act, int d, int f, int r, int grid, size_t smem
   return cfg->smem + reserve <= smem_optin;
 }
 
+bool union_config(int dtype, int act, int d, int f, int B, int grid, size_t smem_optin, UnionConfig* cfg) {
+  if (dtype != kF16 && dtype != kBF16) return false;  // 16-bit tensor-core operands
+  if (d % 128 != 0 || B < 1 || B > 32) return false;
+  const int W = (f + 31) / 32;
+  if (W > kUnionMaxWpt * kUnionThreads) return false;
+  const int bt = B <= 8 ? 8 : B <= 16 ? 16 : 32;
+  const int n1 = std::max(16, bt);
+  const int nm = act == kReglu ? 2 : 1;
+  const int list_cap = (f + grid - 1) / grid + 1;
+  if ((size_t)(list_cap + 1) * 8 > kUnionAtBytes) return false;  // word list scratch
+  const size_t max_slot = std::max<size_t>((size_t)nm * 128 * 128 + (size_t)n1 * 128, 128 * 256);
+  const size_t lists = ((size_t)list_cap * 12 + 1023) / 1024 * 1024;  // neuron, token bits, bias
+  const size_t reserve = 2048;                                        // static shared memory
+  if (smem_optin < reserve + kUnionAtBytes + lists + 2 * max_slot) return false;
+  const size_t ring = std::min<size_t>(kUnionMaxSlots * max_slot,
+                                       (smem_optin - reserve - kUnionAtBytes - lists) / 1024 * 1024);
+  cfg->bt = bt;
+  cfg->list_cap = list_cap;
+  cfg->ring_bytes = ring;
+  cfg->smem = ring + kUnionAtBytes + lists;
+  return true;
+}
+
+cudaError_t launch_union_f16(const UnionConfig&, const UnionArgs&, int, cudaStream_t);
+cudaError_t launch_union_bf16(const UnionConfig&, const UnionArgs&, int, cudaStream_t);
+
+cudaError_t launch_union(int dtype, const UnionConfig& cfg, const UnionArgs& a, int grid, cudaStream_t s) {
+  switch (dtype) {
+    case kF16: return launch_union_f16(cfg, a, grid, s);
+    case kBF16: return launch_union_bf16(cfg, a, grid, s);
+  }
+  return cudaErrorInvalidValue;
+}
+
 cudaError_t launch_layer_f32(const LayerConfig&, const LayerArgs&, int, cudaStream_t);
 cudaError_t launch_layer_f16(const LayerConfig&, const LayerArgs&, int, cudaStream_t);
 cudaError_t launch_layer_bf16(const LayerConfig&, const LayerArgs&, int, cudaStream_t);

@@ -97,3 +97,19 @@ def check_next_input(x_next_gpu, x_next_oracle, fmt):
     err = np.abs(g - o) / np.maximum(np.abs(o), 2.0 ** -6)
     assert err.max() <= 1.01 * ulp + 1e-5, err.max()
     assert (g != o).mean() < 0.05
+
+
+def run_tokens(sffn, layer, X, want_idx=True, device="cuda"):
+    """Decode the tokens X [T][B][d] one step at a time (batch B per step);
+    returns outputs, active lists and counts as numpy arrays."""
+    T, B, d = X.shape
+    f = layer.d_ff
+    ws = sffn.new_workspace(sffn.sffn_workspace_size(layer, B), device)
+    Y = torch.empty(T, B, d, dtype=torch.float32, device=device)
+    I = torch.empty(T, B, f, dtype=torch.int32, device=device) if want_idx else None
+    N = torch.empty(T, B, dtype=torch.int32, device=device) if want_idx else None
+    for t in range(T):
+        sffn.sffn_forward(layer, X[t], Y[t], ws, None if I is None else I[t], None if N is None else N[t])
+    torch.cuda.synchronize()
+    assert sffn.sffn_read_device_status(ws) == 0
+    return Y.cpu().numpy(), None if I is None else I.cpu().numpy(), None if N is None else N.cpu().numpy()

@@ -9,7 +9,7 @@ import torch
 import oracle
 from activation_sparse_decode_gb300 import workloads as W
 from activation_sparse_decode_gb300.workloads import to_numpy_stored as st
-from gpu_helpers import TOL, check_token, hot_first, mask_from_list, oracle_layer, rel_l2
+from gpu_helpers import TOL, check_token, hot_first, mask_from_list, oracle_layer, rel_l2, run_tokens
 
 pytestmark = pytest.mark.gpu
 
@@ -24,21 +24,6 @@ def sffn():
     build.build()
     from activation_sparse_decode_gb300 import sffn as mod
     return mod
-
-
-def run_tokens(sffn, layer, X, want_idx=True):
-    """Decode the tokens X [T][B][d] one step at a time (batch B per step)."""
-    T, B, d = X.shape
-    f = layer.d_ff
-    ws = sffn.new_workspace(sffn.sffn_workspace_size(layer, B), DEV)
-    Y = torch.empty(T, B, d, dtype=torch.float32, device=DEV)
-    I = torch.empty(T, B, f, dtype=torch.int32, device=DEV) if want_idx else None
-    N = torch.empty(T, B, dtype=torch.int32, device=DEV) if want_idx else None
-    for t in range(T):
-        sffn.sffn_forward(layer, X[t], Y[t], ws, None if I is None else I[t], None if N is None else N[t])
-    torch.cuda.synchronize()
-    assert sffn.sffn_read_device_status(ws) == 0
-    return Y.cpu().numpy(), None if I is None else I.cpu().numpy(), None if N is None else N.cpu().numpy()
 
 
 # ---------------------------------------------------------------- ReLU FFN d1024 f4096 fp32 (64 tokens)

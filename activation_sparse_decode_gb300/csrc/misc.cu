@@ -225,7 +225,7 @@ bool union_config(int dtype, int act, int d, int f, int B, int grid, size_t smem
   const int nm = act == kReglu ? 2 : 1;
   const int list_cap = (f + grid - 1) / grid + 1;
   if ((size_t)(list_cap + 1) * 8 > kUnionAtBytes) return false;  // word list scratch
-  const size_t max_slot = std::max<size_t>((size_t)nm * 128 * 128 + (size_t)n1 * 128, 128 * 256);
+  const size_t max_slot = std::max<size_t>(((size_t)nm * 128 + n1) * 128, 128 * 256);
   const size_t lists = ((size_t)list_cap * 12 + 1023) / 1024 * 1024;  // neuron, token bits, bias
   const size_t reserve = 2048;                                        // static shared memory
   if (smem_optin < reserve + kUnionAtBytes + lists + 2 * max_slot) return false;

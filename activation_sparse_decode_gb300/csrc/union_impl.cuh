@@ -31,11 +31,18 @@
 // with per-thread 16-byte cp.async into a ring of slots whose mbarriers count
 // one arrival per copying thread.
 //
-// Shared-memory operand layouts (no swizzle; 8x16-byte core matrices):
-//   K-major  (GEMM1 A and B, GEMM2 B): element (row, k) at
-//            (k/8)*LBO + row*16 + (k%8)*2, LBO = rows*16, SBO = 128;
-//   MN-major (GEMM2 A = W_downT rows): element (m, k) at
-//            (m/8)*SBO + k*16 + (m%8)*2, LBO = 128 (next 8 k), SBO = K*16.
+// Shared-memory operand layouts.  Copied operands use the tensor cores'
+// 128-byte swizzled layouts, so that every 128-byte line a copy brings in
+// lands in 128 contiguous bytes of shared memory (the 16-byte pieces permuted
+// by the row index):
+//   GEMM1 A (gathered W_up / W_gate rows) and B (tokens): K-major, one 128-byte
+//     row per neuron / token (64 elements of d), 8-row groups 1024 bytes apart;
+//   GEMM2 A (gathered W_downT rows, 128 elements of d): MN-major, the two
+//     64-element halves of d K2*128 bytes apart, rows in 1024-byte groups of 8.
+// GEMM2 B (the activations, written by the epilogue) is not swizzled: K-major
+// 8x16-byte core matrices, element (n, k) at (k/8)*LBO + n*16 + (k%8)*2, with
+// LBO = N*16 + 16 so that the 2-byte stores of neighbouring lanes spread over
+// the banks.
 
 #pragma once
 
@@ -56,6 +63,7 @@ constexpr int kNAcc = 4;          // GEMM2 accumulators in flight
 constexpr int kKc = 64;           // columns of d per GEMM1 job (one 128-byte line per 16-bit row)
 constexpr int kDTile = 128;       // rows of d per GEMM2 job
 constexpr int kMaxTile = 128;     // neurons per tile (the MMA's M)
+constexpr int kPieces = 8;        // 16-byte pieces a copying thread owns per job (2 x 128 rows x 8 / 256)
 constexpr int kMaxWpt = kUnionMaxWpt;  // mask words per thread in the union scan
 constexpr int kTmemCols = 512;
 constexpr int kColUp = 0, kColGate = 32, kColAcc = 64, kAccStride = 64;
@@ -63,7 +71,8 @@ constexpr size_t kAtBytes = kUnionAtBytes;
 
 // Detail codes of the device status word (which wait gave up).
 enum : uint32_t { kDetFull = 0x5100, kDetEmpty = 0x5200, kDetD1 = 0x5300, kDetAt = 0x5400,
-                  kDetAccFull = 0x5500, kDetAccEmpty = 0x5600, kDetDone = 0x5700 };
+                  kDetAccFull = 0x5500, kDetAccEmpty = 0x5600, kDetDone = 0x5700,
+                  kDetAlign = 0x5800 };
 
 // tcgen05 shared-memory matrix descriptor, no swizzle (version field = 1).
 __device__ __forceinline__ uint64_t sdesc(uint32_t addr, uint32_t lbo, uint32_t sbo) {
@@ -120,6 +129,34 @@ template <typename T> __device__ __forceinline__ float to_float(T v);
 template <> __device__ __forceinline__ float to_float<__half>(__half v) { return __half2float(v); }
 template <> __device__ __forceinline__ float to_float<__nv_bfloat16>(__nv_bfloat16 v) { return __bfloat162float(v); }
 
+
+// Shared-memory matrix descriptor with 128-byte swizzling (layout type 2).
+__device__ __forceinline__ uint64_t sdesc_sw128(uint32_t addr, uint32_t lbo, uint32_t sbo) {
+  return sdesc(addr, lbo, sbo) | (2ull << 61);
+}
+
+// 128-byte-swizzled K-major tile: row `row` is 128 contiguous bytes (64
+//16-bit elements of K); its 16-byte piece c sits at position c ^ (row % 8).
+// Tiles start on 1024-byte boundaries (8 rows).
+__device__ __forceinline__ uint32_t sw128_k(int row, int c) {
+  return (uint32_t)(row * 128 + ((c ^ (row & 7)) << 4));
+}
+
+// 128-byte-swizzled MN-major tile of W_downT rows (k = neuron, 128 elements
+// of d): 16-byte piece c16 of row k; the two 64-element halves of d are
+// K2*128 bytes apart, rows k form 1024-byte groups of 8.
+__device__ __forceinline__ uint32_t sw128_mn(int k, int c16, int K2) {
+  return (uint32_t)((c16 >> 3) * (K2 * 128) + (k >> 3) * 1024 + (k & 7) * 128 + (((c16 & 7) ^ (k & 7)) << 4));
+}
+
+// Job order of block-dependent rotation: block b starts its walk over the
+// n column chunks at chunk `o`, so that the blocks do not all read the same
+// token columns or add into the same output rows at the same moment.
+__device__ __forceinline__ int rot(int j, int o, int n) {
+  const int v = j + o;
+  return v >= n ? v - n : v;
+}
+
 // Rows of tile t when n members are split into nt near-equal tiles.
 __device__ __forceinline__ int tile_begin(int t, int n, int nt) { return (int)(((long long)t * n) / nt); }
 
@@ -131,6 +168,7 @@ __global__ void __launch_bounds__(un::kThreads, 1) k_union(UnionArgs a) {
   using namespace un;
   constexpr int N1 = BT < 16 ? 16 : BT;  // GEMM1 token columns (M = 128 needs N % 16 == 0)
   constexpr int N2 = 2 * BT;             // GEMM2 columns: high parts, then remainders
+  constexpr int kLa = N2 * 16 + 16;      // activation operand: the same
   constexpr int kWarps = kThreads / 32;
   extern __shared__ __align__(1024) unsigned char dsm[];
   __shared__ __align__(8) uint64_t bars[2 * kMaxSlots + 2 * kNAcc + 3];
@@ -147,6 +185,10 @@ __global__ void __launch_bounds__(un::kThreads, 1) k_union(UnionArgs a) {
 
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const int B = a.B, d = a.d, W = a.W;
+  if (smem_addr(dsm) & 1023u) {  // swizzled tiles need 1024-byte alignment
+    if (tid == 0) set_status(a.hdr, kStCapacity, kDetAlign);
+    return;
+  }
   const int nm = a.act == kReglu ? 2 : 1;
   unsigned char* ring = dsm;
   unsigned char* at = dsm + a.ring_bytes;
@@ -235,14 +277,14 @@ __global__ void __launch_bounds__(un::kThreads, 1) k_union(UnionArgs a) {
   const int rmax = (nc + nt - 1) / nt;
   const int r8max = (rmax + 7) & ~7, k2max = (rmax + 15) & ~15;
   const uint32_t slot_bytes =
-      ((uint32_t)max(nm * r8max * 128 + N1 * 128, k2max * 256) + 127u) & ~127u;
+      ((uint32_t)max((nm * r8max + N1) * 128, k2max * 256) + 1023u) & ~1023u;
   const int S = min(kMaxSlots, (int)(a.ring_bytes / slot_bytes));
   for (int t = 0; t < nt; ++t) {
     const int R = tile_begin(t + 1, nc, nt) - tile_begin(t, nc, nt);
     const int K2 = (R + 15) & ~15, pad = K2 - R;
-    for (int e = tid; e < S * 16 * pad; e += kThreads) {
-      const int s = e / (16 * pad), rem = e - s * 16 * pad, g = rem / pad, k = R + (rem - g * pad);
-      *reinterpret_cast<uint4*>(ring + (size_t)s * slot_bytes + g * (K2 * 16) + k * 16) = make_uint4(0, 0, 0, 0);
+    for (int e = tid; e < S * 16 * pad; e += kThreads) {  // 16 pieces of 16 bytes per padded row
+      const int s = e / (16 * pad), rem = e - s * 16 * pad, k = R + rem / 16, c16 = rem & 15;
+      *reinterpret_cast<uint4*>(ring + (size_t)s * slot_bytes + sw128_mn(k, c16, K2)) = make_uint4(0, 0, 0, 0);
     }
   }
   if (tid == 0) {
@@ -270,15 +312,19 @@ __global__ void __launch_bounds__(un::kThreads, 1) k_union(UnionArgs a) {
   tc_fence_after();
   const uint32_t tmem = s_tmem;
   const int nk = d / kKc, nd = d / kDTile;
+  const int off1 = (int)((blockIdx.x * 7u) % (unsigned)nk), off2 = (int)((blockIdx.x * 5u) % (unsigned)nd);
 
   if (warp > kMmaWarp) {
     // ---- 3a. copies: GEMM1 jobs (W_up/W_gate columns [k0, k0+64) of the
-    // tile's rows, and the tokens), then GEMM2 jobs (W_downT columns [d0, d0+128))
+    // tile's rows, and the tokens), then GEMM2 jobs (W_downT columns
+    // [d0, d0+128)).  A thread copies the same pieces of the same rows in every
+    // job of a phase, so their addresses are formed once per tile.
     const int p = tid - kProdTid0;
-    const T* xg = static_cast<const T*>(a.x);
-    const T* wu = static_cast<const T*>(a.w_up);
-    const T* wg = static_cast<const T*>(a.w_gate);
-    const T* wd = static_cast<const T*>(a.w_downT);
+    const char* xg = static_cast<const char*>(a.x);
+    const char* wu = static_cast<const char*>(a.w_up);
+    const char* wg = static_cast<const char*>(a.w_gate);
+    const char* wd = static_cast<const char*>(a.w_downT);
+    const size_t rowb = (size_t)d * sizeof(T);
     int s = 0, job = 0;
     uint32_t ph = 0;
     bool ok = true;
@@ -286,33 +332,69 @@ __global__ void __launch_bounds__(un::kThreads, 1) k_union(UnionArgs a) {
       const int r0 = tile_begin(t, nc, nt), R = tile_begin(t + 1, nc, nt) - r0;
       const int R8 = (R + 7) & ~7, K2 = (R + 15) & ~15;
       const int32_t* ti = nidx + r0;
-      for (int j = 0; j < nk + nd; ++j, ++job) {
+      const char* src[kPieces];
+      uint32_t dst[kPieces];
+      int np = 0;
+#pragma unroll
+      for (int q = 0; q < kPieces; ++q) {  // GEMM1: 8 pieces of 16 bytes per row and matrix
+        const int e = p + q * kProdThreads;
+        src[q] = nullptr;
+        dst[q] = 0;
+        if (e < nm * R * 8) {
+          const int m = e >= R * 8 ? 1 : 0, rem = e - m * R * 8, r = rem >> 3, c = rem & 7;
+          src[q] = (m ? wg : wu) + (size_t)ti[r] * rowb + c * 16;
+          dst[q] = sw128_k(m * R8 + r, c);
+          np = q + 1;
+        }
+      }
+      const char* srcx = nullptr;
+      uint32_t dstx = 0;
+      if (p < B * 8) {
+        const int n = p >> 3, c = p & 7;
+        srcx = xg + (size_t)n * rowb + c * 16;
+        dstx = sw128_k(nm * R8 + n, c);
+      }
+      for (int j = 0; j < nk; ++j, ++job) {
         if (job >= S && !mbar_wait(&empty[s], ph ^ 1u, a.hdr, a.wait_ns, kDetEmpty)) {
           ok = false;
           break;
         }
         unsigned char* sl = ring + (size_t)s * slot_bytes;
-        if (j < nk) {
-          const int k0 = j * kKc;
-          for (int m = 0; m < nm; ++m) {
-            const T* wmat = m == 0 ? wu : wg;
-            unsigned char* dst = sl + m * R8 * 128;
-            for (int e = p; e < R * 8; e += kProdThreads) {
-              const int r = e >> 3, c = e & 7;
-              cp_async16(dst + c * (R8 * 16) + r * 16, wmat + (size_t)ti[r] * d + k0 + c * 8);
-            }
-          }
-          if (p < B * 8) {
-            const int n = p >> 3, c = p & 7;
-            cp_async16(sl + nm * R8 * 128 + c * (N1 * 16) + n * 16, xg + (size_t)n * d + k0 + c * 8);
-          }
-        } else {
-          const int d0 = (j - nk) * kDTile;
-          for (int e = p; e < R * 16; e += kProdThreads) {
-            const int r = e >> 4, g = e & 15;
-            cp_async16(sl + g * (K2 * 16) + r * 16, wd + (size_t)ti[r] * d + d0 + g * 8);
-          }
+        const size_t off = (size_t)rot(j, off1, nk) * (kKc * sizeof(T));
+#pragma unroll
+        for (int q = 0; q < kPieces; ++q)
+          if (q < np) cp_async16(sl + dst[q], src[q] + off);
+        if (srcx != nullptr) cp_async16(sl + dstx, srcx + off);
+        cp_async_arrive_noinc(&full[s]);
+        if (++s == S) {
+          s = 0;
+          ph ^= 1u;
         }
+      }
+      if (!ok) break;
+      np = 0;
+#pragma unroll
+      for (int q = 0; q < kPieces; ++q) {  // GEMM2: 16 pieces of 16 bytes per row
+        const int e = p + q * kProdThreads;
+        src[q] = nullptr;
+        dst[q] = 0;
+        if (e < R * 16) {
+          const int r = e >> 4, c16 = e & 15;
+          src[q] = wd + (size_t)ti[r] * rowb + c16 * 16;
+          dst[q] = sw128_mn(r, c16, K2);
+          np = q + 1;
+        }
+      }
+      for (int j = 0; j < nd; ++j, ++job) {
+        if (job >= S && !mbar_wait(&empty[s], ph ^ 1u, a.hdr, a.wait_ns, kDetEmpty)) {
+          ok = false;
+          break;
+        }
+        unsigned char* sl = ring + (size_t)s * slot_bytes;
+        const size_t off = (size_t)rot(j, off2, nd) * (kDTile * sizeof(T));
+#pragma unroll
+        for (int q = 0; q < kPieces; ++q)
+          if (q < np) cp_async16(sl + dst[q], src[q] + off);
         cp_async_arrive_noinc(&full[s]);
         if (++s == S) {
           s = 0;
@@ -340,13 +422,13 @@ __global__ void __launch_bounds__(un::kThreads, 1) k_union(UnionArgs a) {
           proxy_fence();
           tc_fence_after();
           const uint32_t sl = ring_a + (uint32_t)s * slot_bytes;
-          const uint32_t xa = sl + nm * R8 * 128;
+          const uint32_t xa = sl + (uint32_t)(nm * R8) * 128;
 #pragma unroll
-          for (int kk = 0; kk < kKc / 16; ++kk) {
-            const uint64_t bd = sdesc(xa + kk * 2 * N1 * 16, N1 * 16, 128);
+          for (int kk = 0; kk < kKc / 16; ++kk) {  // a K step of 16 is 32 bytes inside the 128-byte rows
+            const uint64_t bd = sdesc_sw128(xa + kk * 32, 16, 1024);
             const uint32_t acc = (j | kk) != 0;
-            mma(tmem + kColUp, sdesc(sl + kk * 2 * R8 * 16, R8 * 16, 128), bd, id1, acc);
-            if (nm == 2) mma(tmem + kColGate, sdesc(sl + R8 * 128 + kk * 2 * R8 * 16, R8 * 16, 128), bd, id1, acc);
+            mma(tmem + kColUp, sdesc_sw128(sl + kk * 32, 16, 1024), bd, id1, acc);
+            if (nm == 2) mma(tmem + kColGate, sdesc_sw128(sl + R8 * 128 + kk * 32, 16, 1024), bd, id1, acc);
           }
           mma_commit(&empty[s]);
           if (++s == S) {
@@ -371,8 +453,8 @@ __global__ void __launch_bounds__(un::kThreads, 1) k_union(UnionArgs a) {
           tc_fence_after();
           const uint32_t sl = ring_a + (uint32_t)s * slot_bytes;
           const uint32_t dt = tmem + kColAcc + buf * kAccStride;
-          for (int kk = 0; kk < K2 / 16; ++kk)
-            mma(dt, sdesc(sl + kk * 256, 128, K2 * 16), sdesc(at_a + kk * 2 * N2 * 16, N2 * 16, 128), id2, kk != 0);
+          for (int kk = 0; kk < K2 / 16; ++kk)  // a K step of 16 rows is two 1024-byte row groups
+            mma(dt, sdesc_sw128(sl + kk * 2048, K2 * 128, 1024), sdesc(at_a + kk * 2 * kLa, kLa, 128), id2, kk != 0);
           mma_commit(&empty[s]);
           mma_commit(&accf[buf]);
           if (++s == S) {
@@ -401,7 +483,7 @@ __global__ void __launch_bounds__(un::kThreads, 1) k_union(UnionArgs a) {
         tb = tbits[r0 + m];
         bias = nbias[r0 + m];
       }
-      unsigned char* col = at + (m >> 3) * (N2 * 16) + (m & 7) * 2;
+      unsigned char* col = at + (m >> 3) * kLa + (m & 7) * 2;
 #pragma unroll
       for (int c = 0; c < N1; c += 16) {
         float u[16], g[16];
@@ -433,7 +515,7 @@ __global__ void __launch_bounds__(un::kThreads, 1) k_union(UnionArgs a) {
         }
         tc_fence_after();
         const uint32_t acc_t = tmem + lane_base + kColAcc + buf * kAccStride;
-        float* yr = a.y + (size_t)j * kDTile + m;
+        float* yr = a.y + (size_t)rot(j, off2, nd) * kDTile + m;
 #pragma unroll
         for (int c = 0; c < BT; c += 16) {
           float vh[16], vl[16];

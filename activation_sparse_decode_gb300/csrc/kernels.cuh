@@ -128,7 +128,7 @@ struct UnionArgs {
 };
 constexpr int kUnionThreads = 416;       // 4 epilogue warps, 1 MMA warp, 8 copy warps
 constexpr int kUnionMaxWpt = 4;          // mask words per thread in the union scan
-constexpr int kUnionMaxSlots = 16;
+constexpr int kUnionMaxSlots = 32;
 constexpr size_t kUnionAtBytes = 17408;  // GEMM2 B operand (128 neurons x 64 columns x 2 bytes, padded)
 struct UnionConfig {
   int bt;                 // token columns of the tiles: 8, 16 or 32

@@ -59,14 +59,15 @@ static_assert(kThreads == (kEpiWarps + 1 + kProdWarps) * 32, "warp roles");
 constexpr int kProdThreads = kProdWarps * 32;
 constexpr int kProdTid0 = (kEpiWarps + 1) * 32;
 constexpr int kMaxSlots = kUnionMaxSlots;
-constexpr int kNAcc = 4;          // GEMM2 accumulators in flight
+constexpr int kMaxAcc = 8;        // GEMM2 accumulators in flight, at most
 constexpr int kKc = 64;           // columns of d per GEMM1 job (one 128-byte line per 16-bit row)
 constexpr int kDTile = 128;       // rows of d per GEMM2 job
 constexpr int kMaxTile = 128;     // neurons per tile (the MMA's M)
 constexpr int kPieces = 8;        // 16-byte pieces a copying thread owns per job (2 x 128 rows x 8 / 256)
 constexpr int kMaxWpt = kUnionMaxWpt;  // mask words per thread in the union scan
 constexpr int kTmemCols = 512;
-constexpr int kColUp = 0, kColGate = 32, kColAcc = 64, kAccStride = 64;
+constexpr int kColUp = 0, kColGate = 32, kColAcc = 64;  // GEMM2 accumulators from column 64 on
+constexpr int kXPieces = 4;       // token pieces a copying thread owns per job (up to 4 x 32 x 8 / 256)
 constexpr size_t kAtBytes = kUnionAtBytes;
 
 // Detail codes of the device status word (which wait gave up).
@@ -168,18 +169,19 @@ __global__ void __launch_bounds__(un::kThreads, 1) k_union(UnionArgs a) {
   using namespace un;
   constexpr int N1 = BT < 16 ? 16 : BT;  // GEMM1 token columns (M = 128 needs N % 16 == 0)
   constexpr int N2 = 2 * BT;             // GEMM2 columns: high parts, then remainders
-  constexpr int kLa = N2 * 16 + 16;      // activation operand: the same
+  constexpr int kLa = N2 * 16 + 16;      // activation operand: stride of its 8-neuron core-matrix blocks
+  constexpr int kNAcc = (kTmemCols - kColAcc) / N2 < kMaxAcc ? (kTmemCols - kColAcc) / N2 : kMaxAcc;
   constexpr int kWarps = kThreads / 32;
   extern __shared__ __align__(1024) unsigned char dsm[];
-  __shared__ __align__(8) uint64_t bars[2 * kMaxSlots + 2 * kNAcc + 3];
+  __shared__ __align__(8) uint64_t bars[2 * kMaxSlots + 2 * kMaxAcc + 3];
   __shared__ uint32_t s_tmem;
   __shared__ int s_scan[kWarps];
   __shared__ int s_nwords;
   uint64_t* full = bars;
   uint64_t* empty = bars + kMaxSlots;
   uint64_t* accf = bars + 2 * kMaxSlots;
-  uint64_t* acce = accf + kNAcc;
-  uint64_t* d1f = acce + kNAcc;
+  uint64_t* acce = accf + kMaxAcc;
+  uint64_t* d1f = acce + kMaxAcc;
   uint64_t* atr = d1f + 1;
   uint64_t* done = atr + 1;
 
@@ -270,21 +272,32 @@ __global__ void __launch_bounds__(un::kThreads, 1) k_union(UnionArgs a) {
     }
   }
 
-  // ---- 2. tiles, slots; W_downT rows past a tile's end (up to the next 16)
-  // are read by GEMM2 against zero activations, so they must hold finite
-  // values: zero them once in every slot (copies only ever write weights).
+  // ---- 2. tiles and jobs.  A block's members form nt near-equal tiles of at
+  // most 128 neurons.  A GEMM1 job covers KA column chunks of 64 (KA x 128
+  // bytes of every gathered row), a GEMM2 job DA output tiles of 128 rows of d;
+  // both widen when the tiles are short, so that every job moves enough bytes
+  // to amortise its hand-offs.  A thread owns at most kPieces pieces per job.
+  const int nk = d / kKc, nd = d / kDTile;
   const int nt = (nc + kMaxTile - 1) / kMaxTile;
   const int rmax = (nc + nt - 1) / nt;
   const int r8max = (rmax + 7) & ~7, k2max = (rmax + 15) & ~15;
+  int KA = 1, DA = 1;
+  while (KA < 4 && 2 * KA * nm * r8max <= kPieces * kProdThreads / 8 && nk % (2 * KA) == 0) KA *= 2;
+  while (DA < 4 && 2 * DA * k2max <= kPieces * kProdThreads / 16 && nd % (2 * DA) == 0 && 2 * DA <= kNAcc / 2) DA *= 2;
   const uint32_t slot_bytes =
-      ((uint32_t)max((nm * r8max + N1) * 128, k2max * 256) + 1023u) & ~1023u;
+      ((uint32_t)max(KA * (nm * r8max + N1) * 128, DA * k2max * 256) + 1023u) & ~1023u;
   const int S = min(kMaxSlots, (int)(a.ring_bytes / slot_bytes));
+  // W_downT rows past a tile's end (up to the next 16) are read by GEMM2
+  // against zero activations, so they must hold finite values: zero them once
+  // in every slot (copies only ever write weights and tokens there).
   for (int t = 0; t < nt; ++t) {
     const int R = tile_begin(t + 1, nc, nt) - tile_begin(t, nc, nt);
     const int K2 = (R + 15) & ~15, pad = K2 - R;
-    for (int e = tid; e < S * 16 * pad; e += kThreads) {  // 16 pieces of 16 bytes per padded row
-      const int s = e / (16 * pad), rem = e - s * 16 * pad, k = R + rem / 16, c16 = rem & 15;
-      *reinterpret_cast<uint4*>(ring + (size_t)s * slot_bytes + sw128_mn(k, c16, K2)) = make_uint4(0, 0, 0, 0);
+    for (int e = tid; e < S * DA * 16 * pad; e += kThreads) {  // 16 pieces of 16 bytes per padded row
+      const int s = e / (DA * 16 * pad), rem = e - s * DA * 16 * pad, q = rem / (16 * pad),
+                rem2 = rem - q * 16 * pad, k = R + rem2 / 16, c16 = rem2 & 15;
+      *reinterpret_cast<uint4*>(ring + (size_t)s * slot_bytes + q * K2 * 256 + sw128_mn(k, c16, K2)) =
+          make_uint4(0, 0, 0, 0);
     }
   }
   if (tid == 0) {
@@ -311,14 +324,13 @@ __global__ void __launch_bounds__(un::kThreads, 1) k_union(UnionArgs a) {
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem = s_tmem;
-  const int nk = d / kKc, nd = d / kDTile;
   const int off1 = (int)((blockIdx.x * 7u) % (unsigned)nk), off2 = (int)((blockIdx.x * 5u) % (unsigned)nd);
 
   if (warp > kMmaWarp) {
-    // ---- 3a. copies: GEMM1 jobs (W_up/W_gate columns [k0, k0+64) of the
-    // tile's rows, and the tokens), then GEMM2 jobs (W_downT columns
-    // [d0, d0+128)).  A thread copies the same pieces of the same rows in every
-    // job of a phase, so their addresses are formed once per tile.
+    // ---- 3a. copies: GEMM1 jobs (columns of the tile's W_up/W_gate rows and
+    // of the tokens), then GEMM2 jobs (columns of its W_downT rows).  A thread
+    // copies the same pieces of the same rows in every job of a phase, so their
+    // addresses are formed once per tile; only the column offset moves.
     const int p = tid - kProdTid0;
     const char* xg = static_cast<const char*>(a.x);
     const char* wu = static_cast<const char*>(a.w_up);
@@ -331,40 +343,58 @@ __global__ void __launch_bounds__(un::kThreads, 1) k_union(UnionArgs a) {
     for (int t = 0; t < nt && ok; ++t) {
       const int r0 = tile_begin(t, nc, nt), R = tile_begin(t + 1, nc, nt) - r0;
       const int R8 = (R + 7) & ~7, K2 = (R + 15) & ~15;
+      const uint32_t blk = (uint32_t)(nm * R8 + N1) * 128;  // one column chunk of the tile's rows and tokens
       const int32_t* ti = nidx + r0;
       const char* src[kPieces];
       uint32_t dst[kPieces];
+      int sub[kPieces];
       int np = 0;
+      const int per_atom = nm * R * 8;
 #pragma unroll
-      for (int q = 0; q < kPieces; ++q) {  // GEMM1: 8 pieces of 16 bytes per row and matrix
+      for (int q = 0; q < kPieces; ++q) {  // 8 pieces of 16 bytes per row, matrix and column chunk
         const int e = p + q * kProdThreads;
         src[q] = nullptr;
         dst[q] = 0;
-        if (e < nm * R * 8) {
-          const int m = e >= R * 8 ? 1 : 0, rem = e - m * R * 8, r = rem >> 3, c = rem & 7;
+        sub[q] = 0;
+        if (e < KA * per_atom) {
+          const int at_i = e / per_atom, rem = e - at_i * per_atom;
+          const int m = rem >= R * 8 ? 1 : 0, rem2 = rem - m * R * 8, r = rem2 >> 3, c = rem2 & 7;
           src[q] = (m ? wg : wu) + (size_t)ti[r] * rowb + c * 16;
-          dst[q] = sw128_k(m * R8 + r, c);
+          dst[q] = at_i * blk + sw128_k(m * R8 + r, c);
+          sub[q] = at_i;
           np = q + 1;
         }
       }
-      const char* srcx = nullptr;
-      uint32_t dstx = 0;
-      if (p < B * 8) {
-        const int n = p >> 3, c = p & 7;
-        srcx = xg + (size_t)n * rowb + c * 16;
-        dstx = sw128_k(nm * R8 + n, c);
+      const char* srcx[kXPieces];
+      uint32_t dstx[kXPieces];
+      int subx[kXPieces];
+      int nx = 0;
+#pragma unroll
+      for (int q = 0; q < kXPieces; ++q) {
+        const int e = p + q * kProdThreads;
+        srcx[q] = nullptr;
+        dstx[q] = 0;
+        subx[q] = 0;
+        if (e < KA * B * 8) {
+          const int at_i = e / (B * 8), rem = e - at_i * B * 8, n = rem >> 3, c = rem & 7;
+          srcx[q] = xg + (size_t)n * rowb + c * 16;
+          dstx[q] = at_i * blk + sw128_k(nm * R8 + n, c);
+          subx[q] = at_i;
+          nx = q + 1;
+        }
       }
-      for (int j = 0; j < nk; ++j, ++job) {
+      for (int j = 0; j < nk / KA; ++j, ++job) {
         if (job >= S && !mbar_wait(&empty[s], ph ^ 1u, a.hdr, a.wait_ns, kDetEmpty)) {
           ok = false;
           break;
         }
         unsigned char* sl = ring + (size_t)s * slot_bytes;
-        const size_t off = (size_t)rot(j, off1, nk) * (kKc * sizeof(T));
 #pragma unroll
         for (int q = 0; q < kPieces; ++q)
-          if (q < np) cp_async16(sl + dst[q], src[q] + off);
-        if (srcx != nullptr) cp_async16(sl + dstx, srcx + off);
+          if (q < np) cp_async16(sl + dst[q], src[q] + (size_t)rot(j * KA + sub[q], off1, nk) * (kKc * sizeof(T)));
+#pragma unroll
+        for (int q = 0; q < kXPieces; ++q)
+          if (q < nx) cp_async16(sl + dstx[q], srcx[q] + (size_t)rot(j * KA + subx[q], off1, nk) * (kKc * sizeof(T)));
         cp_async_arrive_noinc(&full[s]);
         if (++s == S) {
           s = 0;
@@ -374,27 +404,28 @@ __global__ void __launch_bounds__(un::kThreads, 1) k_union(UnionArgs a) {
       if (!ok) break;
       np = 0;
 #pragma unroll
-      for (int q = 0; q < kPieces; ++q) {  // GEMM2: 16 pieces of 16 bytes per row
+      for (int q = 0; q < kPieces; ++q) {  // 16 pieces of 16 bytes per row and output tile
         const int e = p + q * kProdThreads;
         src[q] = nullptr;
         dst[q] = 0;
-        if (e < R * 16) {
-          const int r = e >> 4, c16 = e & 15;
+        sub[q] = 0;
+        if (e < DA * R * 16) {
+          const int ot = e / (R * 16), rem = e - ot * R * 16, r = rem >> 4, c16 = rem & 15;
           src[q] = wd + (size_t)ti[r] * rowb + c16 * 16;
-          dst[q] = sw128_mn(r, c16, K2);
+          dst[q] = ot * K2 * 256 + sw128_mn(r, c16, K2);
+          sub[q] = ot;
           np = q + 1;
         }
       }
-      for (int j = 0; j < nd; ++j, ++job) {
+      for (int j = 0; j < nd / DA; ++j, ++job) {
         if (job >= S && !mbar_wait(&empty[s], ph ^ 1u, a.hdr, a.wait_ns, kDetEmpty)) {
           ok = false;
           break;
         }
         unsigned char* sl = ring + (size_t)s * slot_bytes;
-        const size_t off = (size_t)rot(j, off2, nd) * (kDTile * sizeof(T));
 #pragma unroll
         for (int q = 0; q < kPieces; ++q)
-          if (q < np) cp_async16(sl + dst[q], src[q] + off);
+          if (q < np) cp_async16(sl + dst[q], src[q] + (size_t)rot(j * DA + sub[q], off2, nd) * (kDTile * sizeof(T)));
         cp_async_arrive_noinc(&full[s]);
         if (++s == S) {
           s = 0;
@@ -414,7 +445,8 @@ __global__ void __launch_bounds__(un::kThreads, 1) k_union(UnionArgs a) {
       for (int t = 0; t < nt && ok; ++t) {
         const int r0 = tile_begin(t, nc, nt), R = tile_begin(t + 1, nc, nt) - r0;
         const int R8 = (R + 7) & ~7, K2 = (R + 15) & ~15;
-        for (int j = 0; j < nk; ++j) {
+        const uint32_t blk = (uint32_t)(nm * R8 + N1) * 128;
+        for (int j = 0; j < nk / KA; ++j) {
           if (!mbar_wait(&full[s], ph, a.hdr, a.wait_ns, kDetFull)) {
             ok = false;
             break;
@@ -422,13 +454,15 @@ __global__ void __launch_bounds__(un::kThreads, 1) k_union(UnionArgs a) {
           proxy_fence();
           tc_fence_after();
           const uint32_t sl = ring_a + (uint32_t)s * slot_bytes;
-          const uint32_t xa = sl + (uint32_t)(nm * R8) * 128;
+          for (int at_i = 0; at_i < KA; ++at_i) {
+            const uint32_t wa = sl + at_i * blk, xa = wa + (uint32_t)(nm * R8) * 128;
 #pragma unroll
-          for (int kk = 0; kk < kKc / 16; ++kk) {  // a K step of 16 is 32 bytes inside the 128-byte rows
-            const uint64_t bd = sdesc_sw128(xa + kk * 32, 16, 1024);
-            const uint32_t acc = (j | kk) != 0;
-            mma(tmem + kColUp, sdesc_sw128(sl + kk * 32, 16, 1024), bd, id1, acc);
-            if (nm == 2) mma(tmem + kColGate, sdesc_sw128(sl + R8 * 128 + kk * 32, 16, 1024), bd, id1, acc);
+            for (int kk = 0; kk < kKc / 16; ++kk) {  // a K step of 16 is 32 bytes inside the 128-byte rows
+              const uint64_t bd = sdesc_sw128(xa + kk * 32, 16, 1024);
+              const uint32_t acc = (j | at_i | kk) != 0;
+              mma(tmem + kColUp, sdesc_sw128(wa + kk * 32, 16, 1024), bd, id1, acc);
+              if (nm == 2) mma(tmem + kColGate, sdesc_sw128(wa + R8 * 128 + kk * 32, 16, 1024), bd, id1, acc);
+            }
           }
           mma_commit(&empty[s]);
           if (++s == S) {
@@ -441,22 +475,27 @@ __global__ void __launch_bounds__(un::kThreads, 1) k_union(UnionArgs a) {
         if (!mbar_wait(atr, (uint32_t)t & 1u, a.hdr, a.wait_ns, kDetAt)) break;
         proxy_fence();
         tc_fence_after();
-        for (int j = 0; j < nd; ++j, ++ac) {
-          const int buf = ac % kNAcc;
-          if (!mbar_wait(&full[s], ph, a.hdr, a.wait_ns, kDetFull) ||
-              (ac >= kNAcc && !mbar_wait(&acce[buf], (uint32_t)((ac / kNAcc) - 1) & 1u, a.hdr, a.wait_ns,
-                                         kDetAccEmpty))) {
+        for (int j = 0; j < nd / DA && ok; ++j) {
+          if (!mbar_wait(&full[s], ph, a.hdr, a.wait_ns, kDetFull)) {
             ok = false;
             break;
           }
           proxy_fence();
-          tc_fence_after();
           const uint32_t sl = ring_a + (uint32_t)s * slot_bytes;
-          const uint32_t dt = tmem + kColAcc + buf * kAccStride;
-          for (int kk = 0; kk < K2 / 16; ++kk)  // a K step of 16 rows is two 1024-byte row groups
-            mma(dt, sdesc_sw128(sl + kk * 2048, K2 * 128, 1024), sdesc(at_a + kk * 2 * kLa, kLa, 128), id2, kk != 0);
+          for (int ot = 0; ot < DA; ++ot, ++ac) {
+            const int buf = ac % kNAcc;
+            if (ac >= kNAcc &&
+                !mbar_wait(&acce[buf], (uint32_t)((ac / kNAcc) - 1) & 1u, a.hdr, a.wait_ns, kDetAccEmpty)) {
+              ok = false;
+              break;
+            }
+            tc_fence_after();
+            const uint32_t dt = tmem + kColAcc + buf * N2, wa = sl + ot * K2 * 256;
+            for (int kk = 0; kk < K2 / 16; ++kk)  // a K step of 16 rows is two 1024-byte row groups
+              mma(dt, sdesc_sw128(wa + kk * 2048, K2 * 128, 1024), sdesc(at_a + kk * 2 * kLa, kLa, 128), id2, kk != 0);
+            mma_commit(&accf[buf]);
+          }
           mma_commit(&empty[s]);
-          mma_commit(&accf[buf]);
           if (++s == S) {
             s = 0;
             ph ^= 1u;
@@ -514,7 +553,7 @@ __global__ void __launch_bounds__(un::kThreads, 1) k_union(UnionArgs a) {
           break;
         }
         tc_fence_after();
-        const uint32_t acc_t = tmem + lane_base + kColAcc + buf * kAccStride;
+        const uint32_t acc_t = tmem + lane_base + kColAcc + buf * N2;
         float* yr = a.y + (size_t)rot(j, off2, nd) * kDTile + m;
 #pragma unroll
         for (int c = 0; c < BT; c += 16) {

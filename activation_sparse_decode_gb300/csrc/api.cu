@@ -24,6 +24,8 @@ struct sffn_layer {
   int W = 0;           // mask words per token
   int kc_elems = 0;    // predictor K-chunk
   int KS = 0;          // predictor K-chunks
+  int kc32 = 0;        // predictor K-chunk when one block holds up to 32 tokens
+  int KS32 = 0;
   int RG = 0;          // predictor row groups
   int score_grid = 0;  // blocks of the score kernel
   int gather_grid = 0; // blocks of the gather kernel (one per SM)
@@ -64,7 +66,7 @@ size_t align_up(size_t v, size_t a) { return (v + a - 1) / a * a; }
 int bt_slot(int bt) { return bt == 1 ? 0 : bt == 2 ? 1 : 2; }
 
 struct WsLayout {
-  size_t hdr, flags, tickets, h_part, h, mask, y_part, hl_part, bal_counts, bal_lists, total;
+  size_t hdr, flags, tickets, h_part, h, h3, mask, y_part, hl_part, bal_counts, bal_lists, total;
 };
 
 WsLayout layout(const sffn_layer* L, int batch) {
@@ -79,8 +81,9 @@ WsLayout layout(const sffn_layer* L, int batch) {
   w.hdr = take(sizeof(WsHeader));
   w.flags = take(barrier_flag_bytes((uint32_t)L->gather_grid));
   w.tickets = take((size_t)L->RG * batch * sizeof(uint32_t));
-  w.h_part = take((size_t)L->KS * batch * d.rank * sizeof(float));
+  w.h_part = take((size_t)std::max(L->KS, L->KS32) * batch * d.rank * sizeof(float));
   w.h = take((size_t)batch * d.rank * sizeof(float));
+  w.h3 = take(L->esize == 2 ? (size_t)96 * d.rank * 2 : 0);  // h as three 16-bit parts, up to 32 tokens
   w.mask = take((size_t)batch * L->W * sizeof(uint32_t));
   w.y_part = take((size_t)L->gather_grid * std::min(batch, L->max_bt) * d.d_model * sizeof(float));
   w.hl_part = take(L->lcfg_ok ? (size_t)L->lcfg.KS * d.rank * sizeof(float) : 0);
@@ -99,6 +102,7 @@ struct Ws {
   uint32_t* tickets() const { return reinterpret_cast<uint32_t*>(base + lay.tickets); }
   float* h_part() const { return reinterpret_cast<float*>(base + lay.h_part); }
   float* h() const { return reinterpret_cast<float*>(base + lay.h); }
+  void* h3() const { return base + lay.h3; }
   uint32_t* mask() const { return reinterpret_cast<uint32_t*>(base + lay.mask); }
   float* y_part() const { return reinterpret_cast<float*>(base + lay.y_part); }
   float* hl_part() const { return reinterpret_cast<float*>(base + lay.hl_part); }
@@ -142,10 +146,27 @@ sffn_status check_dev_ptr(const void* p, const char* name) {
 
 // Predictor for `batch` tokens: h = V x (split-K, deterministic), then the
 // scores and the mask words (and optionally the scores themselves).
+bool use_union(const sffn_layer* L, int batch, UnionConfig* cfg);
+
 sffn_status run_predictor(const sffn_layer* L, const void* x, int batch, const Ws& ws, float* scores,
                           cudaStream_t s) {
   const auto& d = L->desc;
-  PredHiddenArgs ha{d.pred_V, x, batch, d.rank, d.d_model, L->kc_elems, L->KS, ws.h_part(), ws.h(), ws.tickets()};
+  size_t ring = 0;
+  UnionConfig uc{};
+  if (scores == nullptr && use_union(L, batch, &uc) && score_mma_config(d.dtype, d.rank, batch, L->smem_optin, &ring)) {
+    // one hidden-layer launch for the whole batch (h also as three 16-bit
+    // parts), then the scores and threshold as one tensor-core product
+    const int bt = batch <= 8 ? 8 : batch <= 16 ? 16 : 32;
+    PredHiddenArgs ha{d.pred_V, x, batch, d.rank, d.d_model, L->kc32, L->KS32, ws.h_part(), ws.h(), ws.tickets(),
+                      ws.h3(), bt};
+    SFFN_CUDA(launch_pred_hidden(d.dtype, ha, s), "predictor hidden launch");
+    ScoreMmaArgs sa{d.pred_U, ws.h3(), d.pred_b, d.tau, batch, d.d_ff, d.rank, L->W, ws.mask(), ws.hdr(), ring,
+                    (uint64_t)g_wait_ns};
+    SFFN_CUDA(launch_score_mma(d.dtype, sa, bt, std::min(L->sms, L->W), s), "predictor score launch");
+    return SFFN_OK;
+  }
+  PredHiddenArgs ha{d.pred_V, x, batch, d.rank, d.d_model, L->kc_elems, L->KS, ws.h_part(), ws.h(), ws.tickets(),
+                    nullptr, 0};
   // token groups of up to 8 per launch
   for (int b0 = 0; b0 < batch; b0 += 8) {
     const int nb = std::min(8, batch - b0);
@@ -391,6 +412,9 @@ sffn_status sffn_create_layer(const sffn_layer_desc* desc, sffn_layer_t* out) {
   kc = std::min(kc, std::max(unit, max_kc / unit * unit));
   L->kc_elems = kc;
   L->KS = (d.d_model + kc - 1) / kc;
+  const int max_kc32 = 2048 / esize;  // x chunk of 32 tokens must stay within 64 KB of shared memory
+  L->kc32 = std::min(kc, std::max(unit, max_kc32 / unit * unit));
+  L->KS32 = (d.d_model + L->kc32 - 1) / L->kc32;
   L->score_grid = std::min((d.d_ff + 63) / 64, 8 * L->sms);
 
   L->gather_grid = L->sms;

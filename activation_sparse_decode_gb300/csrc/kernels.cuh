@@ -18,6 +18,8 @@ struct PredHiddenArgs {
   float* h_part;       // [KS][B][r] partial sums (workspace)
   float* h;            // [B][r] final (workspace)
   uint32_t* tickets;   // [row groups][token groups] arrival counters (zeroed)
+  void* h3;            // NULL, or [3*bt][r] dtype: h split into hi, mid, lo 16-bit parts (rows part*bt + b)
+  int bt;              // 0: tokens per block chosen from B; else 8, 16 or 32 (one token group)
 };
 int pred_hidden_row_groups(int r);
 cudaError_t launch_pred_hidden(int dtype, const PredHiddenArgs& a, cudaStream_t s);
@@ -137,6 +139,22 @@ struct UnionConfig {
 };
 bool union_config(int dtype, int act, int d, int f, int B, int grid, size_t smem_optin, UnionConfig* cfg);
 cudaError_t launch_union(int dtype, const UnionConfig& cfg, const UnionArgs& a, int grid, cudaStream_t s);
+
+// ---- batched predictor scores on the tensor cores (8 to 32 tokens)
+struct ScoreMmaArgs {
+  const void* U;        // [f][r] dtype
+  const void* h3;       // [3*bt][r] dtype: the tokens' hidden vectors as hi, mid, lo parts
+  const float* pb;      // [f]
+  float tau;
+  int B, f, r, W;
+  uint32_t* mask;       // [B][W] out
+  WsHeader* hdr;
+  size_t ring_bytes;
+  uint64_t wait_ns;
+};
+constexpr int kScoreMmaThreads = 416;
+bool score_mma_config(int dtype, int r, int B, size_t smem_optin, size_t* ring_bytes);
+cudaError_t launch_score_mma(int dtype, const ScoreMmaArgs& a, int bt, int grid, cudaStream_t s);
 
 // ---- residual + LayerNorm: x_out = round(LN(x + y) * gamma + beta)
 cudaError_t launch_residual_layernorm(int dtype, const void* x, const float* y, int B, int d,

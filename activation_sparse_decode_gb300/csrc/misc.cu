@@ -249,6 +249,28 @@ cudaError_t launch_union(int dtype, const UnionConfig& cfg, const UnionArgs& a, 
   return cudaErrorInvalidValue;
 }
 
+bool score_mma_config(int dtype, int r, int B, size_t smem_optin, size_t* ring_bytes) {
+  if (dtype != kF16 && dtype != kBF16) return false;
+  if (r % 64 != 0 || B < 1 || B > 32) return false;
+  const int bt = B <= 8 ? 8 : B <= 16 ? 16 : 32;
+  const size_t slot = 128 * 128 + (size_t)((3 * bt + 15) / 16 * 16) * 128;
+  const size_t reserve = 2048;  // static shared memory
+  if (smem_optin < reserve + 2 * slot) return false;
+  *ring_bytes = std::min<size_t>(32 * slot, (smem_optin - reserve) / slot * slot);
+  return true;
+}
+
+cudaError_t launch_score_mma_f16(const ScoreMmaArgs&, int, int, size_t, cudaStream_t);
+cudaError_t launch_score_mma_bf16(const ScoreMmaArgs&, int, int, size_t, cudaStream_t);
+
+cudaError_t launch_score_mma(int dtype, const ScoreMmaArgs& a, int bt, int grid, cudaStream_t s) {
+  switch (dtype) {
+    case kF16: return launch_score_mma_f16(a, bt, grid, a.ring_bytes, s);
+    case kBF16: return launch_score_mma_bf16(a, bt, grid, a.ring_bytes, s);
+  }
+  return cudaErrorInvalidValue;
+}
+
 cudaError_t launch_layer_f32(const LayerConfig&, const LayerArgs&, int, cudaStream_t);
 cudaError_t launch_layer_f16(const LayerConfig&, const LayerArgs&, int, cudaStream_t);
 cudaError_t launch_layer_bf16(const LayerConfig&, const LayerArgs&, int, cudaStream_t);

@@ -24,7 +24,8 @@ constexpr int kHiddenRowsPerBlock = kHiddenWarps * kHiddenRowsPerWarp;
 template <typename T, int BT>
 __global__ void __launch_bounds__(kHiddenWarps * 32)
     k_pred_hidden(const T* __restrict__ V, const T* __restrict__ x, int B, int r, int d, int kc_elems,
-                  int KS, float* __restrict__ h_part, float* __restrict__ h, uint32_t* __restrict__ tickets) {
+                  int KS, float* __restrict__ h_part, float* __restrict__ h, uint32_t* __restrict__ tickets,
+                  T* __restrict__ h3) {
   constexpr int E = Chunk<T>::N;
   extern __shared__ uint4 xs[];  // [BT][kc_elems / E]
   __shared__ uint32_t s_last;
@@ -102,6 +103,15 @@ __global__ void __launch_bounds__(kHiddenWarps * 32)
     float s = 0.f;
     for (int k = 0; k < KS; ++k) s += __ldcg(&h_part[((size_t)k * B + b0 + bb) * r + row]);
     h[(size_t)(b0 + bb) * r + row] = s;
+    if (h3 != nullptr) {  // three 16-bit parts whose sum carries the fp32 value
+      const T hi = from_float<T>(s);
+      const float rest = s - static_cast<float>(hi);
+      const T mid = from_float<T>(rest);
+      const T lo = from_float<T>(rest - static_cast<float>(mid));
+      h3[(size_t)(0 * BT + bb) * r + row] = hi;
+      h3[(size_t)(1 * BT + bb) * r + row] = mid;
+      h3[(size_t)(2 * BT + bb) * r + row] = lo;
+    }
   }
 }
 
@@ -264,12 +274,16 @@ cudaError_t hidden_launch(const PredHiddenArgs& a, cudaStream_t s) {
   if (e != cudaSuccess) return e;
   k_pred_hidden<T, BT><<<grid, kHiddenWarps * 32, smem, s>>>(
       static_cast<const T*>(a.V), static_cast<const T*>(a.x), a.B, a.r, a.d, a.kc_elems, a.KS,
-      a.h_part, a.h, a.tickets);
+      a.h_part, a.h, a.tickets, static_cast<T*>(a.h3));
   return cudaGetLastError();
 }
 
 template <typename T>
 cudaError_t hidden_dispatch(const PredHiddenArgs& a, cudaStream_t s) {
+  if (a.bt == 8) return hidden_launch<T, 8>(a, s);
+  if (a.bt == 16) return hidden_launch<T, 16>(a, s);
+  if (a.bt == 32) return hidden_launch<T, 32>(a, s);
+  if (a.bt != 0 || a.h3 != nullptr) return cudaErrorInvalidValue;
   if (a.B == 1) return hidden_launch<T, 1>(a, s);
   if (a.B == 2) return hidden_launch<T, 2>(a, s);
   if (a.B <= 4) return hidden_launch<T, 4>(a, s);

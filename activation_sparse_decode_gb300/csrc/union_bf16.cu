@@ -1,8 +1,13 @@
-// Instantiations of the batched union-of-active-rows kernel for __nv_bfloat16 weights.
+// Instantiations of the tensor-core batch kernels (union-of-active-rows FFN,
+// predictor scores) for __nv_bfloat16 weights.
+#include "score_mma.cuh"
 #include "union_impl.cuh"
 
 namespace sffn {
 cudaError_t launch_union_bf16(const UnionConfig& cfg, const UnionArgs& a, int grid, cudaStream_t s) {
   return union_dispatch<__nv_bfloat16>(cfg, a, grid, s);
+}
+cudaError_t launch_score_mma_bf16(const ScoreMmaArgs& a, int bt, int grid, size_t smem, cudaStream_t s) {
+  return score_mma_dispatch<__nv_bfloat16>(a, bt, grid, smem, s);
 }
 }  // namespace sffn

@@ -405,7 +405,8 @@ sffn_status sffn_create_layer(const sffn_layer_desc* desc, sffn_layer_t* out) {
   const int E = 16 / esize;
   const int unit = 32 * E;  // one warp-wide 16-byte load of a row
   L->RG = pred_hidden_row_groups(d.rank);
-  const int ks_target = std::max(1, (2 * L->sms + L->RG - 1) / L->RG);
+  const int rg16 = (d.rank + 15) / 16;  // row groups of the up-to-8-token kernel
+  const int ks_target = std::max(1, (2 * L->sms + rg16 - 1) / rg16);
   int kc = (d.d_model + ks_target - 1) / ks_target;
   kc = (kc + unit - 1) / unit * unit;
   const int max_kc = 8192 / esize;  // x chunk of 8 tokens must stay within 64 KB of shared memory

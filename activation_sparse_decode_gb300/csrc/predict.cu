@@ -14,8 +14,13 @@ namespace sffn {
 namespace {
 
 constexpr int kHiddenWarps = 8;
-constexpr int kHiddenRowsPerWarp = 2;
-constexpr int kHiddenRowsPerBlock = kHiddenWarps * kHiddenRowsPerWarp;
+// Rows of V per warp: two for up to 8 tokens per block, one beyond (the
+// 2 x BT accumulators would otherwise limit a 32-token block to one per SM).
+template <int BT> struct HiddenRows {
+  static constexpr int kPerWarp = BT <= 8 ? 2 : 1;
+  static constexpr int kPerBlock = kHiddenWarps * kPerWarp;
+};
+constexpr int kHiddenRowsPerBlockMin = kHiddenWarps;  // the smallest row group (most groups)
 
 // Grid (KS, row groups, token groups).  Each block stages its K-chunk of the
 // BT tokens in shared memory; each warp streams two rows of V over the chunk.
@@ -44,6 +49,8 @@ __global__ void __launch_bounds__(kHiddenWarps * 32)
   __syncthreads();
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  constexpr int kHiddenRowsPerWarp = HiddenRows<BT>::kPerWarp;
+  constexpr int kHiddenRowsPerBlock = HiddenRows<BT>::kPerBlock;
   const int row0 = rg * kHiddenRowsPerBlock + warp * kHiddenRowsPerWarp;
   float acc[kHiddenRowsPerWarp][BT];
 #pragma unroll
@@ -100,8 +107,19 @@ __global__ void __launch_bounds__(kHiddenWarps * 32)
     const int q = i / BT, bb = i - q * BT;
     const int row = rg * kHiddenRowsPerBlock + q;
     if (row >= r || b0 + bb >= B) continue;
+    // fixed summation order; eight partial-sum loads in flight at a time
     float s = 0.f;
-    for (int k = 0; k < KS; ++k) s += __ldcg(&h_part[((size_t)k * B + b0 + bb) * r + row]);
+    const float* hp = h_part + (size_t)(b0 + bb) * r + row;
+    const size_t kstride = (size_t)B * r;
+    int k = 0;
+    for (; k + 8 <= KS; k += 8) {
+      float v[8];
+#pragma unroll
+      for (int u = 0; u < 8; ++u) v[u] = __ldcg(hp + (size_t)(k + u) * kstride);
+#pragma unroll
+      for (int u = 0; u < 8; ++u) s += v[u];
+    }
+    for (; k < KS; ++k) s += __ldcg(hp + (size_t)k * kstride);
     h[(size_t)(b0 + bb) * r + row] = s;
     if (h3 != nullptr) {  // three 16-bit parts whose sum carries the fp32 value
       const T hi = from_float<T>(s);
@@ -267,7 +285,7 @@ __global__ void k_count_bits(const uint32_t* __restrict__ mask, int B, int f, in
 
 template <typename T, int BT>
 cudaError_t hidden_launch(const PredHiddenArgs& a, cudaStream_t s) {
-  const dim3 grid(a.KS, pred_hidden_row_groups(a.r), (a.B + BT - 1) / BT);
+  const dim3 grid(a.KS, (a.r + HiddenRows<BT>::kPerBlock - 1) / HiddenRows<BT>::kPerBlock, (a.B + BT - 1) / BT);
   const size_t smem = (size_t)BT * a.kc_elems * sizeof(T);
   static int cur = 48 * 1024;
   const cudaError_t e = ensure_dyn_smem(k_pred_hidden<T, BT>, smem, &cur);
@@ -322,7 +340,9 @@ cudaError_t score_dispatch(const PredScoreArgs& a, cudaStream_t s) {
 
 }  // namespace
 
-int pred_hidden_row_groups(int r) { return (r + kHiddenRowsPerBlock - 1) / kHiddenRowsPerBlock; }
+// Row groups of the hidden-layer kernel at its smallest group size: an upper
+// bound on the arrival tickets any launch uses per token group.
+int pred_hidden_row_groups(int r) { return (r + kHiddenRowsPerBlockMin - 1) / kHiddenRowsPerBlockMin; }
 
 cudaError_t launch_pred_hidden(int dtype, const PredHiddenArgs& a, cudaStream_t s) {
   switch (dtype) {

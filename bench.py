@@ -569,7 +569,7 @@ def recorded_traffic(workload, batch, union_path):
     summary, when the kernel sources still match the ones it was taken on."""
     if union_path:
         path, key, files = "k_union_traffic.json", f"{workload}_b{batch}", ("union_impl.cuh", "common.cuh",
-                                                                           "kernels.cuh")
+                                                                           "kernels.cuh", "tcgen05.cuh")
     elif workload == "c2" and batch == 1:
         path, key, files = "k_layer_traffic.json", None, ("layer_impl.cuh", "common.cuh", "kernels.cuh")
     else:

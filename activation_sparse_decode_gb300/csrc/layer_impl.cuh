@@ -131,7 +131,39 @@ __global__ void __launch_bounds__(kLayerThreads, 1) k_layer(const LayerArgs a) {
   uint8_t* s_act = reinterpret_cast<uint8_t*>(bal_einc + G);      // predicted-active flag per owned row
   SFFN_TRACE(0);
 
-  // ---- phase 0: start every independent stream, zero the outputs
+  // ---- phase 0a: before the previous kernel on the stream has finished
+  // (programmatic dependent launch), touch only constant data: warm L2 with
+  // this block's V tiles, owned U rows and hot rows.  The token, the outputs
+  // and the workspace may still be in use by that kernel.
+  {
+    const int tiles = a.RG * a.KS;
+    const unsigned char* V = static_cast<const unsigned char*>(a.V);
+    for (int tile = c; tile < tiles; tile += G) {
+      const int rg = tile / a.KS, ks = tile - rg * a.KS;
+      const int k0 = ks * a.kc, kn = min(a.kc, d - k0);
+      const int row = rg * 16 + tid;
+      if (tid < 16 && row < r) bulk_prefetch_l2(V + ((size_t)row * d + k0) * ES, (uint32_t)kn * ES);
+    }
+    const unsigned char* Ub = static_cast<const unsigned char*>(a.U);
+    const int ulines = (urow_bytes + 127) / 128;
+    for (int q = tid; q < n_own * ulines; q += kLayerThreads) {
+      const int j = q / ulines, l = q - j * ulines;
+      prefetch_l2(Ub + (size_t)(c + (size_t)j * G) * urow_bytes + l * 128);
+    }
+    const int nh = c < a.hot_rows ? min(a.hot_stages, min(n_own, (a.hot_rows - c + G - 1) / G)) : 0;
+    const int rlines = (row_bytes + 127) / 128;
+    for (int q = tid; q < nh * rlines; q += kLayerThreads) {
+      const int j = q / rlines, l = q - j * rlines;
+      const size_t off = (size_t)(c + (size_t)j * G) * row_bytes + (size_t)l * 128;
+      prefetch_l2(static_cast<const unsigned char*>(a.w_up) + off);
+      if (reglu) prefetch_l2(static_cast<const unsigned char*>(a.w_gate) + off);
+      prefetch_l2(static_cast<const unsigned char*>(a.w_downT) + off);
+    }
+  }
+  grid_dependency_wait();       // the previous kernel has completed and its writes are visible
+  grid_dependents_launch();     // the next one may start its constant-data phase
+
+  // ---- phase 0b: start every stream, zero the outputs
   // generation of this block's barrier flag: it cannot change before this block arrives
   const uint32_t bar_gen = warp == kBarrierThread / 32 ? barrier_generation(a.bar_flags) : 0u;
   // tag of this launch's published balancing counts: the generation the barrier moves to
@@ -183,16 +215,6 @@ __global__ void __launch_bounds__(kLayerThreads, 1) k_layer(const LayerArgs a) {
   if (tid == 0) {
     for (int s = 0; s < S; ++s) mbar_init(&bars[s], kLayerThreads);
     fence_mbar_init();
-  }
-  {  // L2 prefetch of this block's V tiles (one row segment per thread)
-    const int tiles = a.RG * a.KS;
-    const unsigned char* V = static_cast<const unsigned char*>(a.V);
-    for (int tile = c; tile < tiles; tile += G) {
-      const int rg = tile / a.KS, ks = tile - rg * a.KS;
-      const int k0 = ks * a.kc, kn = min(a.kc, d - k0);
-      const int row = rg * 16 + tid;
-      if (tid < 16 && row < r) bulk_prefetch_l2(V + ((size_t)row * d + k0) * ES, (uint32_t)kn * ES);
-    }
   }
   for (int j = tid; j < (tid < kCopyThreads ? n_own : 0); j += kCopyThreads) {
     const int i = c + j * G;
@@ -754,8 +776,20 @@ cudaError_t layer_launch(const LayerConfig& cfg, const LayerArgs& a, int grid, c
   static int cur = 48 * 1024;
   const cudaError_t e = ensure_dyn_smem(k_layer<T, CPT>, cfg.smem, &cur);
   if (e != cudaSuccess) return e;
-  k_layer<T, CPT><<<grid, kLayerThreads, cfg.smem, s>>>(a);
-  return cudaGetLastError();
+  // Programmatic dependent launch: this kernel may start while the previous
+  // kernel on the stream finishes; it waits for it (griddepcontrol.wait)
+  // before touching anything that kernel may write.
+  cudaLaunchConfig_t lc{};
+  lc.gridDim = dim3(grid);
+  lc.blockDim = dim3(kLayerThreads);
+  lc.dynamicSmemBytes = cfg.smem;
+  lc.stream = s;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  lc.attrs = attr;
+  lc.numAttrs = 1;
+  return cudaLaunchKernelEx(&lc, k_layer<T, CPT>, a);
 }
 
 template <typename T>

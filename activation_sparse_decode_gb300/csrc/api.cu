@@ -305,6 +305,7 @@ sffn_status run_layer(const sffn_layer* L, const void* x, const float* y_prev, v
   a.region_bytes = L->lcfg.region_bytes;
   a.u_off = L->lcfg.u_off;
   a.hot_rows = d.hot_rows;
+  a.warm_rows = d.warm_rows;
   a.hot_stages = L->lcfg.hot_stages;
   const int own_cap = (d.d_ff + L->gather_grid - 1) / L->gather_grid;
   a.balance = (d.flags & SFFN_FLAG_BALANCE) != 0 && own_cap >= 8 ? 1 : 0;
@@ -384,6 +385,7 @@ sffn_status sffn_create_layer(const sffn_layer_desc* desc, sffn_layer_t* out) {
   }
   if (d.rank / (16 / esize) > 256) return fail(SFFN_ERR_UNSUPPORTED, "rank too large for the score kernel");
   if (d.hot_rows < 0 || d.hot_rows > d.d_ff) return fail(SFFN_ERR_INVALID_ARG, "hot_rows outside [0, d_ff]");
+  if (d.warm_rows < 0 || d.warm_rows > d.d_ff) return fail(SFFN_ERR_INVALID_ARG, "warm_rows outside [0, d_ff]");
   if (!(d.expected_active >= 0.f)) return fail(SFFN_ERR_INVALID_ARG, "expected_active must be >= 0");
 
   sffn_layer* L = new (std::nothrow) sffn_layer();
@@ -788,6 +790,7 @@ sffn_status sffn_internal_layer_on_scratch(sffn_layer_t L, const void* x, float*
   a.region_bytes = L->lcfg.region_bytes;
   a.u_off = L->lcfg.u_off;
   a.hot_rows = d.hot_rows;
+  a.warm_rows = d.warm_rows;
   a.hot_stages = L->lcfg.hot_stages;
   a.balance = 0;
   a.prefill = 0;

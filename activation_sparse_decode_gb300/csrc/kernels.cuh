@@ -97,6 +97,7 @@ struct LayerArgs {
   uint32_t* bar_flags;    // [grid] grid-barrier release flags, 128 bytes apart
   int d, f, r, KS, kc, RG, act, nstages, u_smem;
   int hot_rows;           // neurons [0, hot_rows) are prefetched before the predictor decides
+  int warm_rows;          // neurons [0, warm_rows): rows warmed in L2 while the predictor runs
   int hot_stages;         // ring stages free of the U rows, usable for that prefetch
   int balance;            // 1: even out the active rows over the blocks (second barrier)
   int prefill;            // own rows each block starts streaming before the balancing

@@ -150,9 +150,12 @@ __global__ void __launch_bounds__(kLayerThreads, 1) k_layer(const LayerArgs a) {
       const int j = q / ulines, l = q - j * ulines;
       prefetch_l2(Ub + (size_t)(c + (size_t)j * G) * urow_bytes + l * 128);
     }
+    // hot rows (copied into the ring right after the barrier), then the other
+    // owned warm rows (likely active; read from L2 by the ring if they are)
     const int nh = c < a.hot_rows ? min(a.hot_stages, min(n_own, (a.hot_rows - c + G - 1) / G)) : 0;
+    const int nw = c < a.warm_rows ? min(n_own, (a.warm_rows - c + G - 1) / G) : 0;
     const int rlines = (row_bytes + 127) / 128;
-    for (int q = tid; q < nh * rlines; q += kLayerThreads) {
+    for (int q = tid; q < max(nh, nw) * rlines; q += kLayerThreads) {
       const int j = q / rlines, l = q - j * rlines;
       const size_t off = (size_t)(c + (size_t)j * G) * row_bytes + (size_t)l * 128;
       prefetch_l2(static_cast<const unsigned char*>(a.w_up) + off);
@@ -162,12 +165,9 @@ __global__ void __launch_bounds__(kLayerThreads, 1) k_layer(const LayerArgs a) {
   }
   grid_dependency_wait();       // the previous kernel has completed and its writes are visible
   grid_dependents_launch();     // the next one may start its constant-data phase
+  SFFN_TRACE(18);
 
   // ---- phase 0b: start every stream, zero the outputs
-  // generation of this block's barrier flag: it cannot change before this block arrives
-  const uint32_t bar_gen = warp == kBarrierThread / 32 ? barrier_generation(a.bar_flags) : 0u;
-  // tag of this launch's published balancing counts: the generation the barrier moves to
-  const uint32_t bar_epoch = barrier_generation(a.bar_flags) + 1u;
   if (a.y_prev == nullptr) {  // the token itself first: everything in phase 1 waits on it
     const uint4* xg = static_cast<const uint4*>(a.x);
     if (tid < kCopyThreads)
@@ -326,12 +326,17 @@ __global__ void __launch_bounds__(kLayerThreads, 1) k_layer(const LayerArgs a) {
   // the V tiles, they do not delay the token and V loads in the request queues.
   SFFN_TRACE(2);
   __shared__ int s_passed;
+  __shared__ uint32_t s_epoch;
   __syncthreads();  // all h partials of this block are written
   if (warp == kBarrierThread / 32) {
     SFFN_TRACE_AT(12, kBarrierThread);
-    const bool ok = barrier_arrive_wait_warp(a.hdr, a.bar_flags, (uint32_t)G, bar_gen, a.wait_ns, 0x300u);
+    unsigned long long target = 0;
+    const bool ok = counter_barrier_warp(a.hdr, (uint32_t)G, a.wait_ns, 0x300u, &target);
     SFFN_TRACE_AT(13, kBarrierThread);
-    if (tid == kBarrierThread) s_passed = ok ? 1 : 0;
+    if (tid == kBarrierThread) {
+      s_passed = ok ? 1 : 0;
+      s_epoch = (uint32_t)(target / (uint32_t)G);  // tags this launch's published balancing counts
+    }
   } else {
     const unsigned char* Ub = static_cast<const unsigned char*>(a.U);
     if (a.u_smem) {  // owned U rows -> shared memory, 16 bytes per copy
@@ -351,6 +356,7 @@ __global__ void __launch_bounds__(kLayerThreads, 1) k_layer(const LayerArgs a) {
   }
   __syncthreads();
   const bool passed = s_passed != 0;
+  const uint32_t bar_epoch = s_epoch;
   // hot rows next: issued after the barrier so that its round trips do not
   // queue behind them; they still land before the predictor has decided
   for (int j = 0; j < n_hot; ++j) fill_hot(j);

@@ -15,10 +15,12 @@ __device__ __forceinline__ uint64_t sdesc(uint32_t addr, uint32_t lbo, uint32_t 
          (1ull << 46);
 }
 
-// Instruction descriptor of kind::f16 with fp32 accumulation, M = 128.
-__device__ __forceinline__ uint32_t idesc(int bf16, int a_mn_major, int n) {
+// Instruction descriptor of kind::f16 with fp32 accumulation (M = 128 or 64).
+// With M = 64 the accumulator's row m sits in tensor-memory lane
+// (m / 16) * 32 + m % 16: 16 rows in each warp's quarter of the lanes.
+__device__ __forceinline__ uint32_t idesc(int bf16, int a_mn_major, int n, int m = 128) {
   return (1u << 4) | ((uint32_t)bf16 << 7) | ((uint32_t)bf16 << 10) | ((uint32_t)a_mn_major << 15) |
-         ((uint32_t)(n >> 3) << 17) | ((uint32_t)(128 >> 4) << 24);
+         ((uint32_t)(n >> 3) << 17) | ((uint32_t)(m >> 4) << 24);
 }
 
 __device__ __forceinline__ void mma(uint32_t d_tmem, uint64_t a, uint64_t b, uint32_t id, uint32_t accumulate) {

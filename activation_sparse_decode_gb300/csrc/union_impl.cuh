@@ -214,6 +214,9 @@ __global__ void __launch_bounds__(un::kThreads, 1) k_union(UnionArgs a) {
   while (DA < 4 && 2 * DA * k2max <= kPieces * kProdThreads / 16 && nd % (2 * DA) == 0 && 2 * DA <= kNAcc / 2) DA *= 2;
   const uint32_t slot_bytes =
       ((uint32_t)max(KA * (nm * r8max + N1) * 128, DA * k2max * 256) + 1023u) & ~1023u;
+  // Tiles of at most 64 neurons use M = 64 MMAs for GEMM1: half the operand
+  // bytes per MMA (the tensor core reads every one of the M rows).
+  const bool m64 = r8max <= 64;
   const int S = min(kMaxSlots, (int)(a.ring_bytes / slot_bytes));
   // W_downT rows past a tile's end (up to the next 16) are read by GEMM2
   // against zero activations, so they must hold finite values: zero them once
@@ -365,7 +368,7 @@ __global__ void __launch_bounds__(un::kThreads, 1) k_union(UnionArgs a) {
   } else if (warp == kMmaWarp) {
     // ---- 3b. one thread issues every MMA
     if (lane == 0) {
-      const uint32_t id1 = idesc(IsBf16<T>::v, 0, N1), id2 = idesc(IsBf16<T>::v, 1, N2);
+      const uint32_t id1 = idesc(IsBf16<T>::v, 0, N1, m64 ? 64 : 128), id2 = idesc(IsBf16<T>::v, 1, N2);
       const uint32_t ring_a = smem_addr(ring), at_a = smem_addr(at);
       int s = 0, ac = 0;
       uint32_t ph = 0;
@@ -435,8 +438,11 @@ __global__ void __launch_bounds__(un::kThreads, 1) k_union(UnionArgs a) {
     }
     __syncwarp();
   } else {
-    // ---- 3c. epilogue: warp w reads tensor-memory lanes [32w, 32w + 32)
+    // ---- 3c. epilogue: warp w reads tensor-memory lanes [32w, 32w + 32).
+    // GEMM1 row of this thread: its lane (M = 128), or with M = 64 lanes 0-15
+    // of each warp hold rows 16w .. 16w + 15; GEMM2 row: its lane.
     const int m = tid;
+    const int m1 = m64 ? (lane < 16 ? warp * 16 + lane : -1) : tid;
     const uint32_t lane_base = (uint32_t)(warp * 32) << 16;
     int ac = 0;
     for (int t = 0; t < nt; ++t) {
@@ -446,18 +452,18 @@ __global__ void __launch_bounds__(un::kThreads, 1) k_union(UnionArgs a) {
       tc_fence_after();
       uint32_t tb = 0;
       float bias = 0.f;
-      if (m < R) {
-        tb = tbits[r0 + m];
-        bias = nbias[r0 + m];
+      if (m1 >= 0 && m1 < R) {
+        tb = tbits[r0 + m1];
+        bias = nbias[r0 + m1];
       }
-      unsigned char* col = at + (m >> 3) * kLa + (m & 7) * 2;
+      unsigned char* col = at + (m1 >> 3) * kLa + (m1 & 7) * 2;
 #pragma unroll
       for (int c = 0; c < N1; c += 16) {
         float u[16], g[16];
         tmem_ld16(tmem + lane_base + kColUp + c, u);
         if (nm == 2) tmem_ld16(tmem + lane_base + kColGate + c, g);
         tmem_wait_ld();
-        if (m < K2) {
+        if (m1 >= 0 && m1 < K2) {
 #pragma unroll
           for (int q = 0; q < 16 && c + q < BT; ++q) {
             float av = 0.f;

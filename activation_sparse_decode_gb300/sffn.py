@@ -40,7 +40,7 @@ class sffn_layer_desc(ctypes.Structure):
                 ("dtype", _i32), ("act", _i32),
                 ("w_up", _vp), ("w_gate", _vp), ("w_downT", _vp), ("b", _vp),
                 ("pred_U", _vp), ("pred_V", _vp), ("pred_b", _vp), ("tau", ctypes.c_float), ("flags", _i32),
-                ("hot_rows", _i32), ("expected_active", ctypes.c_float)]
+                ("hot_rows", _i32), ("expected_active", ctypes.c_float), ("warm_rows", _i32)]
 
 SFFN_FLAG_MULTI_KERNEL = 1
 SFFN_FLAG_BALANCE = 2
@@ -113,7 +113,7 @@ class Layer:
     """A layer handle plus references to the tensors it borrows."""
 
     def __init__(self, w_up, w_downT, b, U, V, pred_b=None, w_gate=None, tau: float = 0.0, max_batch: int = 1,
-                 flags: int = 0, hot_rows: int = 0, expected_active: float = 0.0):
+                 flags: int = 0, hot_rows: int = 0, expected_active: float = 0.0, warm_rows: int = 0):
         self.tensors = [w_up, w_downT, b, U, V, pred_b, w_gate]
         self.act = "reglu" if w_gate is not None else "relu"
         self.dtype = w_up.dtype
@@ -122,7 +122,7 @@ class Layer:
             dtype=DTYPE_CODES[w_up.dtype], act=ACT_CODES[self.act],
             w_up=_ptr(w_up), w_gate=_ptr(w_gate), w_downT=_ptr(w_downT), b=_ptr(b),
             pred_U=_ptr(U), pred_V=_ptr(V), pred_b=_ptr(pred_b if pred_b is not None else b), tau=tau,
-            flags=flags, hot_rows=hot_rows, expected_active=expected_active)
+            flags=flags, hot_rows=hot_rows, expected_active=expected_active, warm_rows=warm_rows)
         self.desc = desc
         h = ctypes.c_void_p()
         _check(_c["create"](ctypes.byref(desc), ctypes.byref(h)))
@@ -131,10 +131,11 @@ class Layer:
 
     @classmethod
     def from_weights(cls, lw, tau: float = 0.0, max_batch: int = 1, flags: int = 0, hot_rows: int = 0,
-                     expected_active: float = 0.0) -> "Layer":
+                     expected_active: float = 0.0, warm_rows: int = 0) -> "Layer":
         """From a workloads.LayerWeights already on the GPU."""
         return cls(lw.w_up, lw.w_downT, lw.b, lw.U, lw.V, pred_b=lw.b, w_gate=lw.w_gate, tau=tau,
-                   max_batch=max_batch, flags=flags, hot_rows=hot_rows, expected_active=expected_active)
+                   max_batch=max_batch, flags=flags, hot_rows=hot_rows, expected_active=expected_active,
+                   warm_rows=warm_rows)
 
     def close(self):
         if getattr(self, "handle", None):
@@ -287,6 +288,14 @@ def hot_first_order(layer: Layer, X: torch.Tensor, ws: torch.Tensor) -> np.ndarr
     counts = torch.empty(layer.d_ff, dtype=torch.int32, device=X.device)
     sffn_profile_counts(layer, X, counts, ws)
     return sffn_hot_first_perm(counts.cpu().numpy()), counts
+
+
+def warm_row_count(counts, n_tokens: int, row_bytes: int, frac: float = 0.2, budget_bytes: int = 32 << 20) -> int:
+    """Leading rows of a hot-first order predicted active for at least `frac`
+    of the profile tokens, capped so that their rows fit in `budget_bytes`
+    (the L2 the batch-1 kernel may fill speculatively)."""
+    c = np.asarray(counts.cpu() if hasattr(counts, "cpu") else counts)
+    return int(min((c >= frac * n_tokens).sum(), budget_bytes // max(1, row_bytes)))
 
 
 def hot_row_count(counts, n_tokens: int, frac: float = 0.99) -> int:

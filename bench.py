@@ -60,6 +60,10 @@ def parse():
     p.add_argument("--row-gather", action="store_true", help="batches: CUDA-core row gather, not the union path")
     p.add_argument("--no-dense", action="store_true", help="skip the dense contrast")
     p.add_argument("--replicas", type=int, default=8)
+    p.add_argument("--hot-frac", type=float, default=0.99,
+                   help="hot rows: profile frequency at which rows are fetched before the predictor decides")
+    p.add_argument("--warm-frac", type=float, default=0.0,
+                   help="warm rows (pulled into L2 during the predictor): profile frequency, 0 = none")
     p.add_argument("--cpu-seconds", type=float, default=15.0)
     p.add_argument("--no-cpu-baseline", action="store_true")
     p.add_argument("--cpu-worker", default=None)
@@ -199,20 +203,22 @@ def run_cpu_baseline(lw, X, seconds, n_layers=1):
 ESIZE = {"f32": 4, "f16": 2, "bf16": 2}
 
 
-def build_layer(sffn, W, wl, layer, dev):
+def build_layer(sffn, W, wl, layer, dev, hot_frac=0.99, warm_frac=0.0):
     """One layer of the workload; hot-first reordered when the workload asks."""
     import torch
     lw = W.make_layer(wl, seed=0, layer=layer, device=dev)
-    hot, ea = 0, 0.0
+    hot, ea, warm = 0, 0.0, 0
     if wl.reorder:
         prof = sffn.Layer.from_weights(lw, tau=wl.tau, max_batch=8)
         ws8 = sffn.new_workspace(sffn.sffn_workspace_size(prof, 8), dev)
         perm, counts = sffn.hot_first_order(prof, W.make_profile_tokens(wl, layer=layer, device=dev), ws8)
-        hot = sffn.hot_row_count(counts, wl.profile_tokens)
+        hot = sffn.hot_row_count(counts, wl.profile_tokens, hot_frac)
         ea = float(counts.sum().item()) / wl.profile_tokens
+        row_bytes = (3 if wl.act == "reglu" else 2) * wl.d_model * ESIZE[wl.dtype]
+        warm = sffn.warm_row_count(counts, wl.profile_tokens, row_bytes, warm_frac) if warm_frac > 0 else 0
         prof.close()
         lw = sffn.permute_layer_weights(lw, torch.from_numpy(perm).to(dev))
-    return lw, hot, ea
+    return lw, hot, ea, warm
 
 
 def clone_layer(W, lw):
@@ -256,22 +262,24 @@ def bench_sffn(args):
 
     # ---- layers: single layers as R rotating replicas, stacks as their L layers
     if stack:
-        lws, hots, eas = [], [], []
+        lws, hots, eas, warms = [], [], [], []
         for l in range(L):
-            lw, hot, ea = build_layer(sffn, W, wl, l, dev)
+            lw, hot, ea, warm = build_layer(sffn, W, wl, l, dev, args.hot_frac, args.warm_frac)
             lws.append(lw)
             hots.append(hot)
             eas.append(ea)
-        layers = [sffn.Layer.from_weights(lw, tau=wl.tau, max_batch=B, flags=flags, hot_rows=h, expected_active=e)
-                  for lw, h, e in zip(lws, hots, eas)]
+            warms.append(warm)
+        layers = [sffn.Layer.from_weights(lw, tau=wl.tau, max_batch=B, flags=flags, hot_rows=h, expected_active=e,
+                                          warm_rows=wr)
+                  for lw, h, e, wr in zip(lws, hots, eas, warms)]
         R = 1
         hot_rows = hots[0]
     else:
-        lw, hot_rows, ea = build_layer(sffn, W, wl, 0, dev)
+        lw, hot_rows, ea, warm = build_layer(sffn, W, wl, 0, dev, args.hot_frac, args.warm_frac)
         R = max(1, args.replicas)
         lws = [lw] + [clone_layer(W, lw) for _ in range(R - 1)]
         layers = [sffn.Layer.from_weights(x, tau=wl.tau, max_batch=B, flags=flags, hot_rows=hot_rows,
-                                          expected_active=ea) for x in lws]
+                                          expected_active=ea, warm_rows=warm) for x in lws]
     torch.cuda.synchronize()
     lw = lws[0]
 
@@ -461,6 +469,7 @@ def bench_sffn(args):
             "mean_active": round(float(np.mean(n_tok)), 1),
             "mean_union": round(float(np.mean(n_union)), 1) if B > 1 else None,
             "hot_rows": hot_rows,
+            "warm_rows": layers[0].desc.warm_rows,
             "us_per_layer": round(us_per_layer, 3),
             "dominant_kernel_us_per_launch": round(k_ms * 1e3, 3),
             "kernel_timing": ktiming,

@@ -105,6 +105,13 @@ typedef struct {
                            token (e.g. from the profile counts), 0 = unknown;
                            a hint for how much work to start before the
                            active rows are balanced over the SMs.           */
+  int32_t warm_rows;    /* neurons [0, warm_rows) are likely active (e.g. the
+                           hot-first rows active for >= 20% of profile tokens):
+                           the batch-1 kernel pulls their rows into L2 while
+                           the predictor runs, when DRAM is otherwise idle.
+                           Speculative: rows that turn out inactive cost DRAM
+                           bandwidth only; results do not depend on it.
+                           0 = none; must be in [0, d_ff].                  */
 } sffn_layer_desc;
 
 /* Batch-1 calls normally run the whole layer (predictor, threshold, gather,

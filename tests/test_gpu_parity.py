@@ -203,15 +203,16 @@ def test_all_false_and_all_true_masks(sffn, tau, expect, batch):
                 assert rel_l2(Y[s, b], oracle.dense_ffn(ol, Xh[s, b])) < TOL["f16"]
 
 
-@pytest.mark.parametrize("hot_rows", [0, 10, 100, 1500])
-def test_hot_row_prefetch_any_setting(sffn, hot_rows):
-    """Rows of "hot" neurons are fetched before the predictor decides; when a
-    prefetched neuron turns out inactive the copy is discarded.  With every
-    neuron declared hot most prefetches are wasted, and the result is the same."""
+@pytest.mark.parametrize("hot_rows,warm_rows", [(0, 0), (10, 0), (100, 0), (1500, 0), (0, 700), (100, 1500)])
+def test_hot_row_prefetch_any_setting(sffn, hot_rows, warm_rows):
+    """Rows of "hot" neurons are fetched before the predictor decides, and the
+    rows of "warm" neurons are pulled into L2; when such a neuron turns out
+    inactive the copy is wasted.  With every neuron declared hot or warm most
+    prefetches are wasted, and the result is the same."""
     wl = W.tiny_workload(d_model=1024, d_ff=1500, rank=32, dtype="f16", mean_p=0.1, name="hot-prefetch")
     lw = W.make_layer(wl, device=DEV)
     ol = oracle_layer(lw)
-    layer = sffn.Layer.from_weights(lw, hot_rows=hot_rows)
+    layer = sffn.Layer.from_weights(lw, hot_rows=hot_rows, warm_rows=warm_rows)
     X = W.make_tokens(wl, 4, device=DEV)
     Y, I, N = run_tokens(sffn, layer, X)
     Xh = st(X)

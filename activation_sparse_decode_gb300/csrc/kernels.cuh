@@ -113,6 +113,8 @@ struct LayerConfig {
 };
 bool layer_config(int dtype, int act, int d, int f, int r, int grid, size_t smem_optin, LayerConfig* cfg);
 cudaError_t launch_layer(int dtype, const LayerConfig& cfg, const LayerArgs& a, int grid, cudaStream_t s);
+// Blocks of the layer kernel that can be resident on one SM with this configuration.
+int layer_blocks_per_sm(int dtype, const LayerConfig& cfg);
 
 // ---- batched decode over the union of the tokens' active rows (tensor cores)
 struct UnionArgs {

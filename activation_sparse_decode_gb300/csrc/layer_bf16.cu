@@ -5,4 +5,5 @@ namespace sffn {
 cudaError_t launch_layer_bf16(const LayerConfig& cfg, const LayerArgs& a, int grid, cudaStream_t s) {
   return layer_dispatch<__nv_bfloat16>(cfg, a, grid, s);
 }
+int layer_blocks_per_sm_bf16(const LayerConfig& cfg) { return layer_blocks_per_sm_t<__nv_bfloat16>(cfg); }
 }  // namespace sffn

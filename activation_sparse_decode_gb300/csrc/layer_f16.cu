@@ -5,4 +5,5 @@ namespace sffn {
 cudaError_t launch_layer_f16(const LayerConfig& cfg, const LayerArgs& a, int grid, cudaStream_t s) {
   return layer_dispatch<__half>(cfg, a, grid, s);
 }
+int layer_blocks_per_sm_f16(const LayerConfig& cfg) { return layer_blocks_per_sm_t<__half>(cfg); }
 }  // namespace sffn

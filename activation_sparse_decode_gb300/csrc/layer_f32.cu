@@ -5,4 +5,5 @@ namespace sffn {
 cudaError_t launch_layer_f32(const LayerConfig& cfg, const LayerArgs& a, int grid, cudaStream_t s) {
   return layer_dispatch<float>(cfg, a, grid, s);
 }
+int layer_blocks_per_sm_f32(const LayerConfig& cfg) { return layer_blocks_per_sm_t<float>(cfg); }
 }  // namespace sffn

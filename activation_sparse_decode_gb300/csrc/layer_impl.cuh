@@ -777,10 +777,16 @@ __global__ void __launch_bounds__(kLayerThreads, 1) k_layer(const LayerArgs a) {
   SFFN_TRACE(7);
 }
 
+// The dynamic shared-memory limit set so far for k_layer<T, CPT> (raised, never lowered).
+template <typename T, int CPT>
+int& layer_smem_limit() {
+  static int cur = 48 * 1024;
+  return cur;
+}
+
 template <typename T, int CPT>
 cudaError_t layer_launch(const LayerConfig& cfg, const LayerArgs& a, int grid, cudaStream_t s) {
-  static int cur = 48 * 1024;
-  const cudaError_t e = ensure_dyn_smem(k_layer<T, CPT>, cfg.smem, &cur);
+  const cudaError_t e = ensure_dyn_smem(k_layer<T, CPT>, cfg.smem, &layer_smem_limit<T, CPT>());
   if (e != cudaSuccess) return e;
   // Programmatic dependent launch: this kernel may start while the previous
   // kernel on the stream finishes; it waits for it (griddepcontrol.wait)
@@ -796,6 +802,26 @@ cudaError_t layer_launch(const LayerConfig& cfg, const LayerArgs& a, int grid, c
   lc.attrs = attr;
   lc.numAttrs = 1;
   return cudaLaunchKernelEx(&lc, k_layer<T, CPT>, a);
+}
+
+template <typename T, int CPT>
+int layer_occupancy(const LayerConfig& cfg) {
+  if (ensure_dyn_smem(k_layer<T, CPT>, cfg.smem, &layer_smem_limit<T, CPT>()) != cudaSuccess) return 0;
+  int n = 0;
+  if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, k_layer<T, CPT>, kLayerThreads, cfg.smem) != cudaSuccess) return 0;
+  return n;
+}
+
+template <typename T>
+int layer_blocks_per_sm_t(const LayerConfig& cfg) {
+  switch (cfg.cpt) {
+    case 1: return layer_occupancy<T, 1>(cfg);
+    case 2: return layer_occupancy<T, 2>(cfg);
+    case 3: return layer_occupancy<T, 3>(cfg);
+    case 4: return layer_occupancy<T, 4>(cfg);
+    case 6: return layer_occupancy<T, 6>(cfg);
+  }
+  return 0;
 }
 
 template <typename T>

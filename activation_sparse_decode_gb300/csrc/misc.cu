@@ -190,7 +190,7 @@ bool layer_config(int dtype, int act, int d, int f, int r, int grid, size_t smem
   kc = (kc + unit - 1) / unit * unit;
   const int own_cap = (f + grid - 1) / grid;
   const int nwords = (own_cap + 31) / 32;
-  if (nwords > 256 || grid > 256) return false;  // the balancing holds 8 block counts per lane
+  if (nwords > 256 || grid > 1024) return false;
   const size_t stage = (size_t)(act == kReglu ? 3 : 2) * d * esize;
   // x, h, stage barriers, own biases (2), list + list biases, words, balancing scratch (3 x grid)
   const size_t fixed = (size_t)d * esize + (size_t)((r + 3) & ~3) * 4 + 17 * 8 + (size_t)own_cap * 16 + nwords * 4 +
@@ -269,6 +269,19 @@ cudaError_t launch_score_mma(int dtype, const ScoreMmaArgs& a, int bt, int grid,
     case kBF16: return launch_score_mma_bf16(a, bt, grid, a.ring_bytes, s);
   }
   return cudaErrorInvalidValue;
+}
+
+int layer_blocks_per_sm_f32(const LayerConfig&);
+int layer_blocks_per_sm_f16(const LayerConfig&);
+int layer_blocks_per_sm_bf16(const LayerConfig&);
+
+int layer_blocks_per_sm(int dtype, const LayerConfig& cfg) {
+  switch (dtype) {
+    case kF32: return layer_blocks_per_sm_f32(cfg);
+    case kF16: return layer_blocks_per_sm_f16(cfg);
+    case kBF16: return layer_blocks_per_sm_bf16(cfg);
+  }
+  return 0;
 }
 
 cudaError_t launch_layer_f32(const LayerConfig&, const LayerArgs&, int, cudaStream_t);

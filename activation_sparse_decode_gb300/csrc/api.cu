@@ -26,6 +26,7 @@ struct sffn_layer {
   int KS = 0;          // predictor K-chunks
   int kc32 = 0;        // predictor K-chunk when one block holds up to 32 tokens
   int KS32 = 0;
+  int KStok = 0;       // K-chunks of the lane-per-token hidden-layer kernel (17-32 tokens)
   int RG = 0;          // predictor row groups
   int score_grid = 0;  // blocks of the score kernel
   int gather_grid = 0; // blocks of the gather kernel (one per SM)
@@ -82,7 +83,7 @@ WsLayout layout(const sffn_layer* L, int batch) {
   w.hdr = take(sizeof(WsHeader));
   w.flags = take(barrier_flag_bytes((uint32_t)L->gather_grid));
   w.tickets = take((size_t)L->RG * batch * sizeof(uint32_t));
-  w.h_part = take((size_t)std::max(L->KS, L->KS32) * batch * d.rank * sizeof(float));
+  w.h_part = take((size_t)std::max(std::max(L->KS, L->KS32), L->KStok) * batch * d.rank * sizeof(float));
   w.h = take((size_t)batch * d.rank * sizeof(float));
   w.h3 = take(L->esize == 2 ? (size_t)96 * d.rank * 2 : 0);  // h as three 16-bit parts, up to 32 tokens
   w.mask = take((size_t)batch * L->W * sizeof(uint32_t));
@@ -160,8 +161,11 @@ sffn_status run_predictor(const sffn_layer* L, const void* x, int batch, const W
     // one hidden-layer launch for the whole batch (h also as three 16-bit
     // parts), then the scores and threshold as one tensor-core product
     const int bt = batch <= 8 ? 8 : batch <= 16 ? 16 : 32;
-    PredHiddenArgs ha{d.pred_V, x, batch, d.rank, d.d_model, L->kc32, L->KS32, ws.h_part(), ws.h(), ws.tickets(),
-                      ws.h3(), bt};
+    // above 16 tokens the lane-per-token kernel (K-chunks of 256); below it
+    // would leave most lanes idle
+    const bool tok = batch > 16;
+    PredHiddenArgs ha{d.pred_V, x, batch, d.rank, d.d_model, tok ? 256 : L->kc32, tok ? L->KStok : L->KS32,
+                      ws.h_part(), ws.h(), ws.tickets(), ws.h3(), bt};
     SFFN_CUDA(launch_pred_hidden(d.dtype, ha, s), "predictor hidden launch");
     ScoreMmaArgs sa{d.pred_U, ws.h3(), d.pred_b, d.tau, batch, d.d_ff, d.rank, L->W, ws.mask(), ws.hdr(), ring,
                     (uint64_t)g_wait_ns};
@@ -422,6 +426,7 @@ sffn_status sffn_create_layer(const sffn_layer_desc* desc, sffn_layer_t* out) {
   const int max_kc32 = 2048 / esize;  // x chunk of 32 tokens must stay within 64 KB of shared memory
   L->kc32 = std::min(kc, std::max(unit, max_kc32 / unit * unit));
   L->KS32 = (d.d_model + L->kc32 - 1) / L->kc32;
+  L->KStok = (d.d_model + 255) / 256;  // the lane-per-token kernel's K-chunks of 256
   L->score_grid = std::min((d.d_ff + 63) / 64, 8 * L->sms);
 
   L->gather_grid = L->sms;

@@ -133,6 +133,115 @@ __global__ void __launch_bounds__(kHiddenWarps * 32)
   }
 }
 
+// Hidden layer for a batch of up to 32 tokens, lane = token.  Grid (KS row
+// K-chunks, r / 32 row groups).  A block stages its 32 rows of V and the
+// tokens' K-chunk in shared memory as fp32 (token rows padded so the lanes'
+// float4 loads spread over the banks); warp w accumulates rows 4w .. 4w+3
+// for token `lane` over the chunk -- no cross-lane reduction -- and writes
+// the partial sums; the last block of a row group to arrive sums the KS
+// partials in a fixed order, writes h and, for the tensor-core score
+// product, h as three 16-bit parts.
+constexpr int kTokRows = 32;   // rows of V per block
+constexpr int kTokKc = 256;    // K-chunk
+
+template <typename T>
+__global__ void __launch_bounds__(256)
+    k_pred_hidden_tok(const T* __restrict__ V, const T* __restrict__ x, int B, int r, int d, int KS,
+                      float* __restrict__ h_part, float* __restrict__ h, uint32_t* __restrict__ tickets,
+                      T* __restrict__ h3, int BT) {
+  constexpr int E = Chunk<T>::N;
+  constexpr int XP = kTokKc + 4;  // padded token row (floats)
+  extern __shared__ __align__(16) float tok_smem[];
+  float(*vs)[kTokKc] = reinterpret_cast<float(*)[kTokKc]>(tok_smem);                 // [kTokRows][kTokKc]
+  float(*xs)[XP] = reinterpret_cast<float(*)[XP]>(tok_smem + kTokRows * kTokKc);     // [32][XP]
+  __shared__ uint32_t s_last;
+  const int ks = blockIdx.x, rg = blockIdx.y;
+  const int k0 = ks * kTokKc, kn = min(kTokKc, d - k0);
+  const int row0 = rg * kTokRows;
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  const int nchk = kn / E;  // 16-byte chunks of the K-chunk per row
+  for (int i = tid; i < kTokRows * nchk; i += 256) {
+    const int rr = i / nchk, c = i - rr * nchk;
+    float v[E];
+    if (row0 + rr < r)
+      unpack<T>(ldg_stream(V + (size_t)(row0 + rr) * d + k0 + c * E), v);
+    else
+#pragma unroll
+      for (int e = 0; e < E; ++e) v[e] = 0.f;
+#pragma unroll
+    for (int e = 0; e < E; ++e) vs[rr][c * E + e] = v[e];
+  }
+  for (int i = tid; i < 32 * nchk; i += 256) {
+    const int bb = i / nchk, c = i - bb * nchk;
+    float v[E];
+    if (bb < B)
+      unpack<T>(*reinterpret_cast<const uint4*>(x + (size_t)bb * d + k0 + c * E), v);
+    else
+#pragma unroll
+      for (int e = 0; e < E; ++e) v[e] = 0.f;
+#pragma unroll
+    for (int e = 0; e < E; ++e) xs[bb][c * E + e] = v[e];
+  }
+  __syncthreads();
+  float acc[4] = {0.f, 0.f, 0.f, 0.f};
+  const float* xr = xs[lane];
+#pragma unroll 4
+  for (int k = 0; k < kn; k += 4) {
+    const float4 xv = *reinterpret_cast<const float4*>(xr + k);
+#pragma unroll
+    for (int q = 0; q < 4; ++q) {
+      const float4 vv = *reinterpret_cast<const float4*>(&vs[warp * 4 + q][k]);
+      acc[q] = fmaf(vv.x, xv.x, fmaf(vv.y, xv.y, fmaf(vv.z, xv.z, fmaf(vv.w, xv.w, acc[q]))));
+    }
+  }
+  const int rowq = row0 + warp * 4;
+  if (lane < B) {
+#pragma unroll
+    for (int q = 0; q < 4; ++q)
+      if (rowq + q < r) h_part[((size_t)ks * B + lane) * r + rowq + q] = acc[q];
+  }
+  __syncthreads();
+  if (tid == 0) {
+    __threadfence();
+    uint32_t* t = &tickets[rg];
+    const uint32_t prev = atomicAdd(t, 1u);
+    s_last = (prev == (uint32_t)KS - 1u);
+    if (s_last) {
+      atomicExch(t, 0u);
+      __threadfence();
+    }
+  }
+  __syncthreads();
+  if (!s_last) return;
+  for (int i = tid; i < kTokRows * B; i += 256) {
+    const int bb = i / kTokRows, q = i - bb * kTokRows;
+    const int row = row0 + q;
+    if (row >= r) continue;
+    const float* hp = h_part + (size_t)bb * r + row;
+    const size_t kstride = (size_t)B * r;
+    float sum = 0.f;
+    int k = 0;
+    for (; k + 8 <= KS; k += 8) {
+      float v[8];
+#pragma unroll
+      for (int u = 0; u < 8; ++u) v[u] = __ldcg(hp + (size_t)(k + u) * kstride);
+#pragma unroll
+      for (int u = 0; u < 8; ++u) sum += v[u];
+    }
+    for (; k < KS; ++k) sum += __ldcg(hp + (size_t)k * kstride);
+    h[(size_t)bb * r + row] = sum;
+    if (h3 != nullptr) {  // three 16-bit parts whose sum carries the fp32 value
+      const T hi = from_float<T>(sum);
+      const float rest = sum - static_cast<float>(hi);
+      const T mid = from_float<T>(rest);
+      const T lo = from_float<T>(rest - static_cast<float>(mid));
+      h3[(size_t)(0 * BT + bb) * r + row] = hi;
+      h3[(size_t)(1 * BT + bb) * r + row] = mid;
+      h3[(size_t)(2 * BT + bb) * r + row] = lo;
+    }
+  }
+}
+
 // Scores.  A block owns 64-row blocks (two mask words) in a grid-stride loop;
 // each warp streams 8 rows of U, lane l holding the 16-byte chunks l, l+32, ...
 // of every row (CPL chunks), and rows are summed with a warp all-reduce.
@@ -298,6 +407,17 @@ cudaError_t hidden_launch(const PredHiddenArgs& a, cudaStream_t s) {
 
 template <typename T>
 cudaError_t hidden_dispatch(const PredHiddenArgs& a, cudaStream_t s) {
+  if (a.bt == 32 && a.B > 16) {  // one group of 17-32 tokens: lane = token kernel, K-chunks of 256
+    if (a.B > 32 || a.kc_elems != kTokKc) return cudaErrorInvalidValue;
+    const dim3 grid(a.KS, (a.r + kTokRows - 1) / kTokRows);
+    const size_t smem = (size_t)(kTokRows * kTokKc + 32 * (kTokKc + 4)) * sizeof(float);
+    static int cur = 48 * 1024;
+    const cudaError_t e = ensure_dyn_smem(k_pred_hidden_tok<T>, smem, &cur);
+    if (e != cudaSuccess) return e;
+    k_pred_hidden_tok<T><<<grid, 256, smem, s>>>(static_cast<const T*>(a.V), static_cast<const T*>(a.x), a.B, a.r,
+                                                 a.d, a.KS, a.h_part, a.h, a.tickets, static_cast<T*>(a.h3), a.bt);
+    return cudaGetLastError();
+  }
   if (a.bt == 8) return hidden_launch<T, 8>(a, s);
   if (a.bt == 16) return hidden_launch<T, 16>(a, s);
   if (a.bt == 32) return hidden_launch<T, 32>(a, s);

@@ -362,6 +362,12 @@ __global__ void __launch_bounds__(kLayerThreads, 1) k_layer(const LayerArgs a) {
   for (int j = 0; j < n_hot; ++j) fill_hot(j);
   if (!passed) {
     cp_async_wait_all();  // nothing of this block is left in flight
+    if (a.pair) {         // the partner block still meets the two cluster barriers of the pair exchange
+      if (tid == 0) s_nloc = 0;
+      __syncthreads();
+      cluster_sync_all();
+      cluster_sync_all();
+    }
     return;
   }
 
@@ -503,6 +509,34 @@ __global__ void __launch_bounds__(kLayerThreads, 1) k_layer(const LayerArgs a) {
   __syncthreads();
   int nloc = s_nloc;
   SFFN_TRACE_VAL(11, nloc);
+
+  // ---- pair exchange (clusters of two blocks): the active rows of a token
+  // fall unevenly on the blocks, and the block with the most sets the
+  // kernel's length.  The two blocks of a cluster split their rows evenly: a
+  // block above its share (at least its prefilled hot stages) hands its last
+  // -- coldest -- rows to the other, which reads them from its shared memory.
+  // Every block passes both cluster barriers exactly once (the failure path
+  // above too); nothing reads a peer's shared memory after the second.
+  if (a.pair) {
+    cluster_sync_all();  // both lists and counts are in place
+    const uint32_t rk = cluster_rank();
+    const int np = ld_peer_s32(peer_smem(&s_nloc, rk ^ 1u));
+    const int tot = nloc + np;
+    const int cap_me = rk == 0 ? (tot + 1) / 2 : tot / 2, cap_peer = tot - cap_me;
+    const int keep_me = min(nloc, max(cap_me, a.hot_stages));
+    const int keep_peer = min(np, max(cap_peer, a.hot_stages));
+    if (np > keep_peer) {  // receive the peer's rows [keep_peer, np)
+      const uint32_t pl = peer_smem(list, rk ^ 1u), pb = peer_smem(lbias, rk ^ 1u);
+      for (int t = tid; t < np - keep_peer; t += kLayerThreads) {
+        list[nloc + t] = ld_peer_s32(pl + 4u * (uint32_t)(keep_peer + t));
+        lbias[nloc + t] = ld_peer_f32(pb + 4u * (uint32_t)(keep_peer + t));
+      }
+      nloc += np - keep_peer;
+    } else {
+      nloc = keep_me;
+    }
+    cluster_sync_all();  // the peer has read what it needed
+  }
 
   // ---- phase 5: the active rows stream through a ring of S one-neuron stages,
   // consumed in groups of up to kGroup neurons per block-wide reduction.
@@ -777,6 +811,7 @@ __global__ void __launch_bounds__(kLayerThreads, 1) k_layer(const LayerArgs a) {
   SFFN_TRACE(7);
 }
 
+
 // The dynamic shared-memory limit set so far for k_layer<T, CPT> (raised, never lowered).
 template <typename T, int CPT>
 int& layer_smem_limit() {
@@ -796,11 +831,15 @@ cudaError_t layer_launch(const LayerConfig& cfg, const LayerArgs& a, int grid, c
   lc.blockDim = dim3(kLayerThreads);
   lc.dynamicSmemBytes = cfg.smem;
   lc.stream = s;
-  cudaLaunchAttribute attr[1];
+  cudaLaunchAttribute attr[2];
   attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
   attr[0].val.programmaticStreamSerializationAllowed = 1;
+  attr[1].id = cudaLaunchAttributeClusterDimension;
+  attr[1].val.clusterDim.x = 2;
+  attr[1].val.clusterDim.y = 1;
+  attr[1].val.clusterDim.z = 1;
   lc.attrs = attr;
-  lc.numAttrs = 1;
+  lc.numAttrs = a.pair ? 2 : 1;
   return cudaLaunchKernelEx(&lc, k_layer<T, CPT>, a);
 }
 
@@ -810,6 +849,37 @@ int layer_occupancy(const LayerConfig& cfg) {
   int n = 0;
   if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, k_layer<T, CPT>, kLayerThreads, cfg.smem) != cudaSuccess) return 0;
   return n;
+}
+
+template <typename T, int CPT>
+int layer_pairs(const LayerConfig& cfg, int grid) {
+  if (ensure_dyn_smem(k_layer<T, CPT>, cfg.smem, &layer_smem_limit<T, CPT>()) != cudaSuccess) return 0;
+  cudaLaunchConfig_t lc{};
+  lc.gridDim = dim3(grid);
+  lc.blockDim = dim3(kLayerThreads);
+  lc.dynamicSmemBytes = cfg.smem;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeClusterDimension;
+  attr[0].val.clusterDim.x = 2;
+  attr[0].val.clusterDim.y = 1;
+  attr[0].val.clusterDim.z = 1;
+  lc.attrs = attr;
+  lc.numAttrs = 1;
+  int n = 0;
+  if (cudaOccupancyMaxActiveClusters(&n, k_layer<T, CPT>, &lc) != cudaSuccess) return 0;
+  return n;
+}
+
+template <typename T>
+int layer_max_pairs_t(const LayerConfig& cfg, int grid) {
+  switch (cfg.cpt) {
+    case 1: return layer_pairs<T, 1>(cfg, grid);
+    case 2: return layer_pairs<T, 2>(cfg, grid);
+    case 3: return layer_pairs<T, 3>(cfg, grid);
+    case 4: return layer_pairs<T, 4>(cfg, grid);
+    case 6: return layer_pairs<T, 6>(cfg, grid);
+  }
+  return 0;
 }
 
 template <typename T>

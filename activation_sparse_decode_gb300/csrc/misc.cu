@@ -275,6 +275,19 @@ int layer_blocks_per_sm_f32(const LayerConfig&);
 int layer_blocks_per_sm_f16(const LayerConfig&);
 int layer_blocks_per_sm_bf16(const LayerConfig&);
 
+int layer_max_pairs_f32(const LayerConfig&, int);
+int layer_max_pairs_f16(const LayerConfig&, int);
+int layer_max_pairs_bf16(const LayerConfig&, int);
+
+int layer_max_pairs(int dtype, const LayerConfig& cfg, int grid) {
+  switch (dtype) {
+    case kF32: return layer_max_pairs_f32(cfg, grid);
+    case kF16: return layer_max_pairs_f16(cfg, grid);
+    case kBF16: return layer_max_pairs_bf16(cfg, grid);
+  }
+  return 0;
+}
+
 int layer_blocks_per_sm(int dtype, const LayerConfig& cfg) {
   switch (dtype) {
     case kF32: return layer_blocks_per_sm_f32(cfg);

@@ -258,7 +258,7 @@ def bench_sffn(args):
     d, f, r = wl.d_model, wl.d_ff, wl.rank
     W_words = (f + 31) // 32
     flags = sffn.SFFN_FLAG_ROW_GATHER if args.row_gather else 0
-    union_path = B >= 8 and wl.dtype != "f32" and d % 128 == 0 and not args.row_gather
+    union_path = B >= 3 and wl.dtype != "f32" and d % 128 == 0 and not args.row_gather
 
     # ---- layers: single layers as R rotating replicas, stacks as their L layers
     if stack:
@@ -346,9 +346,11 @@ def bench_sffn(args):
     if B == 1 and not (flags & sffn.SFFN_FLAG_MULTI_KERNEL):
         per_layer = 1 + (1 if stack else 0)  # stacks: the LayerNorm is folded into the next layer's kernel
         launches_per_step = T * L + (1 if stack else 0)
+    elif union_path:  # hidden layer, scores (one launch each for the whole batch), union kernel
+        per_layer = 3 + (1 if stack else 0)
+        launches_per_step = T * L * per_layer
     else:
-        sparse = 1 if union_path else (B + 3) // 4
-        per_layer = 2 * groups + sparse + (1 if stack else 0)
+        per_layer = 2 * groups + (B + 3) // 4 + (1 if stack else 0)
         launches_per_step = T * L * per_layer
 
     # ---- device-timed steps (inputs resident in HBM); every replay and event on `stream`

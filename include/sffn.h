@@ -126,12 +126,13 @@ typedef struct {
  * split of active rows costs more (wide rows, many rows per SM).  Needs d_ff
  * of at least 8 rows per SM, otherwise ignored. */
 #define SFFN_FLAG_BALANCE 2
-/* Batches of 8 to 32 tokens with fp16/bf16 weights (d_model a multiple of 128)
+/* Batches of 3 to 32 tokens with fp16/bf16 weights (d_model a multiple of 128)
  * normally run on the tensor-core union path: the union of the tokens' active
- * rows is read once, both products are tcgen05 MMAs, and y is accumulated
- * with float atomics (summation order varies from run to run).  With this
- * flag such batches use the CUDA-core row gather instead (passes of up to 4
- * tokens, fixed-order reduction, bit-reproducible). */
+ * rows is read once, both products are tcgen05 MMAs (the predictor's scores
+ * too, when the rank is a multiple of 64), and y is accumulated with float atomics
+ * (summation order varies from run to run).  With this flag such batches use
+ * the CUDA-core predictor and row gather instead (passes of up to 4 tokens,
+ * fixed-order reduction, bit-reproducible). */
 #define SFFN_FLAG_ROW_GATHER 4
 
 /* Validates the descriptor and records it with launch settings chosen for the

@@ -240,10 +240,11 @@ def test_row_balancing(sffn, flags, expected):
 
 
 def test_deterministic_run_to_run(sffn, c3):
-    """The multi-kernel path reduces block partials in a fixed order (the
-    single-launch kernel adds them with float atomics instead)."""
+    """With SFFN_FLAG_ROW_GATHER batches run the CUDA-core row gather, which
+    reduces block partials in a fixed order: bit-reproducible (the
+    single-launch kernel and the union path add with float atomics instead)."""
     wl, lw, _ = c3
-    layer = sffn.Layer.from_weights(lw, max_batch=4)
+    layer = sffn.Layer.from_weights(lw, max_batch=4, flags=sffn.SFFN_FLAG_ROW_GATHER)
     X = W.make_tokens(wl, 1, batch=4, device=DEV)
     a, _, _ = run_tokens(sffn, layer, X, want_idx=False)
     b, _, _ = run_tokens(sffn, layer, X, want_idx=False)

@@ -477,32 +477,21 @@ __global__ void __launch_bounds__(kLayerThreads, 1) k_layer(const LayerArgs a) {
   }
   __syncthreads();
   SFFN_TRACE(9);
-  // ascending list of active owned rows: warp 0 scans the word popcounts
+  // ascending list of active owned rows: warp 0 takes one 32-row word per
+  // step, lane k holding row k's flag; a ballot forms the word and each
+  // active lane writes its row at its rank
   if (warp == 0) {
     int base = 0;
-    for (int q0 = 0; q0 < nwords; q0 += 32) {
-      const int q = q0 + lane;
-      uint32_t bits = 0u;  // word q of the activity flags
-      for (int k = 0; k < 32; ++k) {
-        const int j = q * 32 + k;
-        if (q < nwords && j < n_own && s_act[j]) bits |= 1u << k;
-      }
-      const int cnt = __popc(bits);
-      int incl = cnt;
-#pragma unroll
-      for (int o = 1; o < 32; o <<= 1) {
-        const int v = __shfl_up_sync(0xffffffffu, incl, o);
-        if (lane >= o) incl += v;
-      }
-      int pos = base + incl - cnt;
-      while (bits) {
-        const int k = __ffs(bits) - 1;
-        bits &= bits - 1;
-        const int j = q * 32 + k;
+    for (int q = 0; q < nwords; ++q) {
+      const int j = q * 32 + lane;
+      const bool on = j < n_own && s_act[j] != 0;
+      const uint32_t bits = __ballot_sync(0xffffffffu, on);
+      if (on) {
+        const int pos = base + __popc(bits & ((1u << lane) - 1u));
         list[pos] = c + j * G;
-        lbias[pos++] = ownb[j];
+        lbias[pos] = ownb[j];
       }
-      base += __shfl_sync(0xffffffffu, incl, 31);
+      base += __popc(bits);
     }
     if (lane == 0) s_nloc = base;
   }

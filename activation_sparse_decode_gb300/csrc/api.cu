@@ -36,7 +36,7 @@ struct sffn_layer {
   LayerConfig lcfg{};    // single-launch batch-1 layer kernel
   bool lcfg_ok = false;
   int layer_grid = 0;    // its blocks: two per SM when two fit, else one
-  bool layer_pairs = false;  // launched in clusters of two (every pair co-resident)
+  int layer_cluster = 0;  // > 1: launched in clusters of this many blocks (every cluster co-resident)
   bool fused() const { return lcfg_ok && !(desc.flags & SFFN_FLAG_MULTI_KERNEL); }
 };
 
@@ -320,7 +320,7 @@ sffn_status run_layer(const sffn_layer* L, const void* x, const float* y_prev, v
   const int own_cap = (d.d_ff + L->layer_grid - 1) / L->layer_grid;
   // the balancing exchange holds at most 256 block counts
   a.balance = (d.flags & SFFN_FLAG_BALANCE) != 0 && own_cap >= 8 && L->layer_grid <= 256 ? 1 : 0;
-  a.pair = a.balance == 0 && L->layer_pairs ? 1 : 0;
+  a.cluster = a.balance == 0 ? L->layer_cluster : 0;
   int prefill = L->lcfg.hot_stages;
   if (d.expected_active > 0.f)
     prefill = std::max(prefill, std::min(L->lcfg.nstages, (int)(0.85f * d.expected_active / L->layer_grid)));
@@ -473,8 +473,10 @@ sffn_status sffn_create_layer(const sffn_layer_desc* desc, sffn_layer_t* out) {
     // active rows evenly, when every pair fits at once (ReGLU layer 42.0K ->
     // 45.9K tokens/s; at two blocks per SM the exchange cost more than the
     // smaller spread of rows saved)
-    L->layer_pairs = L->lcfg_ok && L->layer_grid == L->sms && L->layer_grid % 2 == 0 &&
-                     layer_max_pairs(d.dtype, L->lcfg, L->layer_grid) * 2 >= L->layer_grid;
+    L->layer_cluster = L->lcfg_ok && L->layer_grid == L->sms && L->layer_grid % 2 == 0 &&
+                               layer_max_clusters(d.dtype, L->lcfg, L->layer_grid, 2) * 2 >= L->layer_grid
+                           ? 2
+                           : 0;
   }
   *out = L;
   return SFFN_OK;
@@ -832,7 +834,7 @@ sffn_status sffn_internal_layer_on_scratch(sffn_layer_t L, const void* x, float*
   a.warm_rows = d.warm_rows;
   a.hot_stages = L->lcfg.hot_stages;
   a.balance = 0;
-  a.pair = L->layer_pairs ? 1 : 0;
+  a.cluster = L->layer_cluster;
   a.prefill = 0;
   a.wait_ns = (uint64_t)g_wait_ns;
   SFFN_CUDA(launch_layer(d.dtype, L->lcfg, a, L->layer_grid, s), "layer launch");

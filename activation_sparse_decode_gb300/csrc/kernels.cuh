@@ -100,7 +100,8 @@ struct LayerArgs {
   int warm_rows;          // neurons [0, warm_rows): rows warmed in L2 while the predictor runs
   int hot_stages;         // ring stages free of the U rows, usable for that prefetch
   int balance;            // 1: even out the active rows over the blocks (second barrier)
-  int pair;               // 1: launched in clusters of two; the two blocks even out their rows
+  int cluster;            // > 1: launched in clusters of this many blocks, which even out their rows
+  int l2_ahead;           // 1: active rows beyond the ring depth are prefetched into L2 once known
   int prefill;            // own rows each block starts streaming before the balancing
   uint64_t* bal_counts;   // [grid] {epoch, active rows} per block (workspace)
   int32_t* bal_lists;     // [grid][own_cap] {neuron, bias bits} pairs per block (workspace)
@@ -109,15 +110,15 @@ struct LayerArgs {
   uint64_t wait_ns;
 };
 struct LayerConfig {
-  int cpt, nstages, u_smem, KS, kc, RG, hot_stages;
+  int cpt, act, nstages, u_smem, KS, kc, RG, hot_stages;
   size_t region_bytes, u_off, smem;
 };
 bool layer_config(int dtype, int act, int d, int f, int r, int grid, size_t smem_optin, LayerConfig* cfg);
 cudaError_t launch_layer(int dtype, const LayerConfig& cfg, const LayerArgs& a, int grid, cudaStream_t s);
 // Blocks of the layer kernel that can be resident on one SM with this configuration.
 int layer_blocks_per_sm(int dtype, const LayerConfig& cfg);
-// Clusters of two blocks of the layer kernel that can be resident at once.
-int layer_max_pairs(int dtype, const LayerConfig& cfg, int grid);
+// Clusters of cs blocks of the layer kernel that can be resident at once.
+int layer_max_clusters(int dtype, const LayerConfig& cfg, int grid, int cs);
 
 // ---- batched decode over the union of the tokens' active rows (tensor cores)
 struct UnionArgs {

@@ -40,7 +40,9 @@ namespace sffn {
 #define SFFN_TRACE(k) sffn_phase_trace(k)
 #define SFFN_TRACE_VAL(k, v) sffn_phase_value(k, v)
 #define SFFN_TRACE_AT(k, t) sffn_phase_trace_at(k, t)
+#define SFFN_TRACE_GROUP(k) sffn_phase_trace_group(k)
 #else
+#define SFFN_TRACE_GROUP(k) ((void)0)
 #define SFFN_TRACE_AT(k, t) ((void)0)
 #define SFFN_TRACE(k) ((void)0)
 #define SFFN_TRACE_VAL(k, v) ((void)0)
@@ -48,11 +50,18 @@ namespace sffn {
 
 constexpr int kLayerThreads = 256;
 constexpr int kLayerWarps = kLayerThreads / 32;
-constexpr int kGroup = 4;  // neurons per block-wide reduction in the row ring
+constexpr int kGroup = 2;  // neurons per block-wide reduction in the row ring
 // Warps 0..6 do the copying of phase 0; lane 0 of warp 7 runs the grid
 // barrier, so that no copies of its warp are in flight when it fences.
 constexpr int kCopyThreads = kLayerThreads - 32;
 constexpr int kBarrierThread = kLayerThreads - 32;
+constexpr int kMaxCluster = 8;  // blocks per cluster in the row exchange (portable limit)
+
+// The ring's stage wait once the first test has failed: kept out of line so
+// that the loop body stays small enough for the instruction cache.
+static __device__ __noinline__ bool layer_wait_slow(uint64_t* bar, uint32_t parity, WsHeader* h, uint64_t limit_ns) {
+  return mbar_wait(bar, parity, h, limit_ns, 0x303u);
+}
 
 __device__ __forceinline__ void bulk_prefetch_l2(const void* src, uint32_t bytes) {
   asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(src), "r"(bytes) : "memory");
@@ -90,7 +99,7 @@ __device__ __forceinline__ void pack_store<__nv_bfloat16>(__nv_bfloat16* dst, co
   *reinterpret_cast<uint4*>(dst) = *reinterpret_cast<const uint4*>(o);
 }
 
-template <typename T, int CPT>
+template <typename T, int CPT, int ACT>
 __global__ void __launch_bounds__(kLayerThreads, 1) k_layer(const LayerArgs a) {
   constexpr int CPL = 4;  // up to 4 16-byte chunks of a U row per lane (rank <= 128 * elements per chunk)
   constexpr int E = Chunk<T>::N;
@@ -99,6 +108,7 @@ __global__ void __launch_bounds__(kLayerThreads, 1) k_layer(const LayerArgs a) {
   __shared__ float s_red[2][kLayerWarps][kGroup][2];
   __shared__ float s_warp[kLayerWarps];
   __shared__ int s_nloc;
+  __shared__ int s_cnt[kMaxCluster];  // cluster exchange: every member's active-row count
 
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   const int G = gridDim.x, c = blockIdx.x;
@@ -107,8 +117,8 @@ __global__ void __launch_bounds__(kLayerThreads, 1) k_layer(const LayerArgs a) {
   const int NC = r / E;        // 16-byte chunks per U row
   const uint32_t row_bytes = (uint32_t)d * ES;
   const uint32_t urow_bytes = (uint32_t)r * ES;
-  const bool reglu = a.act == kReglu;
-  const int nrows = reglu ? 3 : 2;
+  constexpr bool reglu = ACT == kReglu;
+  constexpr int nrows = reglu ? 3 : 2;
   const uint32_t stage_bytes = nrows * row_bytes;
   const int S = a.nstages;
   const int n_own = c < f ? (f - c + G - 1) / G : 0;
@@ -362,11 +372,12 @@ __global__ void __launch_bounds__(kLayerThreads, 1) k_layer(const LayerArgs a) {
   for (int j = 0; j < n_hot; ++j) fill_hot(j);
   if (!passed) {
     cp_async_wait_all();  // nothing of this block is left in flight
-    if (a.pair) {         // the partner block still meets the two cluster barriers of the pair exchange
-      if (tid == 0) s_nloc = 0;
-      __syncthreads();
+    if (a.cluster > 1) {  // the other members still meet the barriers of the cluster exchange
+      const uint32_t rk = cluster_rank();
+      if (tid < a.cluster) st_peer_s32(peer_smem(&s_cnt[rk], (uint32_t)tid), 0);
       cluster_sync_all();
-      cluster_sync_all();
+      cluster_arrive_relaxed();
+      cluster_wait();
     }
     return;
   }
@@ -499,32 +510,70 @@ __global__ void __launch_bounds__(kLayerThreads, 1) k_layer(const LayerArgs a) {
   int nloc = s_nloc;
   SFFN_TRACE_VAL(11, nloc);
 
-  // ---- pair exchange (clusters of two blocks): the active rows of a token
-  // fall unevenly on the blocks, and the block with the most sets the
-  // kernel's length.  The two blocks of a cluster split their rows evenly: a
-  // block above its share (at least its prefilled hot stages) hands its last
-  // -- coldest -- rows to the other, which reads them from its shared memory.
-  // Every block passes both cluster barriers exactly once (the failure path
-  // above too); nothing reads a peer's shared memory after the second.
-  if (a.pair) {
-    cluster_sync_all();  // both lists and counts are in place
-    const uint32_t rk = cluster_rank();
-    const int np = ld_peer_s32(peer_smem(&s_nloc, rk ^ 1u));
-    const int tot = nloc + np;
-    const int cap_me = rk == 0 ? (tot + 1) / 2 : tot / 2, cap_peer = tot - cap_me;
-    const int keep_me = min(nloc, max(cap_me, a.hot_stages));
-    const int keep_peer = min(np, max(cap_peer, a.hot_stages));
-    if (np > keep_peer) {  // receive the peer's rows [keep_peer, np)
-      const uint32_t pl = peer_smem(list, rk ^ 1u), pb = peer_smem(lbias, rk ^ 1u);
-      for (int t = tid; t < np - keep_peer; t += kLayerThreads) {
-        list[nloc + t] = ld_peer_s32(pl + 4u * (uint32_t)(keep_peer + t));
-        lbias[nloc + t] = ld_peer_f32(pb + 4u * (uint32_t)(keep_peer + t));
+  // ---- cluster exchange (clusters of CS blocks, CS <= 8): the active rows of
+  // a token fall unevenly on the blocks, and the block with the most sets the
+  // kernel's length.  The blocks of a cluster even out their rows before any
+  // of them starts streaming (copies in flight stretch the round trips of the
+  // exchange): every member writes its count into every member's table, and
+  // after one cluster barrier all compute the same assignment -- capacities
+  // T/CS or T/CS + 1 by rank, each block keeping its rows up to
+  // max(capacity, prefilled hot stages) -- and the rows above that, taken in
+  // rank order, fill the free capacity of the members below their share, in
+  // rank order.  A receiver reads them from the owner's shared memory, then
+  // arrives (without waiting) on a second cluster barrier, whose wait every
+  // block passes just before it exits, so that no block leaves while another
+  // may still read its shared memory.  The failure paths keep the same
+  // barrier sequence.
+  if (a.cluster > 1) {
+    const int CS = a.cluster;
+    const int rk = (int)cluster_rank();
+    if (tid < CS) st_peer_s32(peer_smem(&s_cnt[rk], (uint32_t)tid), nloc);
+    cluster_sync_all();  // every table is complete; every list is in place
+    int cnt[kMaxCluster];
+#pragma unroll
+    for (int i = 0; i < kMaxCluster; ++i) cnt[i] = i < CS ? s_cnt[i] : 0;
+    int tot = 0;
+#pragma unroll
+    for (int i = 0; i < kMaxCluster; ++i) tot += cnt[i];
+    const int base = tot / CS, extra = tot - base * CS;
+    auto keep_of = [&](int i) { return min(cnt[i], max(base + (i < extra ? 1 : 0), a.hot_stages)); };
+    // deficits of the lower ranks, this block's deficit, and the total excess
+    int e_tot = 0, d_before = 0, my_def = 0, my_keep = nloc;
+#pragma unroll
+    for (int i = 0; i < kMaxCluster; ++i) {
+      if (i < CS) {
+        const int def = max(0, base + (i < extra ? 1 : 0) - cnt[i]);
+        if (i < rk) d_before += def;
+        if (i == rk) {
+          my_def = def;
+          my_keep = keep_of(i);
+        }
+        e_tot += cnt[i] - keep_of(i);
       }
-      nloc += np - keep_peer;
-    } else {
-      nloc = keep_me;
     }
-    cluster_sync_all();  // the peer has read what it needed
+    const int n_recv = max(0, min(d_before + my_def, e_tot) - d_before);
+    for (int t = tid; t < n_recv; t += kLayerThreads) {
+      // excess item x belongs to the member whose excess range holds it
+      const int x = d_before + t;
+      int owner = 0, pos = 0, e0 = 0;
+#pragma unroll
+      for (int i = 0; i < kMaxCluster; ++i) {
+        if (i < CS) {
+          const int k = keep_of(i), e = cnt[i] - k;
+          if (x >= e0 && x < e0 + e) {
+            owner = i;
+            pos = k + (x - e0);
+          }
+          e0 += e;
+        }
+      }
+      list[nloc + t] = ld_peer_s32(peer_smem(list + pos, (uint32_t)owner));
+      lbias[nloc + t] = ld_peer_f32(peer_smem(lbias + pos, (uint32_t)owner));
+    }
+    __syncthreads();           // the received entries are in place for every thread
+    cluster_arrive_relaxed();  // this block reads no other member's shared memory from here on
+    nloc = my_keep + n_recv;   // a receiver keeps all of its own rows (my_keep == nloc)
+    SFFN_TRACE(16);
   }
 
   // ---- phase 5: the active rows stream through a ring of S one-neuron stages,
@@ -536,15 +585,12 @@ __global__ void __launch_bounds__(kLayerThreads, 1) k_layer(const LayerArgs a) {
   // phase ahead.  List position p uses stage p % S.
   bool hot_ok = n_hot <= nloc;
   for (int k = 0; k < n_hot && hot_ok; ++k) hot_ok = list[k] == c + k * G;
-  auto parity = [&](int p) -> uint32_t {
-    const int st = p % S;
-    return (uint32_t)((p / S) + ((!hot_ok && st < n_hot) ? 1 : 0)) & 1u;
-  };
   bool failed = false;
   if (!hot_ok)
     for (int k = 0; k < n_hot; ++k) failed |= !mbar_wait(&bars[k], 0, a.hdr, a.wait_ns, 0x305u);
   if (__syncthreads_or(failed)) {
     cp_async_wait_all();
+    if (a.cluster > 1) cluster_wait();  // no member exits while another may read its shared memory
     return;
   }
   // Own rows start streaming now, up to the prefill count when the rows are
@@ -555,6 +601,19 @@ __global__ void __launch_bounds__(kLayerThreads, 1) k_layer(const LayerArgs a) {
   const int P = a.hot_stages;
   const int pre = a.balance ? min(nloc, P) : nloc;
   for (int p = hot_ok ? n_hot : 0; p < min(S, pre); ++p) fill(p % S, list[p]);
+  // Rows past the ring depth are known now but enter the ring only as stages
+  // free up, each refill a full memory round trip: ask L2 for them at once
+  // (behind the ring's own copies), so that the refills find them there.
+  if (!a.balance && a.l2_ahead)
+    for (int p = S + tid; p < nloc; p += kLayerThreads) {
+      const size_t off = (size_t)list[p] * row_bytes;
+      bulk_prefetch_l2(gup + off, row_bytes);
+      if (reglu) bulk_prefetch_l2(ggt + off, row_bytes);
+      bulk_prefetch_l2(gdn + off, row_bytes);
+    }
+
+  SFFN_TRACE_VAL(19, nloc);
+
 
   // ---- balancing: each token's active rows fall unevenly on the blocks (a
   // sum of independent Bernoulli draws per block), and the block with the
@@ -696,19 +755,30 @@ __global__ void __launch_bounds__(kLayerThreads, 1) k_layer(const LayerArgs a) {
 #pragma unroll
     for (int e = 0; e < E; ++e) yacc[cq][e] = 0.f;
   }
+  // Groups of up to kGroup list positions; st0 and ph0 are the stage and the
+  // barrier phase of the group's first position (advanced, not divided out).
   const int ng_max = max(1, min(kGroup, S / 2));
-  int grp = 0;
+  int grp = 0, st0 = 0;
+  uint32_t ph0 = 0;
   for (int p0 = 0, ng = 0; p0 < nloc; p0 += ng, ++grp) {
     // the first group is the prefetched hot rows alone, so it need not wait for a cold row
     ng = (grp == 0 && hot_ok && n_hot > 0) ? min(n_hot, ng_max) : min(ng_max, nloc - p0);
     bool ok = true;
+    int stg[kGroup];
     float pu[kGroup], pg[kGroup];
 #pragma unroll
     for (int g = 0; g < kGroup; ++g) {
       pu[g] = pg[g] = 0.f;
+      int st = st0 + g;
+      uint32_t ph = ph0;
+      if (st >= S) {
+        st -= S;
+        ph ^= 1u;
+      }
+      if (!hot_ok && st < n_hot) ph ^= 1u;  // that stage's discarded hot copy took one phase
+      stg[g] = st;
       if (g < ng) {
-        const int st = (p0 + g) % S;
-        ok &= mbar_wait(&bars[st], parity(p0 + g), a.hdr, a.wait_ns, 0x303u);
+        if (!mbar_try_wait(&bars[st], ph)) ok &= layer_wait_slow(&bars[st], ph, a.hdr, a.wait_ns);
         const uint4* up = reinterpret_cast<const uint4*>(region + (size_t)st * stage_bytes);
 #pragma unroll
         for (int cq = 0; cq < CPT; ++cq) {
@@ -728,6 +798,7 @@ __global__ void __launch_bounds__(kLayerThreads, 1) k_layer(const LayerArgs a) {
       }
     }
     if (grp == 0) SFFN_TRACE(10);
+    SFFN_TRACE_GROUP(3 * grp);
 #pragma unroll
     for (int g = 0; g < kGroup; ++g) {
       pu[g] = warp_sum(pu[g]);
@@ -737,13 +808,14 @@ __global__ void __launch_bounds__(kLayerThreads, 1) k_layer(const LayerArgs a) {
 #pragma unroll
       for (int g = 0; g < kGroup; ++g) {
         s_red[grp & 1][warp][g][0] = pu[g];
-        s_red[grp & 1][warp][g][1] = pg[g];
+        if (reglu) s_red[grp & 1][warp][g][1] = pg[g];
       }
     }
     if (__syncthreads_or(!ok)) {
       failed = true;
       break;
     }
+    SFFN_TRACE_GROUP(3 * grp + 1);
     float act[kGroup];
 #pragma unroll
     for (int g = 0; g < kGroup; ++g) {
@@ -751,7 +823,7 @@ __global__ void __launch_bounds__(kLayerThreads, 1) k_layer(const LayerArgs a) {
 #pragma unroll
       for (int w = 0; w < kLayerWarps; ++w) {
         u += s_red[grp & 1][w][g][0];
-        gt += s_red[grp & 1][w][g][1];
+        if (reglu) gt += s_red[grp & 1][w][g][1];
       }
       const float bias = g < ng ? lbias[p0 + g] : 0.f;
       act[g] = g < ng ? (reglu ? fmaxf(gt + bias, 0.f) * u : fmaxf(u + bias, 0.f)) : 0.f;
@@ -759,7 +831,7 @@ __global__ void __launch_bounds__(kLayerThreads, 1) k_layer(const LayerArgs a) {
 #pragma unroll
     for (int g = 0; g < kGroup; ++g) {
       if (g < ng) {
-        const int st = (p0 + g) % S;
+        const int st = stg[g];
         if (act[g] != 0.f) {
           const uint4* dn = reinterpret_cast<const uint4*>(region + (size_t)st * stage_bytes) + (size_t)(nrows - 1) * NCH;
 #pragma unroll
@@ -774,12 +846,20 @@ __global__ void __launch_bounds__(kLayerThreads, 1) k_layer(const LayerArgs a) {
           }
         }
         // this thread is done with its chunks of the stage: refill them
+        // (position p0 + g + S maps to the same stage)
         if (p0 + g + S < nloc) fill(st, list[p0 + g + S]);
       }
     }
+    st0 += ng;
+    if (st0 >= S) {
+      st0 -= S;
+      ph0 ^= 1u;
+    }
+    SFFN_TRACE_GROUP(3 * grp + 2);
   }
   if (failed) {
     cp_async_wait_all();
+    if (a.cluster > 1) cluster_wait();
     return;
   }
 
@@ -798,19 +878,33 @@ __global__ void __launch_bounds__(kLayerThreads, 1) k_layer(const LayerArgs a) {
     }
   }
   SFFN_TRACE(7);
+  if (a.cluster > 1) cluster_wait();  // the second barrier of the cluster exchange
 }
 
 
-// The dynamic shared-memory limit set so far for k_layer<T, CPT> (raised, never lowered).
-template <typename T, int CPT>
+// The dynamic shared-memory limit set so far for k_layer<T, CPT, ACT> (raised, never lowered).
+template <typename T, int CPT, int ACT>
 int& layer_smem_limit() {
   static int cur = 48 * 1024;
   return cur;
 }
 
+// k_layer for the configuration's activation, with its shared-memory limit raised to cfg.smem.
+template <typename T, int CPT>
+void (*layer_kernel(const LayerConfig& cfg, cudaError_t* err))(LayerArgs) {
+  if (cfg.act == kReglu) {
+    *err = ensure_dyn_smem(k_layer<T, CPT, kReglu>, cfg.smem, &layer_smem_limit<T, CPT, kReglu>());
+    return k_layer<T, CPT, kReglu>;
+  }
+  *err = ensure_dyn_smem(k_layer<T, CPT, kRelu>, cfg.smem, &layer_smem_limit<T, CPT, kRelu>());
+  return k_layer<T, CPT, kRelu>;
+}
+
 template <typename T, int CPT>
 cudaError_t layer_launch(const LayerConfig& cfg, const LayerArgs& a, int grid, cudaStream_t s) {
-  const cudaError_t e = ensure_dyn_smem(k_layer<T, CPT>, cfg.smem, &layer_smem_limit<T, CPT>());
+  if (a.act != cfg.act) return cudaErrorInvalidValue;
+  cudaError_t e;
+  void (*kern)(LayerArgs) = layer_kernel<T, CPT>(cfg, &e);
   if (e != cudaSuccess) return e;
   // Programmatic dependent launch: this kernel may start while the previous
   // kernel on the stream finishes; it waits for it (griddepcontrol.wait)
@@ -824,49 +918,53 @@ cudaError_t layer_launch(const LayerConfig& cfg, const LayerArgs& a, int grid, c
   attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
   attr[0].val.programmaticStreamSerializationAllowed = 1;
   attr[1].id = cudaLaunchAttributeClusterDimension;
-  attr[1].val.clusterDim.x = 2;
+  attr[1].val.clusterDim.x = a.cluster > 1 ? a.cluster : 1;
   attr[1].val.clusterDim.y = 1;
   attr[1].val.clusterDim.z = 1;
   lc.attrs = attr;
-  lc.numAttrs = a.pair ? 2 : 1;
-  return cudaLaunchKernelEx(&lc, k_layer<T, CPT>, a);
+  lc.numAttrs = a.cluster > 1 ? 2 : 1;
+  return cudaLaunchKernelEx(&lc, kern, a);
 }
 
 template <typename T, int CPT>
 int layer_occupancy(const LayerConfig& cfg) {
-  if (ensure_dyn_smem(k_layer<T, CPT>, cfg.smem, &layer_smem_limit<T, CPT>()) != cudaSuccess) return 0;
+  cudaError_t e;
+  void (*kern)(LayerArgs) = layer_kernel<T, CPT>(cfg, &e);
+  if (e != cudaSuccess) return 0;
   int n = 0;
-  if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, k_layer<T, CPT>, kLayerThreads, cfg.smem) != cudaSuccess) return 0;
+  if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, kern, kLayerThreads, cfg.smem) != cudaSuccess) return 0;
   return n;
 }
 
 template <typename T, int CPT>
-int layer_pairs(const LayerConfig& cfg, int grid) {
-  if (ensure_dyn_smem(k_layer<T, CPT>, cfg.smem, &layer_smem_limit<T, CPT>()) != cudaSuccess) return 0;
+int layer_clusters(const LayerConfig& cfg, int grid, int cs) {
+  cudaError_t e;
+  void (*kern)(LayerArgs) = layer_kernel<T, CPT>(cfg, &e);
+  if (e != cudaSuccess) return 0;
   cudaLaunchConfig_t lc{};
   lc.gridDim = dim3(grid);
   lc.blockDim = dim3(kLayerThreads);
   lc.dynamicSmemBytes = cfg.smem;
   cudaLaunchAttribute attr[1];
   attr[0].id = cudaLaunchAttributeClusterDimension;
-  attr[0].val.clusterDim.x = 2;
+  attr[0].val.clusterDim.x = cs;
   attr[0].val.clusterDim.y = 1;
   attr[0].val.clusterDim.z = 1;
   lc.attrs = attr;
   lc.numAttrs = 1;
   int n = 0;
-  if (cudaOccupancyMaxActiveClusters(&n, k_layer<T, CPT>, &lc) != cudaSuccess) return 0;
+  if (cudaOccupancyMaxActiveClusters(&n, kern, &lc) != cudaSuccess) return 0;
   return n;
 }
 
 template <typename T>
-int layer_max_pairs_t(const LayerConfig& cfg, int grid) {
+int layer_max_clusters_t(const LayerConfig& cfg, int grid, int cs) {
   switch (cfg.cpt) {
-    case 1: return layer_pairs<T, 1>(cfg, grid);
-    case 2: return layer_pairs<T, 2>(cfg, grid);
-    case 3: return layer_pairs<T, 3>(cfg, grid);
-    case 4: return layer_pairs<T, 4>(cfg, grid);
-    case 6: return layer_pairs<T, 6>(cfg, grid);
+    case 1: return layer_clusters<T, 1>(cfg, grid, cs);
+    case 2: return layer_clusters<T, 2>(cfg, grid, cs);
+    case 3: return layer_clusters<T, 3>(cfg, grid, cs);
+    case 4: return layer_clusters<T, 4>(cfg, grid, cs);
+    case 6: return layer_clusters<T, 6>(cfg, grid, cs);
   }
   return 0;
 }

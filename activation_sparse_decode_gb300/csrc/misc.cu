@@ -201,6 +201,7 @@ bool layer_config(int dtype, int act, int d, int f, int r, int grid, size_t smem
   const size_t s = std::min<size_t>(16, budget / stage);
   const size_t u_bytes = (size_t)own_cap * r * esize;
   cfg->cpt = cpt;
+  cfg->act = act;
   cfg->nstages = (int)s;
   cfg->u_smem = u_bytes <= budget ? 1 : 0;
   cfg->RG = rg;
@@ -275,15 +276,15 @@ int layer_blocks_per_sm_f32(const LayerConfig&);
 int layer_blocks_per_sm_f16(const LayerConfig&);
 int layer_blocks_per_sm_bf16(const LayerConfig&);
 
-int layer_max_pairs_f32(const LayerConfig&, int);
-int layer_max_pairs_f16(const LayerConfig&, int);
-int layer_max_pairs_bf16(const LayerConfig&, int);
+int layer_max_clusters_f32(const LayerConfig&, int, int);
+int layer_max_clusters_f16(const LayerConfig&, int, int);
+int layer_max_clusters_bf16(const LayerConfig&, int, int);
 
-int layer_max_pairs(int dtype, const LayerConfig& cfg, int grid) {
+int layer_max_clusters(int dtype, const LayerConfig& cfg, int grid, int cs) {
   switch (dtype) {
-    case kF32: return layer_max_pairs_f32(cfg, grid);
-    case kF16: return layer_max_pairs_f16(cfg, grid);
-    case kBF16: return layer_max_pairs_bf16(cfg, grid);
+    case kF32: return layer_max_clusters_f32(cfg, grid, cs);
+    case kF16: return layer_max_clusters_f16(cfg, grid, cs);
+    case kBF16: return layer_max_clusters_bf16(cfg, grid, cs);
   }
   return 0;
 }

@@ -89,7 +89,7 @@ WsLayout layout(const sffn_layer* L, int batch) {
   w.h3 = take(L->esize == 2 ? (size_t)96 * d.rank * 2 : 0);  // h as three 16-bit parts, up to 32 tokens
   w.mask = take((size_t)batch * L->W * sizeof(uint32_t));
   w.y_part = take((size_t)L->gather_grid * std::min(batch, L->max_bt) * d.d_model * sizeof(float));
-  w.hl_part = take(L->lcfg_ok ? (size_t)L->lcfg.KS * d.rank * sizeof(float) : 0);
+  w.hl_part = take(L->lcfg_ok ? layer_slot_bytes(d.rank) : 0);
   const size_t own_cap = (size_t)(d.d_ff + L->gather_grid - 1) / L->gather_grid;
   const int lg = std::max(L->gather_grid, L->layer_grid);
   const size_t lown_cap = L->layer_grid > 0 ? (size_t)(d.d_ff + L->layer_grid - 1) / L->layer_grid : own_cap;
@@ -110,7 +110,7 @@ struct Ws {
   void* h3() const { return base + lay.h3; }
   uint32_t* mask() const { return reinterpret_cast<uint32_t*>(base + lay.mask); }
   float* y_part() const { return reinterpret_cast<float*>(base + lay.y_part); }
-  float* hl_part() const { return reinterpret_cast<float*>(base + lay.hl_part); }
+  unsigned long long* hl_slots() const { return reinterpret_cast<unsigned long long*>(base + lay.hl_part); }
   uint64_t* bal_counts() const { return reinterpret_cast<uint64_t*>(base + lay.bal_counts); }
   int32_t* bal_lists() const { return reinterpret_cast<int32_t*>(base + lay.bal_lists); }
 };
@@ -299,7 +299,7 @@ sffn_status run_layer(const sffn_layer* L, const void* x, const float* y_prev, v
   a.w_gate = d.w_gate;
   a.w_downT = d.w_downT;
   a.y = y;
-  a.h_part = ws.hl_part();
+  a.h_slots = ws.hl_slots();
   a.mask = mask;
   a.hdr = ws.hdr();
   a.bar_flags = ws.flags();
@@ -319,7 +319,7 @@ sffn_status run_layer(const sffn_layer* L, const void* x, const float* y_prev, v
   a.hot_stages = L->lcfg.hot_stages;
   const int own_cap = (d.d_ff + L->layer_grid - 1) / L->layer_grid;
   // the balancing exchange holds at most 256 block counts
-  a.balance = (d.flags & SFFN_FLAG_BALANCE) != 0 && own_cap >= 8 && L->layer_grid <= 256 ? 1 : 0;
+  a.balance = L->lcfg.balance && own_cap >= 8 && L->layer_grid <= 256 ? 1 : 0;
   a.cluster = a.balance == 0 ? L->layer_cluster : 0;
   int prefill = L->lcfg.hot_stages;
   if (d.expected_active > 0.f)
@@ -452,21 +452,24 @@ sffn_status sffn_create_layer(const sffn_layer_desc* desc, sffn_layer_t* out) {
   // The batch-1 layer kernel runs two blocks per SM when two fit with at
   // least four ring stages each (two copy rings per SM move more than one:
   // OPT-6.7B layer 44.4K -> 48.9K tokens/s; with three 24 KB ReGLU stages it
-  // was slower), else one; its grid barrier needs every block resident,
-  // which the occupancy query confirms.
+  // was slower), else one; every block waits for h values that other blocks
+  // publish, so every block must be resident, which the occupancy query
+  // confirms.  The balancing scratch takes shared memory only when asked for.
   {
+    const bool balance = (d.flags & SFFN_FLAG_BALANCE) != 0;
     int smem_sm = 0;
     cudaDeviceGetAttribute(&smem_sm, cudaDevAttrMaxSharedMemoryPerMultiprocessor, L->device);
     const size_t half = smem_sm > 0 ? (size_t)smem_sm / 2 - 1024 - 3072 : 0;  // per-block reserve, static smem
     LayerConfig c2{};
-    if (half > 0 && layer_config(d.dtype, d.act, d.d_model, d.d_ff, d.rank, 2 * L->sms, half, &c2) &&
+    if (half > 0 && layer_config(d.dtype, d.act, d.d_model, d.d_ff, d.rank, 2 * L->sms, half, balance, &c2) &&
         c2.nstages >= 4 && layer_blocks_per_sm(d.dtype, c2) >= 2) {
       L->lcfg = c2;
       L->layer_grid = 2 * L->sms;
       L->lcfg_ok = true;
     } else {
       L->layer_grid = L->gather_grid;
-      L->lcfg_ok = layer_config(d.dtype, d.act, d.d_model, d.d_ff, d.rank, L->layer_grid, L->smem_optin, &L->lcfg) &&
+      L->lcfg_ok = layer_config(d.dtype, d.act, d.d_model, d.d_ff, d.rank, L->layer_grid, L->smem_optin, balance,
+                                &L->lcfg) &&
                    layer_blocks_per_sm(d.dtype, L->lcfg) >= 1;
     }
     // With one block per SM, pairs of blocks (clusters of two) split their
@@ -794,17 +797,17 @@ sffn_status sffn_internal_layer_on_scratch(sffn_layer_t L, const void* x, float*
   SFFN_TRY(check_dev_ptr(x, "x"));
   SFFN_TRY(check_dev_ptr(y, "y"));
   const auto& d = L->desc;
-  // header, barrier flags, predictor partial sums -- the workspace layout's order
+  // header, barrier flags, the launch's h slots -- the workspace layout's order
   const size_t flags_off = align_up(sizeof(WsHeader), 256);
   const size_t part_off = flags_off + align_up(barrier_flag_bytes((uint32_t)L->layer_grid), 256);
-  const size_t need = part_off + align_up((size_t)L->lcfg.KS * d.rank * sizeof(float), 256);
+  const size_t need = part_off + align_up(layer_slot_bytes(d.rank), 256);
   if (need > scratch_bytes)
     return fail(SFFN_ERR_UNSUPPORTED, "this layer needs %zu bytes of scratch, the fixed array holds %zu", need,
                 scratch_bytes);
   unsigned char* base = static_cast<unsigned char*>(scratch);
   cudaStream_t s = static_cast<cudaStream_t>(stream);
-  // the barrier counter and flags must start at zero: the array keeps whatever the last call left
-  SFFN_CUDA(cudaMemsetAsync(base, 0, part_off, s), "scratch clear");
+  // the launch counter and the slots must start at zero: the array keeps whatever the last call left
+  SFFN_CUDA(cudaMemsetAsync(base, 0, need, s), "scratch clear");
   LayerArgs a{};
   a.x = x;
   a.V = d.pred_V;
@@ -816,7 +819,7 @@ sffn_status sffn_internal_layer_on_scratch(sffn_layer_t L, const void* x, float*
   a.w_gate = d.w_gate;
   a.w_downT = d.w_downT;
   a.y = y;
-  a.h_part = reinterpret_cast<float*>(base + part_off);
+  a.h_slots = reinterpret_cast<unsigned long long*>(base + part_off);
   a.hdr = reinterpret_cast<WsHeader*>(base);
   a.bar_flags = reinterpret_cast<uint32_t*>(base + flags_off);
   a.d = d.d_model;

@@ -17,7 +17,7 @@ struct WsHeader {
   uint32_t detail;     // where it happened (kernel-specific code)
   uint32_t bar_count;  // grid barrier: arrivals in the current generation
   uint32_t reserved;
-  unsigned long long arrivals;  // counter barrier: arrivals since the workspace was zeroed
+  unsigned long long arrivals;  // layer kernel: launch counter (one per block, rounded up to 2^20 per launch)
   uint32_t pad[58];
 };
 static_assert(sizeof(WsHeader) == 256, "workspace header is 256 bytes");
@@ -161,43 +161,6 @@ __device__ __forceinline__ bool barrier_arrive_wait_warp(WsHeader* h, uint32_t* 
   return __shfl_sync(0xffffffffu, ok, 0) != 0;
 }
 
-// Grid-wide barrier on a monotonic 64-bit arrival counter (h->arrivals): a
-// block arrives with one acq_rel atomic add and, unless it was the last,
-// polls the counter with acquire loads until it reaches the next multiple of
-// `expected`.  The adds form one release sequence, so the poll that sees the
-// final count also sees every block's writes before its arrival; there is no
-// release store and no fence.  The counter is a multiple of `expected` between
-// launches (every barrier completes), so each block derives the barrier's
-// target from the value its own add returned.  Called by all 32 lanes of one
-// warp; returns the same value on all lanes and the target (a per-launch tag)
-// in *target.  Bounded: after limit_ns, kStTimeout and false (zero the
-// workspace before reusing it).
-__device__ __forceinline__ bool counter_barrier_warp(WsHeader* h, uint32_t expected, uint64_t limit_ns,
-                                                     uint32_t detail, unsigned long long* target) {
-  const uint32_t lane = threadIdx.x & 31u;
-  unsigned long long t = 0;
-  int ok = 1;
-  if (lane == 0) {
-    unsigned long long old;
-    asm volatile("atom.add.acq_rel.gpu.global.u64 %0, [%1], 1;" : "=l"(old) : "l"(&h->arrivals) : "memory");
-    t = (old / expected + 1ull) * expected;
-    if (old + 1ull != t) {
-      const uint64_t t0 = globaltimer_ns();
-      while (true) {
-        unsigned long long v;
-        asm volatile("ld.acquire.gpu.global.u64 %0, [%1];" : "=l"(v) : "l"(&h->arrivals) : "memory");
-        if (v >= t) break;
-        if (globaltimer_ns() - t0 > limit_ns) {
-          set_status(h, kStTimeout, detail);
-          ok = 0;
-          break;
-        }
-      }
-    }
-  }
-  *target = __shfl_sync(0xffffffffu, t, 0);
-  return __shfl_sync(0xffffffffu, ok, 0) != 0;
-}
 
 // Whole-block form; warp `bwarp` does the barrier work.
 __device__ __forceinline__ bool grid_barrier(WsHeader* h, uint32_t* flags, uint32_t expected, uint32_t gen,

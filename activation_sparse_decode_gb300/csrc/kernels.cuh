@@ -91,7 +91,7 @@ struct LayerArgs {
   const void* w_gate;
   const void* w_downT;
   float* y;               // [d] output, zeroed and accumulated here
-  float* h_part;          // [KS][r] workspace
+  unsigned long long* h_slots;  // [r][16] {launch tag, h value} in word 0 of each 128-byte line (workspace)
   uint32_t* mask;         // NULL or [ceil(f/32)] words, zeroed and set here
   WsHeader* hdr;
   uint32_t* bar_flags;    // [grid] grid-barrier release flags, 128 bytes apart
@@ -101,7 +101,6 @@ struct LayerArgs {
   int hot_stages;         // ring stages free of the U rows, usable for that prefetch
   int balance;            // 1: even out the active rows over the blocks (second barrier)
   int cluster;            // > 1: launched in clusters of this many blocks, which even out their rows
-  int l2_ahead;           // 1: active rows beyond the ring depth are prefetched into L2 once known
   int prefill;            // own rows each block starts streaming before the balancing
   uint64_t* bal_counts;   // [grid] {epoch, active rows} per block (workspace)
   int32_t* bal_lists;     // [grid][own_cap] {neuron, bias bits} pairs per block (workspace)
@@ -111,9 +110,14 @@ struct LayerArgs {
 };
 struct LayerConfig {
   int cpt, act, nstages, u_smem, KS, kc, RG, hot_stages;
+  int balance;  // 1: shared memory holds the balancing scratch
   size_t region_bytes, u_off, smem;
 };
-bool layer_config(int dtype, int act, int d, int f, int r, int grid, size_t smem_optin, LayerConfig* cfg);
+bool layer_config(int dtype, int act, int d, int f, int r, int grid, size_t smem_optin, bool balance,
+                  LayerConfig* cfg);
+// Workspace bytes of the layer kernel's h slots: one {tag, h value} word per
+// rank row, each on its own 128-byte line.
+inline size_t layer_slot_bytes(int r) { return (size_t)r * 128; }
 cudaError_t launch_layer(int dtype, const LayerConfig& cfg, const LayerArgs& a, int grid, cudaStream_t s);
 // Blocks of the layer kernel that can be resident on one SM with this configuration.
 int layer_blocks_per_sm(int dtype, const LayerConfig& cfg);

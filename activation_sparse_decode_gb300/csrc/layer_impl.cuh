@@ -53,7 +53,7 @@ constexpr int kLayerWarps = kLayerThreads / 32;
 constexpr int kGroup = 2;  // neurons per block-wide reduction in the row ring
 // Warps 0..6 do the copying of phase 0; lane 0 of warp 7 runs the grid
 // barrier, so that no copies of its warp are in flight when it fences.
-constexpr int kCopyThreads = kLayerThreads - 32;
+constexpr int kSlotStride = 16;  // launch slots: one per 128-byte line (16 words)
 constexpr int kBarrierThread = kLayerThreads - 32;
 constexpr int kMaxCluster = 8;  // blocks per cluster in the row exchange (portable limit)
 
@@ -109,6 +109,7 @@ __global__ void __launch_bounds__(kLayerThreads, 1) k_layer(const LayerArgs a) {
   __shared__ float s_warp[kLayerWarps];
   __shared__ int s_nloc;
   __shared__ int s_cnt[kMaxCluster];  // cluster exchange: every member's active-row count
+  __shared__ int s_passed;
 
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   const int G = gridDim.x, c = blockIdx.x;
@@ -135,58 +136,13 @@ __global__ void __launch_bounds__(kLayerThreads, 1) k_layer(const LayerArgs a) {
   uint32_t* words = reinterpret_cast<uint32_t*>(ownpb + own_cap);
   int32_t* list = reinterpret_cast<int32_t*>(words + nwords);  // active neurons (global index) per ring position
   float* lbias = reinterpret_cast<float*>(list + own_cap);       // their biases
-  int32_t* bal_cnt = reinterpret_cast<int32_t*>(lbias + own_cap);  // balancing: rows per block,
-  int32_t* bal_keep = bal_cnt + G;                                 // rows each block keeps,
-  int32_t* bal_einc = bal_keep + G;                                // inclusive prefix of given-away rows
-  uint8_t* s_act = reinterpret_cast<uint8_t*>(bal_einc + G);      // predicted-active flag per owned row
+  uint8_t* s_act = reinterpret_cast<uint8_t*>(lbias + own_cap);  // predicted-active flag per owned row
+  // balancing scratch, last: allocated only for launches that balance
+  int32_t* bal_cnt = reinterpret_cast<int32_t*>(s_act + ((own_cap + 15) & ~15));  // rows per block,
+  int32_t* bal_keep = bal_cnt + G;                                                // rows each block keeps,
+  int32_t* bal_einc = bal_keep + G;  // inclusive prefix of given-away rows
   SFFN_TRACE(0);
 
-  // ---- phase 0a: before the previous kernel on the stream has finished
-  // (programmatic dependent launch), touch only constant data: warm L2 with
-  // this block's V tiles, owned U rows and hot rows.  The token, the outputs
-  // and the workspace may still be in use by that kernel.
-  {
-    const int tiles = a.RG * a.KS;
-    const unsigned char* V = static_cast<const unsigned char*>(a.V);
-    for (int tile = c; tile < tiles; tile += G) {
-      const int rg = tile / a.KS, ks = tile - rg * a.KS;
-      const int k0 = ks * a.kc, kn = min(a.kc, d - k0);
-      const int row = rg * 16 + tid;
-      if (tid < 16 && row < r) bulk_prefetch_l2(V + ((size_t)row * d + k0) * ES, (uint32_t)kn * ES);
-    }
-    const unsigned char* Ub = static_cast<const unsigned char*>(a.U);
-    const int ulines = (urow_bytes + 127) / 128;
-    for (int q = tid; q < n_own * ulines; q += kLayerThreads) {
-      const int j = q / ulines, l = q - j * ulines;
-      prefetch_l2(Ub + (size_t)(c + (size_t)j * G) * urow_bytes + l * 128);
-    }
-    // hot rows (copied into the ring right after the barrier), then the other
-    // owned warm rows (likely active; read from L2 by the ring if they are)
-    const int nh = c < a.hot_rows ? min(a.hot_stages, min(n_own, (a.hot_rows - c + G - 1) / G)) : 0;
-    const int nw = c < a.warm_rows ? min(n_own, (a.warm_rows - c + G - 1) / G) : 0;
-    const int rlines = (row_bytes + 127) / 128;
-    for (int q = tid; q < max(nh, nw) * rlines; q += kLayerThreads) {
-      const int j = q / rlines, l = q - j * rlines;
-      const size_t off = (size_t)(c + (size_t)j * G) * row_bytes + (size_t)l * 128;
-      prefetch_l2(static_cast<const unsigned char*>(a.w_up) + off);
-      if (reglu) prefetch_l2(static_cast<const unsigned char*>(a.w_gate) + off);
-      prefetch_l2(static_cast<const unsigned char*>(a.w_downT) + off);
-    }
-  }
-  grid_dependency_wait();       // the previous kernel has completed and its writes are visible
-  grid_dependents_launch();     // the next one may start its constant-data phase
-  SFFN_TRACE(18);
-
-  // ---- phase 0b: start every stream, zero the outputs
-  if (a.y_prev == nullptr) {  // the token itself first: everything in phase 1 waits on it
-    const uint4* xg = static_cast<const uint4*>(a.x);
-    if (tid < kCopyThreads)
-      for (int ch = tid; ch < NCH; ch += kCopyThreads) cp_async16(reinterpret_cast<uint4*>(xs) + ch, xg + ch);
-  }
-  cp_async_commit();  // group 1: x
-  // hot rows: the first owned neurons under the hot-first order are almost
-  // always active, so their rows start streaming before the predictor decides
-  const int n_hot = c < a.hot_rows ? min(a.hot_stages, min(n_own, (a.hot_rows - c + G - 1) / G)) : 0;
   const unsigned char* gup = static_cast<const unsigned char*>(a.w_up);
   const unsigned char* ggt = static_cast<const unsigned char*>(a.w_gate);
   const unsigned char* gdn = static_cast<const unsigned char*>(a.w_downT);
@@ -208,25 +164,37 @@ __global__ void __launch_bounds__(kLayerThreads, 1) k_layer(const LayerArgs a) {
     }
     cp_async_arrive_noinc(&bars[s]);
   };
-  // Hot rows, fetched before the predictor decides: warps 0..6 copy every
-  // chunk (the barrier warp has nothing in flight when it fences) and all
-  // threads arrive, so the stage completes when the copies have landed.
-  auto fill_hot = [&](int s) {
-    const size_t off = (size_t)(c + (size_t)s * G) * row_bytes;
-    unsigned char* dst = region + (size_t)s * stage_bytes;
-    if (tid < kCopyThreads)
-      for (int ch = tid; ch < NCH; ch += kCopyThreads) {
-        cp_async16(dst + (size_t)ch * 16, gup + off + (size_t)ch * 16);
-        if (reglu) cp_async16(dst + row_bytes + (size_t)ch * 16, ggt + off + (size_t)ch * 16);
-        cp_async16(dst + (size_t)(nrows - 1) * row_bytes + (size_t)ch * 16, gdn + off + (size_t)ch * 16);
-      }
-    cp_async_arrive_noinc(&bars[s]);
-  };
+
+  // ---- phase 0a: before the previous kernel on the stream has finished
+  // (programmatic dependent launch), touch only constant data and this
+  // block's own shared memory: the first V row this block reduces goes to
+  // registers, its owned U rows and biases to shared memory, its hot rows
+  // (the first owned neurons under the hot-first order, almost always
+  // active) to the first ring stages, and its other V rows and warm rows to
+  // L2.  The token, the outputs and the workspace may still be in use by
+  // that kernel.
+  uint64_t* ubar = bars + S;  // completes when this block's U rows and biases have landed
   if (tid == 0) {
     for (int s = 0; s < S; ++s) mbar_init(&bars[s], kLayerThreads);
+    mbar_init(ubar, kLayerThreads);
     fence_mbar_init();
   }
-  for (int j = tid; j < (tid < kCopyThreads ? n_own : 0); j += kCopyThreads) {
+  __syncthreads();
+  const int nh = c < r ? (r - c + G - 1) / G : 0;  // h rows of this block: c, c + G, ...
+  const uint4* V4 = static_cast<const uint4*>(a.V);
+  // rows are reduced RB at a time (every load of a batch in flight at once);
+  // the first batch's chunks are loaded now
+  constexpr int RB = CPT <= 2 ? 1 : CPT <= 3 ? 2 : 4;
+  uint4 vr[RB][CPT];
+#pragma unroll
+  for (int jj = 0; jj < RB; ++jj)
+#pragma unroll
+    for (int cq = 0; cq < CPT; ++cq) {
+      const int ch = tid + cq * kLayerThreads;
+      vr[jj][cq] = jj < nh && ch < NCH ? ldg_stream(V4 + (size_t)(c + jj * G) * NCH + ch) : make_uint4(0, 0, 0, 0);
+    }
+  if (tid < nh - RB) bulk_prefetch_l2(V4 + (size_t)(c + (tid + RB) * G) * NCH, row_bytes);
+  for (int j = tid; j < n_own; j += kLayerThreads) {
     const int i = c + j * G;
     if (a.b != nullptr)
       cp_async4(&ownb[j], &a.b[i]);
@@ -234,20 +202,72 @@ __global__ void __launch_bounds__(kLayerThreads, 1) k_layer(const LayerArgs a) {
       ownb[j] = 0.f;
     cp_async4(&ownpb[j], &a.pb[i]);
   }
+  const unsigned char* Ub = static_cast<const unsigned char*>(a.U);
+  if (a.u_smem) {  // owned U rows -> shared memory, 16 bytes per copy
+    for (int q = tid; q < n_own * NC; q += kLayerThreads) {
+      const int j = q / NC, ch = q - j * NC;
+      cp_async16(region + a.u_off + (size_t)j * urow_bytes + ch * 16,
+                 Ub + (size_t)(c + (size_t)j * G) * urow_bytes + ch * 16);
+    }
+  } else {  // too large to stage: warm L2 with the owned rows instead
+    const int ulines = (urow_bytes + 127) / 128;
+    for (int q = tid; q < n_own * ulines; q += kLayerThreads) {
+      const int j = q / ulines, l = q - j * ulines;
+      prefetch_l2(Ub + (size_t)(c + (size_t)j * G) * urow_bytes + l * 128);
+    }
+  }
+  cp_async_arrive_noinc(ubar);
+  const int n_hot = c < a.hot_rows ? min(a.hot_stages, min(n_own, (a.hot_rows - c + G - 1) / G)) : 0;
+  for (int j = 0; j < n_hot; ++j) fill(j, c + j * G);
   {
+    const int nw = c < a.warm_rows ? min(n_own, (a.warm_rows - c + G - 1) / G) : 0;
+    const int rlines = (row_bytes + 127) / 128;
+    for (int q = n_hot * rlines + tid; q < nw * rlines; q += kLayerThreads) {
+      const int j = q / rlines, l = q - j * rlines;
+      const size_t off = (size_t)(c + (size_t)j * G) * row_bytes + (size_t)l * 128;
+      prefetch_l2(gup + off);
+      if (reglu) prefetch_l2(ggt + off);
+      prefetch_l2(gdn + off);
+    }
+  }
+  grid_dependency_wait();       // the previous kernel has completed and its writes are visible
+  grid_dependents_launch();     // the next one may start its constant-data phase
+  SFFN_TRACE(18);
+
+  // ---- phase 0b: this launch's tag, the token, zeroed outputs.
+  // Tag: every block adds one to the workspace's launch counter; the last
+  // arrival of a launch rounds the counter up to the next multiple of 2^20,
+  // so the counter's high part numbers the launches whatever their grid
+  // sizes, and every block reads the same number from its own arrival.
+  __shared__ uint32_t s_tag;
+  if (tid == kLayerThreads - 32) {
+    unsigned long long old;
+    asm volatile("atom.add.relaxed.gpu.global.u64 %0, [%1], 1;" : "=l"(old) : "l"(&a.hdr->arrivals) : "memory");
+    const unsigned long long base = old & ~((1ull << 20) - 1ull);
+    if (old - base == (unsigned long long)(G - 1))
+      asm volatile("red.relaxed.gpu.global.add.u64 [%0], %1;" ::"l"(&a.hdr->arrivals),
+                   "l"((unsigned long long)((1u << 20) - G))
+                   : "memory");
+    s_tag = (uint32_t)(base >> 20) + 1u;  // never 0, the value of a zeroed slot
+  }
+  // outputs zeroed by the h-row owners, slice k of y and of the mask with h
+  // row k, so that the slots every block acquires below cover all of them
+  for (int j = 0; j < nh; ++j) {
+    const int k = c + j * G;
     float4* y4 = reinterpret_cast<float4*>(a.y);
     const int N4 = d / 4;
-    const int q1 = tid < kCopyThreads ? (int)((int64_t)N4 * (c + 1) / G) : 0;
-    for (int q = (int)((int64_t)N4 * c / G) + tid; q < q1; q += kCopyThreads) y4[q] = make_float4(0.f, 0.f, 0.f, 0.f);
+    const int q1 = (int)((int64_t)N4 * (k + 1) / r);
+    for (int q = (int)((int64_t)N4 * k / r) + tid; q < q1; q += kLayerThreads) y4[q] = make_float4(0.f, 0.f, 0.f, 0.f);
     if (a.mask != nullptr) {
       const int W = (f + 31) / 32;
-      const int w1 = tid < kCopyThreads ? (int)((int64_t)W * (c + 1) / G) : 0;
-      for (int w = (int)((int64_t)W * c / G) + tid; w < w1; w += kCopyThreads) a.mask[w] = 0u;
+      const int w1 = (int)((int64_t)W * (k + 1) / r);
+      for (int w = (int)((int64_t)W * k / r) + tid; w < w1; w += kLayerThreads) a.mask[w] = 0u;
     }
   }
   // the token: loaded, or formed from the previous layer by residual + LayerNorm
   if (a.y_prev == nullptr) {
-    cp_async_wait_all();  // this thread's copies of x have landed
+    const uint4* xg = static_cast<const uint4*>(a.x);
+    for (int ch = tid; ch < NCH; ch += kLayerThreads) reinterpret_cast<uint4*>(xs)[ch] = __ldcg(xg + ch);
   } else {
     const T* xp = static_cast<const T*>(a.x);
     auto load = [&](int ch, float* v) {
@@ -297,79 +317,104 @@ __global__ void __launch_bounds__(kLayerThreads, 1) k_layer(const LayerArgs a) {
   }
 
   SFFN_TRACE(1);
-  // ---- phase 1: partial h over this block's (16-row, K-chunk) tiles of V
-  {
-    const T* V = static_cast<const T*>(a.V);
-    const int tiles = a.RG * a.KS;
-    for (int tile = c; tile < tiles; tile += G) {
-      const int rg = tile / a.KS, ks = tile - rg * a.KS;
-      const int k0 = ks * a.kc;
-      const int nch = min(a.kc, d - k0) / E;
-      const int row0 = rg * 16 + warp * 2;
-      float acc0 = 0.f, acc1 = 0.f;
-#pragma unroll 4
-      for (int ch = lane; ch < nch; ch += 32) {
-        const uint4 r0 = row0 < r ? ldg_stream(V + (size_t)row0 * d + k0 + ch * E) : make_uint4(0, 0, 0, 0);
-        const uint4 r1 = row0 + 1 < r ? ldg_stream(V + (size_t)(row0 + 1) * d + k0 + ch * E) : make_uint4(0, 0, 0, 0);
-        float xv[E], w0[E], w1[E];
-        unpack<T>(reinterpret_cast<const uint4*>(xs + k0)[ch], xv);
-        unpack<T>(r0, w0);
-        unpack<T>(r1, w1);
+  // ---- phase 1: this block's h rows, h_k = V_k . x in fp32 (each a fixed-
+  // order block reduction), published with the tag in slot k (one 128-byte
+  // line per slot, so that the polls below spread over L2).  Each slot is one
+  // release store after the whole block's writes above (the zeroed slices).
+  const uint32_t tag = s_tag;
+  unsigned long long* slots = a.h_slots;
+  __shared__ float s_hred[kLayerWarps][RB];
+  for (int j0 = 0; j0 < nh; j0 += RB) {
+    if (j0 > 0)
 #pragma unroll
-        for (int e = 0; e < E; ++e) {
-          acc0 = fmaf(w0[e], xv[e], acc0);
-          acc1 = fmaf(w1[e], xv[e], acc1);
+      for (int jj = 0; jj < RB; ++jj)
+#pragma unroll
+        for (int cq = 0; cq < CPT; ++cq) {
+          const int ch = tid + cq * kLayerThreads;
+          if (j0 + jj < nh && ch < NCH) vr[jj][cq] = ldg_stream(V4 + (size_t)(c + (j0 + jj) * G) * NCH + ch);
+        }
+    float acc[RB];
+#pragma unroll
+    for (int jj = 0; jj < RB; ++jj) {
+      float acc0 = 0.f, acc1 = 0.f;
+#pragma unroll
+      for (int cq = 0; cq < CPT; ++cq) {
+        const int ch = tid + cq * kLayerThreads;
+        if (j0 + jj < nh && ch < NCH) {
+          float w[E], xv[E];
+          unpack<T>(vr[jj][cq], w);
+          unpack<T>(reinterpret_cast<const uint4*>(xs)[ch], xv);
+#pragma unroll
+          for (int e = 0; e < E; e += 2) {
+            acc0 = fmaf(w[e], xv[e], acc0);
+            acc1 = fmaf(w[e + 1], xv[e + 1], acc1);
+          }
         }
       }
-      acc0 = warp_sum(acc0);
-      acc1 = warp_sum(acc1);
-      if (lane == 0) {
-        if (row0 < r) a.h_part[(size_t)ks * r + row0] = acc0;
-        if (row0 + 1 < r) a.h_part[(size_t)ks * r + row0 + 1] = acc1;
-      }
+      acc[jj] = warp_sum(acc0 + acc1);
+    }
+    __syncthreads();  // the previous batch's sums have been read
+    if (lane == 0)
+#pragma unroll
+      for (int jj = 0; jj < RB; ++jj) s_hred[warp][jj] = acc[jj];
+    __syncthreads();
+    if (tid < RB && j0 + tid < nh) {
+      float hk = 0.f;
+#pragma unroll
+      for (int w = 0; w < kLayerWarps; ++w) hk += s_hred[w][tid];
+      asm volatile("st.release.gpu.global.u64 [%0], %1;" ::"l"(slots + (size_t)(c + (j0 + tid) * G) * kSlotStride),
+                   "l"(((unsigned long long)tag << 32) | __float_as_uint(hk))
+                   : "memory");
     }
   }
-
-  // ---- phase 2: grid barrier (every block's h partials are in place).  The
-  // barrier thread arrives and waits while the other warps issue the copies
-  // needed after it: the owned U rows, then the hot rows.  Issued here, behind
-  // the V tiles, they do not delay the token and V loads in the request queues.
   SFFN_TRACE(2);
-  __shared__ int s_passed;
-  __shared__ uint32_t s_epoch;
-  __syncthreads();  // all h partials of this block are written
-  if (warp == kBarrierThread / 32) {
-    SFFN_TRACE_AT(12, kBarrierThread);
-    unsigned long long target = 0;
-    const bool ok = counter_barrier_warp(a.hdr, (uint32_t)G, a.wait_ns, 0x300u, &target);
-    SFFN_TRACE_AT(13, kBarrierThread);
-    if (tid == kBarrierThread) {
-      s_passed = ok ? 1 : 0;
-      s_epoch = (uint32_t)(target / (uint32_t)G);  // tags this launch's published balancing counts
-    }
-  } else {
-    const unsigned char* Ub = static_cast<const unsigned char*>(a.U);
-    if (a.u_smem) {  // owned U rows -> shared memory, 16 bytes per copy
-      for (int q = tid; q < n_own * NC; q += kCopyThreads) {
-        const int j = q / NC, ch = q - j * NC;
-        cp_async16(region + a.u_off + (size_t)j * urow_bytes + ch * 16,
-                   Ub + (size_t)(c + (size_t)j * G) * urow_bytes + ch * 16);
+
+  // ---- phase 2: every h slot of this launch: h is complete and every
+  // block's zeroed slices precede what follows.  Warp 0 polls, lane l slots
+  // l, l + 32, ..., with relaxed loads (each round's loads all in flight, a
+  // short pause between rounds), then one acquire fence.
+  bool ok = true;
+  if (warp == 0) {
+    uint32_t pending = 0;  // bit q: slot lane + 32 q not yet tagged
+    for (int q = 0; q < 32; ++q)
+      if (lane + 32 * q < r) pending |= 1u << q;
+    uint64_t t0 = 0;
+    while (true) {
+      uint32_t left = pending;
+      while (left) {
+        // up to 8 loads in flight, then their checks
+        unsigned long long v[8];
+        int qs[8];
+        int n = 0;
+        while (left && n < 8) {
+          const int q = __ffs(left) - 1;
+          left &= left - 1;
+          qs[n] = q;
+          asm volatile("ld.relaxed.gpu.global.u64 %0, [%1];"
+                       : "=l"(v[n])
+                       : "l"(slots + (size_t)(lane + 32 * q) * kSlotStride)
+                       : "memory");
+          ++n;
+        }
+        for (int m = 0; m < n; ++m)
+          if ((uint32_t)(v[m] >> 32) == tag) {
+            hs[lane + 32 * qs[m]] = __uint_as_float((uint32_t)v[m]);
+            pending &= ~(1u << qs[m]);
+          }
       }
-    } else {  // too large to stage: warm L2 with the owned rows instead
-      const int lines = (urow_bytes + 127) / 128;
-      for (int q = tid; q < n_own * lines; q += kCopyThreads) {
-        const int j = q / lines, l = q - j * lines;
-        prefetch_l2(Ub + (size_t)(c + (size_t)j * G) * urow_bytes + l * 128);
+      if (!__any_sync(0xffffffffu, pending != 0)) break;
+      if (t0 == 0) t0 = globaltimer_ns();
+      if (globaltimer_ns() - t0 > a.wait_ns) {
+        if (pending) set_status(a.hdr, kStTimeout, 0x300u);
+        ok = false;
+        break;
       }
+      __nanosleep(64);
     }
-    cp_async_commit();
+    asm volatile("fence.acq_rel.gpu;" ::: "memory");
   }
-  __syncthreads();
-  const bool passed = s_passed != 0;
-  const uint32_t bar_epoch = s_epoch;
-  // hot rows next: issued after the barrier so that its round trips do not
-  // queue behind them; they still land before the predictor has decided
-  for (int j = 0; j < n_hot; ++j) fill_hot(j);
+  const bool passed = !__syncthreads_or(!ok);
+  SFFN_TRACE_AT(13, 0);
   if (!passed) {
     cp_async_wait_all();  // nothing of this block is left in flight
     if (a.cluster > 1) {  // the other members still meet the barriers of the cluster exchange
@@ -381,23 +426,26 @@ __global__ void __launch_bounds__(kLayerThreads, 1) k_layer(const LayerArgs a) {
     }
     return;
   }
-
   SFFN_TRACE(3);
-  // ---- phase 3: h = sum of the K-chunk partials (fixed order)
-  for (int k = tid; k < r; k += kLayerThreads) {
-    float s = 0.f;
-    for (int ks = 0; ks < a.KS; ++ks) s += __ldcg(&a.h_part[(size_t)ks * r + k]);
-    hs[k] = s;
-  }
-  __syncthreads();
 
   // ---- phase 4: scores of the owned neurons.  One warp per 32-row word: lane
   // l holds 16-byte chunks l, l+32, ... of every row, rows are summed with a
   // warp all-reduce, and lane k keeps row k's score.  A compact loop: fully
   // unrolled variants of it overflow the instruction cache.
   SFFN_TRACE(4);
-  cp_async_wait_all();  // this thread's U-row copies have landed; the barrier below publishes all
-  __syncthreads();
+  // this block's U rows and biases have landed (every thread's copies)
+  if (!mbar_try_wait(ubar, 0) && !layer_wait_slow(ubar, 0, a.hdr, a.wait_ns)) ok = false;
+  if (__syncthreads_or(!ok)) {
+    cp_async_wait_all();
+    if (a.cluster > 1) {
+      const uint32_t rk = cluster_rank();
+      if (tid < a.cluster) st_peer_s32(peer_smem(&s_cnt[rk], (uint32_t)tid), 0);
+      cluster_sync_all();
+      cluster_arrive_relaxed();
+      cluster_wait();
+    }
+    return;
+  }
   SFFN_TRACE(8);
   if (a.u_smem) {
     // Lr lanes per row from shared memory (a power of two, as many as keep all
@@ -601,16 +649,6 @@ __global__ void __launch_bounds__(kLayerThreads, 1) k_layer(const LayerArgs a) {
   const int P = a.hot_stages;
   const int pre = a.balance ? min(nloc, P) : nloc;
   for (int p = hot_ok ? n_hot : 0; p < min(S, pre); ++p) fill(p % S, list[p]);
-  // Rows past the ring depth are known now but enter the ring only as stages
-  // free up, each refill a full memory round trip: ask L2 for them at once
-  // (behind the ring's own copies), so that the refills find them there.
-  if (!a.balance && a.l2_ahead)
-    for (int p = S + tid; p < nloc; p += kLayerThreads) {
-      const size_t off = (size_t)list[p] * row_bytes;
-      bulk_prefetch_l2(gup + off, row_bytes);
-      if (reglu) bulk_prefetch_l2(ggt + off, row_bytes);
-      bulk_prefetch_l2(gdn + off, row_bytes);
-    }
 
   SFFN_TRACE_VAL(19, nloc);
 
@@ -625,13 +663,13 @@ __global__ void __launch_bounds__(kLayerThreads, 1) k_layer(const LayerArgs a) {
   // capacity in block order.
   if (a.balance) {
     // publish: the list as {neuron, bias} pairs, then the count tagged with
-    // this launch's epoch (the barrier generation), released after the pairs
+    // this launch's tag, released after the pairs
     int2* pub = reinterpret_cast<int2*>(a.bal_lists) + (size_t)c * own_cap;
     for (int p = tid; p < nloc; p += kLayerThreads) pub[p] = make_int2(list[p], __float_as_int(lbias[p]));
     __syncthreads();
     if (tid == kBarrierThread) {  // its warp has no copies in flight, so the fence is short
       __threadfence();
-      const uint64_t word = ((uint64_t)bar_epoch << 32) | (uint32_t)nloc;
+      const uint64_t word = ((uint64_t)tag << 32) | (uint32_t)nloc;
       asm volatile("st.relaxed.gpu.global.u64 [%0], %1;" ::"l"(a.bal_counts + c), "l"(word) : "memory");
       SFFN_TRACE_AT(15, kBarrierThread);
     }
@@ -653,7 +691,7 @@ __global__ void __launch_bounds__(kLayerThreads, 1) k_layer(const LayerArgs a) {
 #pragma unroll
         for (int k = 0; k < kCnt; ++k) {
           const int cc = lane + 32 * k;
-          if (cc < G && (uint32_t)(v[k] >> 32) != bar_epoch) {
+          if (cc < G && (uint32_t)(v[k] >> 32) != tag) {
             all = false;
             asm volatile("ld.acquire.gpu.global.u64 %0, [%1];" : "=l"(v[k]) : "l"(a.bal_counts + cc) : "memory");
           }

@@ -177,7 +177,8 @@ bool gather_config(int dtype, int act, int d, int f, int bt, int grid, size_t sm
   return true;
 }
 
-bool layer_config(int dtype, int act, int d, int f, int r, int grid, size_t smem_optin, LayerConfig* cfg) {
+bool layer_config(int dtype, int act, int d, int f, int r, int grid, size_t smem_optin, bool balance,
+                  LayerConfig* cfg) {
   const int esize = dtype == kF32 ? 4 : 2;
   const int E = 16 / esize;
   const int cpt = round_cpt((d / E + 255) / 256);
@@ -191,10 +192,13 @@ bool layer_config(int dtype, int act, int d, int f, int r, int grid, size_t smem
   const int own_cap = (f + grid - 1) / grid;
   const int nwords = (own_cap + 31) / 32;
   if (nwords > 256 || grid > 1024) return false;
+  if (r > 32 * 32) return false;  // h slots: at most 32 per lane of the polling warp
   const size_t stage = (size_t)(act == kReglu ? 3 : 2) * d * esize;
-  // x, h, stage barriers, own biases (2), list + list biases, words, balancing scratch (3 x grid)
+  // x, h, stage barriers, own biases (2), list + list biases, words, activity
+  // flags, and the balancing scratch (3 x grid) when the launches balance
+  const size_t bal = balance ? (size_t)grid * 12 : 0;
   const size_t fixed = (size_t)d * esize + (size_t)((r + 3) & ~3) * 4 + 17 * 8 + (size_t)own_cap * 16 + nwords * 4 +
-                       (size_t)grid * 12 + (size_t)own_cap + 80;
+                       bal + (size_t)(own_cap + 15) / 16 * 16 + 80;
   const size_t reserve = 2048;  // static shared memory of the kernel
   if (smem_optin < fixed + reserve + 2 * stage) return false;
   const size_t budget = (smem_optin - fixed - reserve) / 16 * 16;
@@ -211,8 +215,9 @@ bool layer_config(int dtype, int act, int d, int f, int r, int grid, size_t smem
   const size_t u_round = (u_bytes + 15) / 16 * 16;
   cfg->u_off = cfg->u_smem ? cfg->region_bytes - u_round : 0;  // U rows sit at the end of the region
   cfg->hot_stages = (int)std::min<size_t>(4, cfg->u_smem ? cfg->u_off / stage : s);
+  cfg->balance = balance ? 1 : 0;
   cfg->smem = cfg->region_bytes + (size_t)d * esize + (size_t)((r + 3) & ~3) * 4 + (s + 1) * 8 +
-              (size_t)own_cap * 16 + nwords * 4 + (size_t)grid * 12 + (size_t)own_cap + 80;
+              (size_t)own_cap * 16 + nwords * 4 + (size_t)(own_cap + 15) / 16 * 16 + bal + 80;
   return cfg->smem + reserve <= smem_optin;
 }
 

@@ -43,6 +43,7 @@ struct sffn_layer {
 namespace {
 
 thread_local std::string g_err;
+constexpr int kMinStages2 = 4;  // ring stages a block needs for the two-blocks-per-SM layer kernel
 int64_t g_wait_ns = 1000000000LL;  // 1 s
 cudaEvent_t g_prof_start = nullptr, g_prof_stop = nullptr;  // bracket gather launches when set
 
@@ -450,9 +451,10 @@ sffn_status sffn_create_layer(const sffn_layer_desc* desc, sffn_layer_t* out) {
   }
   while (!L->gcfg_ok[bt_slot(L->max_bt)]) L->max_bt /= 2;
   // The batch-1 layer kernel runs two blocks per SM when two fit with at
-  // least four ring stages each (two copy rings per SM move more than one:
-  // OPT-6.7B layer 44.4K -> 48.9K tokens/s; with three 24 KB ReGLU stages it
-  // was slower), else one; every block waits for h values that other blocks
+  // least kMinStages2 ring stages each (two copy rings per SM move more than
+  // one: OPT-6.7B layer, six 16 KB stages, 17.9 us per layer against 19.3;
+  // Llama-7B ReGLU layer, four 24 KB stages, 19.0 us against 19.9), else one;
+  // every block waits for h values that other blocks
   // publish, so every block must be resident, which the occupancy query
   // confirms.  The balancing scratch takes shared memory only when asked for.
   {
@@ -462,7 +464,7 @@ sffn_status sffn_create_layer(const sffn_layer_desc* desc, sffn_layer_t* out) {
     const size_t half = smem_sm > 0 ? (size_t)smem_sm / 2 - 1024 - 3072 : 0;  // per-block reserve, static smem
     LayerConfig c2{};
     if (half > 0 && layer_config(d.dtype, d.act, d.d_model, d.d_ff, d.rank, 2 * L->sms, half, balance, &c2) &&
-        c2.nstages >= 4 && layer_blocks_per_sm(d.dtype, c2) >= 2) {
+        c2.nstages >= kMinStages2 && layer_blocks_per_sm(d.dtype, c2) >= 2) {
       L->lcfg = c2;
       L->layer_grid = 2 * L->sms;
       L->lcfg_ok = true;

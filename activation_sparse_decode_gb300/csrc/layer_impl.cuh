@@ -55,10 +55,20 @@ constexpr int kGroup = 2;  // neurons per block-wide reduction in the row ring
 // barrier, so that no copies of its warp are in flight when it fences.
 constexpr int kSlotStride = 16;  // launch slots: one per 128-byte line (16 words)
 constexpr int kBarrierThread = kLayerThreads - 32;
-constexpr int kMaxCluster = 8;  // blocks per cluster in the row exchange (portable limit)
 
 // The ring's stage wait once the first test has failed: kept out of line so
 // that the loop body stays small enough for the instruction cache.
+static __device__ __noinline__ bool pair_wait_slow(uint64_t* bar, WsHeader* h, uint64_t limit_ns) {
+  const uint64_t t0 = globaltimer_ns();
+  while (!mbar_try_wait_cluster(bar, 0)) {
+    if (globaltimer_ns() - t0 > limit_ns) {
+      set_status(h, kStTimeout, 0x307u);
+      return false;
+    }
+  }
+  return true;
+}
+
 static __device__ __noinline__ bool layer_wait_slow(uint64_t* bar, uint32_t parity, WsHeader* h, uint64_t limit_ns) {
   return mbar_wait(bar, parity, h, limit_ns, 0x303u);
 }
@@ -108,8 +118,9 @@ __global__ void __launch_bounds__(kLayerThreads, 1) k_layer(const LayerArgs a) {
   __shared__ float s_red[2][kLayerWarps][kGroup][2];
   __shared__ float s_warp[kLayerWarps];
   __shared__ int s_nloc;
-  __shared__ int s_cnt[kMaxCluster];  // cluster exchange: every member's active-row count
   __shared__ int s_passed;
+  __shared__ __align__(8) uint64_t s_xbar;  // pair exchange: the partner's message has landed
+  __shared__ int s_pcnt;                    // pair exchange: the partner's row count
 
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   const int G = gridDim.x, c = blockIdx.x;
@@ -137,8 +148,10 @@ __global__ void __launch_bounds__(kLayerThreads, 1) k_layer(const LayerArgs a) {
   int32_t* list = reinterpret_cast<int32_t*>(words + nwords);  // active neurons (global index) per ring position
   float* lbias = reinterpret_cast<float*>(list + own_cap);       // their biases
   uint8_t* s_act = reinterpret_cast<uint8_t*>(lbias + own_cap);  // predicted-active flag per owned row
+  // pair exchange inbox {neuron, bias bits}: 8-byte entries, so 16-byte aligned
+  int2* inbox = reinterpret_cast<int2*>((reinterpret_cast<uintptr_t>(s_act + own_cap) + 15) & ~uintptr_t(15));
   // balancing scratch, last: allocated only for launches that balance
-  int32_t* bal_cnt = reinterpret_cast<int32_t*>(s_act + ((own_cap + 15) & ~15));  // rows per block,
+  int32_t* bal_cnt = reinterpret_cast<int32_t*>(inbox + ((own_cap + 1) & ~1));  // rows per block,
   int32_t* bal_keep = bal_cnt + G;                                                // rows each block keeps,
   int32_t* bal_einc = bal_keep + G;  // inclusive prefix of given-away rows
   SFFN_TRACE(0);
@@ -177,9 +190,28 @@ __global__ void __launch_bounds__(kLayerThreads, 1) k_layer(const LayerArgs a) {
   if (tid == 0) {
     for (int s = 0; s < S; ++s) mbar_init(&bars[s], kLayerThreads);
     mbar_init(ubar, kLayerThreads);
+    if (a.cluster == 2) mbar_init(&s_xbar, 1);
     fence_mbar_init();
   }
   __syncthreads();
+  // Pair exchange barrier sequence (clusters of two; every path takes it):
+  // phase 1 arrives here and is waited before this block first writes into
+  // its partner's shared memory, so the partner's barrier is initialised;
+  // phase 2 arrives after the last such write and is waited just before the
+  // block exits, so no block leaves while its partner may still write to it.
+  if (a.cluster == 2) cluster_arrive();
+  // An early exit still sends the partner a count of zero (it does not wait
+  // for this block's rows) and passes both phases.
+  auto pair_exit_early = [&]() {
+    cluster_wait();
+    if (tid == 0) {
+      const uint32_t peer = cluster_rank() ^ 1u;
+      st_peer_s32(peer_smem(&s_pcnt, peer), 0);
+      mbar_arrive_remote(peer_smem(&s_xbar, peer));
+    }
+    cluster_arrive();
+    cluster_wait();
+  };
   const int nh = c < r ? (r - c + G - 1) / G : 0;  // h rows of this block: c, c + G, ...
   const uint4* V4 = static_cast<const uint4*>(a.V);
   // rows are reduced RB at a time (every load of a batch in flight at once);
@@ -417,13 +449,7 @@ __global__ void __launch_bounds__(kLayerThreads, 1) k_layer(const LayerArgs a) {
   SFFN_TRACE_AT(13, 0);
   if (!passed) {
     cp_async_wait_all();  // nothing of this block is left in flight
-    if (a.cluster > 1) {  // the other members still meet the barriers of the cluster exchange
-      const uint32_t rk = cluster_rank();
-      if (tid < a.cluster) st_peer_s32(peer_smem(&s_cnt[rk], (uint32_t)tid), 0);
-      cluster_sync_all();
-      cluster_arrive_relaxed();
-      cluster_wait();
-    }
+    if (a.cluster == 2) pair_exit_early();
     return;
   }
   SFFN_TRACE(3);
@@ -437,13 +463,7 @@ __global__ void __launch_bounds__(kLayerThreads, 1) k_layer(const LayerArgs a) {
   if (!mbar_try_wait(ubar, 0) && !layer_wait_slow(ubar, 0, a.hdr, a.wait_ns)) ok = false;
   if (__syncthreads_or(!ok)) {
     cp_async_wait_all();
-    if (a.cluster > 1) {
-      const uint32_t rk = cluster_rank();
-      if (tid < a.cluster) st_peer_s32(peer_smem(&s_cnt[rk], (uint32_t)tid), 0);
-      cluster_sync_all();
-      cluster_arrive_relaxed();
-      cluster_wait();
-    }
+    if (a.cluster == 2) pair_exit_early();
     return;
   }
   SFFN_TRACE(8);
@@ -536,14 +556,21 @@ __global__ void __launch_bounds__(kLayerThreads, 1) k_layer(const LayerArgs a) {
   }
   __syncthreads();
   SFFN_TRACE(9);
-  // ascending list of active owned rows: warp 0 takes one 32-row word per
-  // step, lane k holding row k's flag; a ballot forms the word and each
-  // active lane writes its row at its rank
+  // The ring's list: positions 0..n_hot-1 are the prefetched rows, active or
+  // not (an inactive one carries the bias -inf, which the activation below
+  // turns into an exact zero: it adds nothing), then the other active owned
+  // rows in ascending order.  Warp 0 takes one 32-row word per step, lane k
+  // holding row k's flag; a ballot forms the word and each active lane
+  // writes its row at its rank.
   if (warp == 0) {
-    int base = 0;
+    for (int j = lane; j < n_hot; j += 32) {
+      list[j] = c + j * G;
+      lbias[j] = s_act[j] != 0 ? ownb[j] : -INFINITY;
+    }
+    int base = n_hot;
     for (int q = 0; q < nwords; ++q) {
       const int j = q * 32 + lane;
-      const bool on = j < n_own && s_act[j] != 0;
+      const bool on = j >= n_hot && j < n_own && s_act[j] != 0;
       const uint32_t bits = __ballot_sync(0xffffffffu, on);
       if (on) {
         const int pos = base + __popc(bits & ((1u << lane) - 1u));
@@ -558,97 +585,75 @@ __global__ void __launch_bounds__(kLayerThreads, 1) k_layer(const LayerArgs a) {
   int nloc = s_nloc;
   SFFN_TRACE_VAL(11, nloc);
 
-  // ---- cluster exchange (clusters of CS blocks, CS <= 8): the active rows of
-  // a token fall unevenly on the blocks, and the block with the most sets the
-  // kernel's length.  The blocks of a cluster even out their rows before any
-  // of them starts streaming (copies in flight stretch the round trips of the
-  // exchange): every member writes its count into every member's table, and
-  // after one cluster barrier all compute the same assignment -- capacities
-  // T/CS or T/CS + 1 by rank, each block keeping its rows up to
-  // max(capacity, prefilled hot stages) -- and the rows above that, taken in
-  // rank order, fill the free capacity of the members below their share, in
-  // rank order.  A receiver reads them from the owner's shared memory, then
-  // arrives (without waiting) on a second cluster barrier, whose wait every
-  // block passes just before it exits, so that no block leaves while another
-  // may still read its shared memory.  The failure paths keep the same
-  // barrier sequence.
-  if (a.cluster > 1) {
-    const int CS = a.cluster;
-    const int rk = (int)cluster_rank();
-    if (tid < CS) st_peer_s32(peer_smem(&s_cnt[rk], (uint32_t)tid), nloc);
-    cluster_sync_all();  // every table is complete; every list is in place
-    int cnt[kMaxCluster];
-#pragma unroll
-    for (int i = 0; i < kMaxCluster; ++i) cnt[i] = i < CS ? s_cnt[i] : 0;
-    int tot = 0;
-#pragma unroll
-    for (int i = 0; i < kMaxCluster; ++i) tot += cnt[i];
-    const int base = tot / CS, extra = tot - base * CS;
-    auto keep_of = [&](int i) { return min(cnt[i], max(base + (i < extra ? 1 : 0), a.hot_stages)); };
-    // deficits of the lower ranks, this block's deficit, and the total excess
-    int e_tot = 0, d_before = 0, my_def = 0, my_keep = nloc;
-#pragma unroll
-    for (int i = 0; i < kMaxCluster; ++i) {
-      if (i < CS) {
-        const int def = max(0, base + (i < extra ? 1 : 0) - cnt[i]);
-        if (i < rk) d_before += def;
-        if (i == rk) {
-          my_def = def;
-          my_keep = keep_of(i);
-        }
-        e_tot += cnt[i] - keep_of(i);
-      }
+  // ---- pair exchange (clusters of two blocks): a token's active rows fall
+  // unevenly on the blocks, and the block with the most sets the kernel's
+  // length.  The two blocks of a cluster split their rows evenly -- T rows
+  // in all, capacities ceil(T/2) (rank 0) and floor(T/2), each keeping its
+  // own rows up to max(capacity, prefetched stages) and handing the rest,
+  // its last rows, to the other -- without waiting for each other: each
+  // block keeps at least k_safe = max(count/2, prefetched stages) rows
+  // whatever the partner has, streams those at once, and sends its count and
+  // rows [k_safe, count) into the partner's inbox (shared-memory stores, then
+  // one release-arrive on the partner's barrier).  The split is settled when
+  // the partner's message is in, from this block's own shared memory.
+  int k_safe = nloc;
+  if (a.cluster == 2) {
+    k_safe = min(nloc, max(nloc / 2, a.hot_stages));
+    cluster_wait();  // phase 1: the partner's barrier is initialised
+    const uint32_t peer = cluster_rank() ^ 1u;
+    for (int t = tid; t < nloc - k_safe; t += kLayerThreads)
+      st_peer_v2(peer_smem(inbox + t, peer), list[k_safe + t], __float_as_int(lbias[k_safe + t]));
+    __syncthreads();  // every entry is stored before the release below
+    if (tid == 0) {
+      st_peer_s32(peer_smem(&s_pcnt, peer), nloc);
+      mbar_arrive_remote(peer_smem(&s_xbar, peer));
     }
-    const int n_recv = max(0, min(d_before + my_def, e_tot) - d_before);
-    for (int t = tid; t < n_recv; t += kLayerThreads) {
-      // excess item x belongs to the member whose excess range holds it
-      const int x = d_before + t;
-      int owner = 0, pos = 0, e0 = 0;
-#pragma unroll
-      for (int i = 0; i < kMaxCluster; ++i) {
-        if (i < CS) {
-          const int k = keep_of(i), e = cnt[i] - k;
-          if (x >= e0 && x < e0 + e) {
-            owner = i;
-            pos = k + (x - e0);
-          }
-          e0 += e;
-        }
-      }
-      list[nloc + t] = ld_peer_s32(peer_smem(list + pos, (uint32_t)owner));
-      lbias[nloc + t] = ld_peer_f32(peer_smem(lbias + pos, (uint32_t)owner));
-    }
-    __syncthreads();           // the received entries are in place for every thread
-    cluster_arrive_relaxed();  // this block reads no other member's shared memory from here on
-    nloc = my_keep + n_recv;   // a receiver keeps all of its own rows (my_keep == nloc)
-    SFFN_TRACE(16);
   }
 
   // ---- phase 5: the active rows stream through a ring of S one-neuron stages,
   // consumed in groups of up to kGroup neurons per block-wide reduction.
   SFFN_TRACE(5);
-  // If the hot rows fetched in phase 0 are exactly the first list entries (the
-  // usual case) their stages already hold positions 0..n_hot-1; otherwise
-  // those copies are waited out and discarded, and each such stage is one
-  // phase ahead.  List position p uses stage p % S.
-  bool hot_ok = n_hot <= nloc;
-  for (int k = 0; k < n_hot && hot_ok; ++k) hot_ok = list[k] == c + k * G;
+  // The rows fetched in phase 0 are list positions 0..n_hot-1, in their
+  // stages already.  List position p uses stage p % S.
   bool failed = false;
-  if (!hot_ok)
-    for (int k = 0; k < n_hot; ++k) failed |= !mbar_wait(&bars[k], 0, a.hdr, a.wait_ns, 0x305u);
-  if (__syncthreads_or(failed)) {
-    cp_async_wait_all();
-    if (a.cluster > 1) cluster_wait();  // no member exits while another may read its shared memory
-    return;
-  }
   // Own rows start streaming now, up to the prefill count when the rows are
   // balanced afterwards (every block keeps at least that many of its own).
   // Rows every block keeps and streams before the balancing: only the hot
   // ones.  Traffic in flight lengthens the exchange's round trips (requests
   // queue behind it), so the exchange runs with the request queues short.
   const int P = a.hot_stages;
-  const int pre = a.balance ? min(nloc, P) : nloc;
-  for (int p = hot_ok ? n_hot : 0; p < min(S, pre); ++p) fill(p % S, list[p]);
+  const int pre = a.balance ? min(nloc, P) : k_safe;
+  for (int p = n_hot; p < min(S, pre); ++p) fill(p % S, list[p]);
+  if (a.cluster == 2) {  // settle the pair split (see the pair exchange above)
+    bool got = mbar_try_wait_cluster(&s_xbar, 0);
+    if (!got) got = pair_wait_slow(&s_xbar, a.hdr, a.wait_ns);
+    if (__syncthreads_or(!got)) {
+      cp_async_wait_all();
+      cluster_arrive();
+      cluster_wait();
+      return;
+    }
+    const int rk = (int)cluster_rank();
+    const int np = s_pcnt;
+    const int tot = nloc + np;
+    const int cap_me = rk == 0 ? (tot + 1) / 2 : tot / 2, cap_peer = tot - cap_me;
+    const int keep_peer = min(np, max(cap_peer, P));
+    if (np > keep_peer) {  // the partner's rows [keep_peer, np), from the inbox
+      const int ks_peer = min(np, max(np / 2, P));
+      for (int t = tid; t < np - keep_peer; t += kLayerThreads) {
+        const int2 e = inbox[keep_peer - ks_peer + t];
+        list[nloc + t] = e.x;
+        lbias[nloc + t] = __int_as_float(e.y);
+      }
+      nloc += np - keep_peer;
+    } else {
+      nloc = min(nloc, max(cap_me, P));
+    }
+    __syncthreads();  // the received entries are in place for every thread
+    cluster_arrive();  // phase 2: no more writes into the partner's shared memory
+    for (int p = max(n_hot, min(S, k_safe)); p < min(S, nloc); ++p) fill(p % S, list[p]);
+    SFFN_TRACE(16);
+  }
 
   SFFN_TRACE_VAL(19, nloc);
 
@@ -800,7 +805,7 @@ __global__ void __launch_bounds__(kLayerThreads, 1) k_layer(const LayerArgs a) {
   uint32_t ph0 = 0;
   for (int p0 = 0, ng = 0; p0 < nloc; p0 += ng, ++grp) {
     // the first group is the prefetched hot rows alone, so it need not wait for a cold row
-    ng = (grp == 0 && hot_ok && n_hot > 0) ? min(n_hot, ng_max) : min(ng_max, nloc - p0);
+    ng = (grp == 0 && n_hot > 0) ? min(n_hot, ng_max) : min(ng_max, nloc - p0);
     bool ok = true;
     int stg[kGroup];
     float pu[kGroup], pg[kGroup];
@@ -813,7 +818,6 @@ __global__ void __launch_bounds__(kLayerThreads, 1) k_layer(const LayerArgs a) {
         st -= S;
         ph ^= 1u;
       }
-      if (!hot_ok && st < n_hot) ph ^= 1u;  // that stage's discarded hot copy took one phase
       stg[g] = st;
       if (g < ng) {
         if (!mbar_try_wait(&bars[st], ph)) ok &= layer_wait_slow(&bars[st], ph, a.hdr, a.wait_ns);
@@ -863,8 +867,8 @@ __global__ void __launch_bounds__(kLayerThreads, 1) k_layer(const LayerArgs a) {
         u += s_red[grp & 1][w][g][0];
         if (reglu) gt += s_red[grp & 1][w][g][1];
       }
-      const float bias = g < ng ? lbias[p0 + g] : 0.f;
-      act[g] = g < ng ? (reglu ? fmaxf(gt + bias, 0.f) * u : fmaxf(u + bias, 0.f)) : 0.f;
+      const float bias = g < ng ? lbias[p0 + g] : -INFINITY;
+      act[g] = bias == -INFINITY ? 0.f : (reglu ? fmaxf(gt + bias, 0.f) * u : fmaxf(u + bias, 0.f));
     }
 #pragma unroll
     for (int g = 0; g < kGroup; ++g) {
@@ -897,7 +901,7 @@ __global__ void __launch_bounds__(kLayerThreads, 1) k_layer(const LayerArgs a) {
   }
   if (failed) {
     cp_async_wait_all();
-    if (a.cluster > 1) cluster_wait();
+    if (a.cluster == 2) cluster_wait();  // phase 2 of the pair exchange
     return;
   }
 
@@ -916,7 +920,7 @@ __global__ void __launch_bounds__(kLayerThreads, 1) k_layer(const LayerArgs a) {
     }
   }
   SFFN_TRACE(7);
-  if (a.cluster > 1) cluster_wait();  // the second barrier of the cluster exchange
+  if (a.cluster == 2) cluster_wait();  // phase 2 of the pair exchange
 }
 
 

@@ -195,10 +195,12 @@ bool layer_config(int dtype, int act, int d, int f, int r, int grid, size_t smem
   if (r > 32 * 32) return false;  // h slots: at most 32 per lane of the polling warp
   const size_t stage = (size_t)(act == kReglu ? 3 : 2) * d * esize;
   // x, h, stage barriers, own biases (2), list + list biases, words, activity
-  // flags, and the balancing scratch (3 x grid) when the launches balance
+  // flags, the pair-exchange inbox, and the balancing scratch (3 x grid) when
+  // the launches balance
   const size_t bal = balance ? (size_t)grid * 12 : 0;
+  const size_t inbox = (size_t)((own_cap + 1) & ~1) * 8 + 16;  // pair exchange entries, 16-byte aligned
   const size_t fixed = (size_t)d * esize + (size_t)((r + 3) & ~3) * 4 + 17 * 8 + (size_t)own_cap * 16 + nwords * 4 +
-                       bal + (size_t)(own_cap + 15) / 16 * 16 + 80;
+                       bal + (size_t)(own_cap + 15) / 16 * 16 + inbox + 80;
   const size_t reserve = 2048;  // static shared memory of the kernel
   if (smem_optin < fixed + reserve + 2 * stage) return false;
   const size_t budget = (smem_optin - fixed - reserve) / 16 * 16;
@@ -217,7 +219,7 @@ bool layer_config(int dtype, int act, int d, int f, int r, int grid, size_t smem
   cfg->hot_stages = (int)std::min<size_t>(4, cfg->u_smem ? cfg->u_off / stage : s);
   cfg->balance = balance ? 1 : 0;
   cfg->smem = cfg->region_bytes + (size_t)d * esize + (size_t)((r + 3) & ~3) * 4 + (s + 1) * 8 +
-              (size_t)own_cap * 16 + nwords * 4 + (size_t)(own_cap + 15) / 16 * 16 + bal + 80;
+              (size_t)own_cap * 16 + nwords * 4 + (size_t)(own_cap + 15) / 16 * 16 + inbox + bal + 80;
   return cfg->smem + reserve <= smem_optin;
 }
 

@@ -239,6 +239,38 @@ def test_row_balancing(sffn, flags, expected):
         check_token(ol, Xh[t, 0], mask_from_list(I[t, 0], N[t, 0], wl.d_ff), Y[t, 0], TOL["f16"])
 
 
+def test_shared_workspace_across_grid_sizes(sffn):
+    """Two layers whose batch-1 kernels run on different grids (two blocks
+    per SM for narrow rows, one for 48 KB rows) take turns on one workspace:
+    every launch must find its own tag however many blocks the previous
+    launch had, and give the oracle's result."""
+    specs = [dict(d_model=512, d_ff=4096, rank=64), dict(d_model=12288, d_ff=2048, rank=64)]
+    layers, ols, wls = [], [], []
+    for i, sp in enumerate(specs):
+        wl = W.tiny_workload(dtype="f16", act="relu", mean_p=0.1, name=f"shared-ws-{i}", **sp)
+        lw = W.make_layer(wl, device=DEV)
+        layers.append(sffn.Layer.from_weights(lw))
+        ols.append(oracle_layer(lw))
+        wls.append(wl)
+    ws = sffn.new_workspace(max(sffn.sffn_workspace_size(l, 1) for l in layers), DEV)
+    X = [W.make_tokens(wl, 3, device=DEV) for wl in wls]
+    outs = []
+    for t in range(3):
+        for i, layer in enumerate(layers):
+            f = layer.d_ff
+            y = torch.empty(1, specs[i]["d_model"], dtype=torch.float32, device=DEV)
+            idx = torch.empty(1, f, dtype=torch.int32, device=DEV)
+            n = torch.empty(1, dtype=torch.int32, device=DEV)
+            sffn.sffn_forward(layer, X[i][t], y, ws, idx, n)
+            outs.append((i, t, y, idx, n))
+    torch.cuda.synchronize()
+    assert sffn.sffn_read_device_status(ws) == 0
+    for i, t, y, idx, n in outs:
+        nn = int(n.item())
+        m = mask_from_list(idx[0].cpu().numpy(), nn, layers[i].d_ff)
+        check_token(ols[i], st(X[i])[t, 0], m, y[0].cpu().numpy(), TOL["f16"])
+
+
 def test_deterministic_run_to_run(sffn, c3):
     """With SFFN_FLAG_ROW_GATHER batches run the CUDA-core row gather, which
     reduces block partials in a fixed order: bit-reproducible (the

@@ -109,8 +109,12 @@ __device__ __forceinline__ void pack_store<__nv_bfloat16>(__nv_bfloat16* dst, co
   *reinterpret_cast<uint4*>(dst) = *reinterpret_cast<const uint4*>(o);
 }
 
+// The three-chunk form (d_model up to 6144 for 16-bit weights) is held to
+// two blocks per SM worth of registers: uncapped it needs 139, and the
+// OPT-13B-shaped layer then runs one block per SM, 2.4% slower.  The smaller
+// forms fit two blocks per SM uncapped; the larger ones run one.
 template <typename T, int CPT, int ACT>
-__global__ void __launch_bounds__(kLayerThreads, 1) k_layer(const LayerArgs a) {
+__global__ void __launch_bounds__(kLayerThreads, CPT == 3 ? 2 : 1) k_layer(const LayerArgs a) {
   constexpr int CPL = 4;  // up to 4 16-byte chunks of a U row per lane (rank <= 128 * elements per chunk)
   constexpr int E = Chunk<T>::N;
   constexpr int ES = sizeof(T);

@@ -492,6 +492,23 @@ sffn_status sffn_destroy_layer(sffn_layer_t layer) {
   return SFFN_OK;
 }
 
+sffn_status sffn_get_layer_info(sffn_layer_t L, sffn_layer_info* info) {
+  g_err.clear();
+  if (L == nullptr || info == nullptr) return fail(SFFN_ERR_INVALID_ARG, "layer or info is NULL");
+  sffn_layer_info o{};
+  o.fused = L->fused() ? 1 : 0;
+  if (L->lcfg_ok) {
+    o.grid = L->layer_grid;
+    o.blocks_per_sm = L->sms > 0 ? L->layer_grid / L->sms : 0;
+    o.cluster = L->layer_cluster;
+    o.ring_stages = L->lcfg.nstages;
+    o.hot_stages = L->lcfg.hot_stages;
+  }
+  if (!o.fused) o.grid = 0;
+  *info = o;
+  return SFFN_OK;
+}
+
 size_t sffn_workspace_size(sffn_layer_t L, int32_t batch) {
   if (L == nullptr || batch < 1 || batch > L->desc.max_batch) return 0;
   return layout(L, batch).total;

@@ -35,6 +35,11 @@ _i64 = ctypes.c_int64
 _sz = ctypes.c_size_t
 
 
+class sffn_layer_info(ctypes.Structure):
+    _fields_ = [("fused", _i32), ("grid", _i32), ("blocks_per_sm", _i32), ("cluster", _i32),
+                ("ring_stages", _i32), ("hot_stages", _i32)]
+
+
 class sffn_layer_desc(ctypes.Structure):
     _fields_ = [("d_model", _i32), ("d_ff", _i32), ("rank", _i32), ("max_batch", _i32),
                 ("dtype", _i32), ("act", _i32),
@@ -58,6 +63,7 @@ _c = {
     "create": _sig("sffn_create_layer", _i32, ctypes.POINTER(sffn_layer_desc), ctypes.POINTER(_vp)),
     "destroy": _sig("sffn_destroy_layer", _i32, _vp),
     "ws_size": _sig("sffn_workspace_size", _sz, _vp, _i32),
+    "layer_info": _sig("sffn_get_layer_info", _i32, _vp, ctypes.POINTER(sffn_layer_info)),
     "ws_init": _sig("sffn_workspace_init", _i32, _vp, _sz, _vp),
     "predict": _sig("sffn_predict", _i32, _vp, _vp, _i32, _vp, _vp, _vp, _sz, _vp),
     "scores": _sig("sffn_predict_scores", _i32, _vp, _vp, _i32, _vp, _vp, _sz, _vp),
@@ -80,7 +86,8 @@ _c = {
     "version": _sig("sffn_version", _i32),
 }
 
-EXPORTED = ["sffn_create_layer", "sffn_destroy_layer", "sffn_workspace_size", "sffn_workspace_init",
+EXPORTED = ["sffn_create_layer", "sffn_destroy_layer", "sffn_workspace_size", "sffn_get_layer_info",
+            "sffn_workspace_init",
             "sffn_predict", "sffn_predict_scores", "sffn_forward", "sffn_dense_forward",
             "sffn_residual_layernorm", "sffn_forward_stack", "sffn_stack_workspace_size",
             "sffn_profile_counts", "sffn_hot_first_perm", "sffn_permute_rows", "sffn_read_device_status",
@@ -161,6 +168,14 @@ def sffn_create_layer(**kw) -> Layer:
 
 def sffn_destroy_layer(layer: Layer):
     layer.close()
+
+
+def sffn_get_layer_info(layer: Layer) -> dict:
+    """How the layer's batch-1 calls run: fused kernel, grid, blocks per SM,
+    cluster size, ring stages, hot stages."""
+    info = sffn_layer_info()
+    _check(_c["layer_info"](layer.handle, ctypes.byref(info)))
+    return {k: getattr(info, k) for k, _ in sffn_layer_info._fields_}
 
 
 def sffn_workspace_size(layer: Layer, batch: int) -> int:

@@ -144,6 +144,19 @@ sffn_status sffn_destroy_layer(sffn_layer_t layer);
 /* Bytes of workspace a call with `batch` tokens needs (0 on bad arguments). */
 size_t sffn_workspace_size(sffn_layer_t layer, int32_t batch);
 
+/* How a layer's batch-1 calls run on its device, as chosen at creation (no
+ * compute; for tuning and tests).  All fields are written; on error the
+ * struct is untouched.  Errors: SFFN_ERR_INVALID_ARG for a NULL argument. */
+typedef struct {
+  int32_t fused;          /* 1: the single-launch layer kernel, 0: multi-kernel  */
+  int32_t grid;           /* its blocks (0 when not fused)                       */
+  int32_t blocks_per_sm;  /* 1 or 2                                              */
+  int32_t cluster;        /* 2: pairs of blocks even out their rows, else 0      */
+  int32_t ring_stages;    /* row stages per block                                */
+  int32_t hot_stages;     /* of which filled before the predictor has decided    */
+} sffn_layer_info;
+sffn_status sffn_get_layer_info(sffn_layer_t layer, sffn_layer_info* info);
+
 /* Zero-fills a workspace (cudaMemsetAsync on `stream`). */
 sffn_status sffn_workspace_init(void* workspace, size_t workspace_bytes, void* stream);
 

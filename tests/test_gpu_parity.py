@@ -271,6 +271,31 @@ def test_shared_workspace_across_grid_sizes(sffn):
         check_token(ols[i], st(X[i])[t, 0], m, y[0].cpu().numpy(), TOL["f16"])
 
 
+@pytest.mark.parametrize("shape,dt,act,bps", [
+    ((4096, 16384, 256), "f16", "relu", 2),    # OPT-6.7B layer: six 16 KB stages
+    ((4096, 11008, 256), "bf16", "reglu", 2),  # Llama-7B ReGLU layer: four 24 KB stages
+    ((5120, 20480, 384), "f16", "relu", 2),    # OPT-13B layer: needs the register cap
+    ((12288, 2048, 64), "f16", "relu", 1),     # 48 KB stages: one block per SM
+], ids=["opt6.7b", "llama7b-reglu", "opt13b", "wide-rows"])
+def test_batch1_launch_shape(sffn, shape, dt, act, bps):
+    """The batch-1 kernel's launch shape for the benchmarked layer shapes: a
+    register or shared-memory change that silently drops a layer to one block
+    per SM costs several percent, so it is pinned here (weights are not read)."""
+    d, f, r = shape
+    tdt = W.TORCH_DTYPES[dt]
+    e = lambda *sz: torch.empty(*sz, dtype=tdt, device=DEV)
+    b = torch.zeros(f, dtype=torch.float32, device=DEV)
+    layer = sffn.Layer(e(f, d), e(f, d), b, e(f, r), e(r, d), w_gate=e(f, d) if act == "reglu" else None)
+    info = sffn.sffn_get_layer_info(layer)
+    nsm = torch.cuda.get_device_properties(0).multi_processor_count
+    assert info["fused"] == 1
+    assert info["blocks_per_sm"] == bps, info
+    assert info["grid"] == bps * nsm
+    assert info["ring_stages"] >= 4 or bps == 1
+    assert info["cluster"] in (0, 2)
+    layer.close()
+
+
 def test_deterministic_run_to_run(sffn, c3):
     """With SFFN_FLAG_ROW_GATHER batches run the CUDA-core row gather, which
     reduces block partials in a fixed order: bit-reproducible (the

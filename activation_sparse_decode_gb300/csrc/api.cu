@@ -307,9 +307,6 @@ sffn_status run_layer(const sffn_layer* L, const void* x, const float* y_prev, v
   a.d = d.d_model;
   a.f = d.d_ff;
   a.r = d.rank;
-  a.KS = L->lcfg.KS;
-  a.kc = L->lcfg.kc;
-  a.RG = L->lcfg.RG;
   a.act = d.act;
   a.nstages = L->lcfg.nstages;
   a.u_smem = L->lcfg.u_smem;
@@ -844,9 +841,6 @@ sffn_status sffn_internal_layer_on_scratch(sffn_layer_t L, const void* x, float*
   a.d = d.d_model;
   a.f = d.d_ff;
   a.r = d.rank;
-  a.KS = L->lcfg.KS;
-  a.kc = L->lcfg.kc;
-  a.RG = L->lcfg.RG;
   a.act = d.act;
   a.nstages = L->lcfg.nstages;
   a.u_smem = L->lcfg.u_smem;

@@ -95,7 +95,7 @@ struct LayerArgs {
   uint32_t* mask;         // NULL or [ceil(f/32)] words, zeroed and set here
   WsHeader* hdr;
   uint32_t* bar_flags;    // [grid] grid-barrier release flags, 128 bytes apart
-  int d, f, r, KS, kc, RG, act, nstages, u_smem;
+  int d, f, r, act, nstages, u_smem;
   int hot_rows;           // neurons [0, hot_rows) are prefetched before the predictor decides
   int warm_rows;          // neurons [0, warm_rows): rows warmed in L2 while the predictor runs
   int hot_stages;         // ring stages free of the U rows, usable for that prefetch
@@ -109,7 +109,7 @@ struct LayerArgs {
   uint64_t wait_ns;
 };
 struct LayerConfig {
-  int cpt, act, nstages, u_smem, KS, kc, RG, hot_stages;
+  int cpt, act, nstages, u_smem, hot_stages;
   int balance;  // 1: shared memory holds the balancing scratch
   size_t region_bytes, u_off, smem;
 };

@@ -184,11 +184,6 @@ bool layer_config(int dtype, int act, int d, int f, int r, int grid, size_t smem
   const int cpt = round_cpt((d / E + 255) / 256);
   if (cpt == 0 || cpt * E > 48) return false;  // x and y accumulators live in registers
   if (r / E > 4 * 32) return false;            // at most 4 chunks of a U row per lane
-  const int rg = (r + 15) / 16;
-  const int unit = 32 * E;
-  const int ks_target = std::max(1, (grid + rg - 1) / rg);
-  int kc = (d + ks_target - 1) / ks_target;
-  kc = (kc + unit - 1) / unit * unit;
   const int own_cap = (f + grid - 1) / grid;
   const int nwords = (own_cap + 31) / 32;
   if (nwords > 256 || grid > 1024) return false;
@@ -210,9 +205,6 @@ bool layer_config(int dtype, int act, int d, int f, int r, int grid, size_t smem
   cfg->act = act;
   cfg->nstages = (int)s;
   cfg->u_smem = u_bytes <= budget ? 1 : 0;
-  cfg->RG = rg;
-  cfg->kc = kc;
-  cfg->KS = (d + kc - 1) / kc;
   cfg->region_bytes = (std::max(s * stage, cfg->u_smem ? u_bytes : 0) + 15) / 16 * 16;
   const size_t u_round = (u_bytes + 15) / 16 * 16;
   cfg->u_off = cfg->u_smem ? cfg->region_bytes - u_round : 0;  // U rows sit at the end of the region

@@ -319,6 +319,7 @@ sffn_status run_layer(const sffn_layer* L, const void* x, const float* y_prev, v
   // the balancing exchange holds at most 256 block counts
   a.balance = L->lcfg.balance && own_cap >= 8 && L->layer_grid <= 256 ? 1 : 0;
   a.cluster = a.balance == 0 ? L->layer_cluster : 0;
+  a.static_weights = (d.flags & SFFN_FLAG_STATIC_WEIGHTS) ? 1 : 0;
   int prefill = L->lcfg.hot_stages;
   if (d.expected_active > 0.f)
     prefill = std::max(prefill, std::min(L->lcfg.nstages, (int)(0.85f * d.expected_active / L->layer_grid)));
@@ -376,7 +377,7 @@ sffn_status sffn_create_layer(const sffn_layer_desc* desc, sffn_layer_t* out) {
   if (d.d_model <= 0 || d.d_ff <= 0 || d.rank <= 0)
     return fail(SFFN_ERR_INVALID_ARG, "d_model, d_ff and rank must be positive");
   if (d.max_batch < 1 || d.max_batch > 32) return fail(SFFN_ERR_INVALID_ARG, "max_batch must be in [1, 32]");
-  if (d.flags & ~(SFFN_FLAG_MULTI_KERNEL | SFFN_FLAG_BALANCE | SFFN_FLAG_ROW_GATHER))
+  if (d.flags & ~(SFFN_FLAG_MULTI_KERNEL | SFFN_FLAG_BALANCE | SFFN_FLAG_ROW_GATHER | SFFN_FLAG_STATIC_WEIGHTS))
     return fail(SFFN_ERR_INVALID_ARG, "unknown flag bits 0x%x", (unsigned)d.flags);
   const int esize = d.dtype == SFFN_F32 ? 4 : 2;
   if (((size_t)d.d_model * esize) % 16 != 0)
@@ -851,6 +852,7 @@ sffn_status sffn_internal_layer_on_scratch(sffn_layer_t L, const void* x, float*
   a.hot_stages = L->lcfg.hot_stages;
   a.balance = 0;
   a.cluster = L->layer_cluster;
+  a.static_weights = (d.flags & SFFN_FLAG_STATIC_WEIGHTS) ? 1 : 0;
   a.prefill = 0;
   a.wait_ns = (uint64_t)g_wait_ns;
   SFFN_CUDA(launch_layer(d.dtype, L->lcfg, a, L->layer_grid, s), "layer launch");

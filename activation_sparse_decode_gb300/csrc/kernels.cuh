@@ -101,6 +101,7 @@ struct LayerArgs {
   int hot_stages;         // ring stages free of the U rows, usable for that prefetch
   int balance;            // 1: even out the active rows over the blocks (second barrier)
   int cluster;            // > 1: launched in clusters of this many blocks, which even out their rows
+  int static_weights;     // 1: the weights are read before the dependency wait (never written by kernels)
   int prefill;            // own rows each block starts streaming before the balancing
   uint64_t* bal_counts;   // [grid] {epoch, active rows} per block (workspace)
   int32_t* bal_lists;     // [grid][own_cap] {neuron, bias bits} pairs per block (workspace)

@@ -183,13 +183,15 @@ __global__ void __launch_bounds__(kLayerThreads, CPT == 3 ? 2 : 1) k_layer(const
   };
 
   // ---- phase 0a: before the previous kernel on the stream has finished
-  // (programmatic dependent launch), touch only constant data and this
-  // block's own shared memory: the first V row this block reduces goes to
-  // registers, its owned U rows and biases to shared memory, its hot rows
-  // (the first owned neurons under the hot-first order, almost always
-  // active) to the first ring stages, and its other V rows and warm rows to
-  // L2.  The token, the outputs and the workspace may still be in use by
-  // that kernel.
+  // (programmatic dependent launch) the kernel touches only its own shared
+  // memory and warms L2: this block's V rows, owned U rows and biases, hot
+  // rows and warm rows are prefetched into L2.  A prefetch of a line that
+  // kernel is still writing is harmless (the later reads see its writes).
+  // The weights themselves are read here only when the layer declares them
+  // static (no kernel writes them while the layer exists): then the first V
+  // rows go to registers, the owned U rows and biases to shared memory and
+  // the hot rows to the first ring stages before the wait.  The token, the
+  // outputs and the workspace may still be in use by that kernel.
   uint64_t* ubar = bars + S;  // completes when this block's U rows and biases have landed
   if (tid == 0) {
     for (int s = 0; s < S; ++s) mbar_init(&bars[s], kLayerThreads);
@@ -218,47 +220,22 @@ __global__ void __launch_bounds__(kLayerThreads, CPT == 3 ? 2 : 1) k_layer(const
   };
   const int nh = c < r ? (r - c + G - 1) / G : 0;  // h rows of this block: c, c + G, ...
   const uint4* V4 = static_cast<const uint4*>(a.V);
-  // rows are reduced RB at a time (every load of a batch in flight at once);
-  // the first batch's chunks are loaded now
-  constexpr int RB = CPT <= 2 ? 1 : CPT <= 3 ? 2 : 4;
-  uint4 vr[RB][CPT];
-#pragma unroll
-  for (int jj = 0; jj < RB; ++jj)
-#pragma unroll
-    for (int cq = 0; cq < CPT; ++cq) {
-      const int ch = tid + cq * kLayerThreads;
-      vr[jj][cq] = jj < nh && ch < NCH ? ldg_stream(V4 + (size_t)(c + jj * G) * NCH + ch) : make_uint4(0, 0, 0, 0);
-    }
-  if (tid < nh - RB) bulk_prefetch_l2(V4 + (size_t)(c + (tid + RB) * G) * NCH, row_bytes);
-  for (int j = tid; j < n_own; j += kLayerThreads) {
-    const int i = c + j * G;
-    if (a.b != nullptr)
-      cp_async4(&ownb[j], &a.b[i]);
-    else
-      ownb[j] = 0.f;
-    cp_async4(&ownpb[j], &a.pb[i]);
-  }
   const unsigned char* Ub = static_cast<const unsigned char*>(a.U);
-  if (a.u_smem) {  // owned U rows -> shared memory, 16 bytes per copy
-    for (int q = tid; q < n_own * NC; q += kLayerThreads) {
-      const int j = q / NC, ch = q - j * NC;
-      cp_async16(region + a.u_off + (size_t)j * urow_bytes + ch * 16,
-                 Ub + (size_t)(c + (size_t)j * G) * urow_bytes + ch * 16);
+  const int n_hot = c < a.hot_rows ? min(a.hot_stages, min(n_own, (a.hot_rows - c + G - 1) / G)) : 0;
+  {
+    if (tid < nh) bulk_prefetch_l2(V4 + (size_t)(c + tid * G) * NCH, row_bytes);
+    for (int j = tid; j < n_own; j += kLayerThreads) {
+      if (a.b != nullptr) prefetch_l2(&a.b[c + j * G]);
+      prefetch_l2(&a.pb[c + j * G]);
     }
-  } else {  // too large to stage: warm L2 with the owned rows instead
     const int ulines = (urow_bytes + 127) / 128;
     for (int q = tid; q < n_own * ulines; q += kLayerThreads) {
       const int j = q / ulines, l = q - j * ulines;
       prefetch_l2(Ub + (size_t)(c + (size_t)j * G) * urow_bytes + l * 128);
     }
-  }
-  cp_async_arrive_noinc(ubar);
-  const int n_hot = c < a.hot_rows ? min(a.hot_stages, min(n_own, (a.hot_rows - c + G - 1) / G)) : 0;
-  for (int j = 0; j < n_hot; ++j) fill(j, c + j * G);
-  {
     const int nw = c < a.warm_rows ? min(n_own, (a.warm_rows - c + G - 1) / G) : 0;
     const int rlines = (row_bytes + 127) / 128;
-    for (int q = n_hot * rlines + tid; q < nw * rlines; q += kLayerThreads) {
+    for (int q = tid; q < max(n_hot, nw) * rlines; q += kLayerThreads) {
       const int j = q / rlines, l = q - j * rlines;
       const size_t off = (size_t)(c + (size_t)j * G) * row_bytes + (size_t)l * 128;
       prefetch_l2(gup + off);
@@ -266,9 +243,56 @@ __global__ void __launch_bounds__(kLayerThreads, CPT == 3 ? 2 : 1) k_layer(const
       prefetch_l2(gdn + off);
     }
   }
+  // Staging of this block's weights: the first V rows (registers, RB rows
+  // per batch, every load of a batch in flight at once), owned biases and U
+  // rows (shared memory, completing on ubar) and hot rows (the first ring
+  // stages).
+  constexpr int RB = CPT <= 2 ? 1 : CPT <= 3 ? 2 : 4;
+  uint4 vr[RB][CPT];
+  auto stage_weights = [&]() {
+#pragma unroll
+    for (int jj = 0; jj < RB; ++jj)
+#pragma unroll
+      for (int cq = 0; cq < CPT; ++cq) {
+        const int ch = tid + cq * kLayerThreads;
+        vr[jj][cq] = jj < nh && ch < NCH ? ldg_stream(V4 + (size_t)(c + jj * G) * NCH + ch) : make_uint4(0, 0, 0, 0);
+      }
+    for (int j = tid; j < n_own; j += kLayerThreads) {
+      const int i = c + j * G;
+      if (a.b != nullptr)
+        cp_async4(&ownb[j], &a.b[i]);
+      else
+        ownb[j] = 0.f;
+      cp_async4(&ownpb[j], &a.pb[i]);
+    }
+    if (a.u_smem)  // owned U rows -> shared memory, 16 bytes per copy
+      for (int q = tid; q < n_own * NC; q += kLayerThreads) {
+        const int j = q / NC, ch = q - j * NC;
+        cp_async16(region + a.u_off + (size_t)j * urow_bytes + ch * 16,
+                   Ub + (size_t)(c + (size_t)j * G) * urow_bytes + ch * 16);
+      }
+    cp_async_arrive_noinc(ubar);
+    for (int j = 0; j < n_hot; ++j) fill(j, c + j * G);
+  };
+  if (a.static_weights) stage_weights();
   grid_dependency_wait();       // the previous kernel has completed and its writes are visible
-  grid_dependents_launch();     // the next one may start its constant-data phase
+  grid_dependents_launch();     // the next one may start its phase 0a
   SFFN_TRACE(18);
+
+  // ---- the token's loads first (to registers: nothing below waits for
+  // them), then, unless staged above, this block's weights; the token
+  // reaches shared memory after all of these are issued.
+  uint4 xreg[CPT];
+  if (a.y_prev == nullptr) {
+    const uint4* xg = static_cast<const uint4*>(a.x);
+#pragma unroll
+    for (int cq = 0; cq < CPT; ++cq) {
+      const int ch = tid + cq * kLayerThreads;
+      xreg[cq] = ch < NCH ? __ldcg(xg + ch) : make_uint4(0, 0, 0, 0);
+    }
+  }
+  if (!a.static_weights) stage_weights();
+
 
   // ---- phase 0b: this launch's tag, the token, zeroed outputs.
   // Tag: every block adds one to the workspace's launch counter; the last
@@ -302,8 +326,11 @@ __global__ void __launch_bounds__(kLayerThreads, CPT == 3 ? 2 : 1) k_layer(const
   }
   // the token: loaded, or formed from the previous layer by residual + LayerNorm
   if (a.y_prev == nullptr) {
-    const uint4* xg = static_cast<const uint4*>(a.x);
-    for (int ch = tid; ch < NCH; ch += kLayerThreads) reinterpret_cast<uint4*>(xs)[ch] = __ldcg(xg + ch);
+#pragma unroll
+    for (int cq = 0; cq < CPT; ++cq) {
+      const int ch = tid + cq * kLayerThreads;
+      if (ch < NCH) reinterpret_cast<uint4*>(xs)[ch] = xreg[cq];
+    }
   } else {
     const T* xp = static_cast<const T*>(a.x);
     auto load = [&](int ch, float* v) {

@@ -50,6 +50,7 @@ class sffn_layer_desc(ctypes.Structure):
 SFFN_FLAG_MULTI_KERNEL = 1
 SFFN_FLAG_BALANCE = 2
 SFFN_FLAG_ROW_GATHER = 4
+SFFN_FLAG_STATIC_WEIGHTS = 8
 
 
 def _sig(name, res, *args):

@@ -257,7 +257,10 @@ def bench_sffn(args):
     nm = 2 if wl.act == "reglu" else 1
     d, f, r = wl.d_model, wl.d_ff, wl.rank
     W_words = (f + 31) // 32
-    flags = sffn.SFFN_FLAG_ROW_GATHER if args.row_gather else 0
+    # the layers' weights are written and synchronised before the first call
+    # and never written after: batch-1 calls may stage them before the
+    # previous kernel on the stream has finished
+    flags = (sffn.SFFN_FLAG_ROW_GATHER if args.row_gather else 0) | sffn.SFFN_FLAG_STATIC_WEIGHTS
     union_path = B >= 3 and wl.dtype != "f32" and d % 128 == 0 and not args.row_gather
 
     # ---- layers: single layers as R rotating replicas, stacks as their L layers

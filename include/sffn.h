@@ -134,6 +134,16 @@ typedef struct {
  * the CUDA-core predictor and row gather instead (passes of up to 4 tokens,
  * fixed-order reduction, bit-reproducible). */
 #define SFFN_FLAG_ROW_GATHER 4
+/* The layer's weights, biases and predictor matrices are static: no kernel
+ * writes them while the layer exists (they were written, and the writes
+ * synchronised, before the first call).  Batch-1 calls may start while the
+ * previous kernel on the stream is still finishing (programmatic dependent
+ * launch); with this flag they stage the weights they need first (V rows, U
+ * rows, biases, hot rows) before waiting for that kernel, which saves about
+ * 1 us per call on the OPT-6.7B layer.  Without it they only warm L2 with
+ * them before the wait, so a kernel queued just before the call may still be
+ * writing the weights (a reorder, a dequantisation). */
+#define SFFN_FLAG_STATIC_WEIGHTS 8
 
 /* Validates the descriptor and records it with launch settings chosen for the
  * current device.  Allocates only host memory.  Returns INVALID_ARG for bad

@@ -28,7 +28,9 @@ def sffn():
 
 # ---------------------------------------------------------------- ReLU FFN d1024 f4096 fp32 (64 tokens)
 
-PATHS = {"fused": 0, "multi": 1}  # single-launch layer kernel vs separate predictor/score/gather kernels
+# single-launch layer kernel (weights staged after / before the dependency
+# wait) vs separate predictor/score/gather kernels
+PATHS = {"fused": 0, "fused-static": 8, "multi": 1}
 
 
 @pytest.mark.parametrize("path", list(PATHS))
@@ -168,7 +170,7 @@ SMALL = [  # (d_model, d_ff, rank, dtype, act, batch); batch-1 shapes run both p
 @pytest.mark.parametrize("shape", SMALL, ids=lambda s: "d%d_f%d_r%d_%s_%s_b%d" % s)
 def test_ragged_small_layers(sffn, shape, path):
     d, f, r, dt, act, batch = shape
-    if path == "fused" and batch > 1:
+    if path.startswith("fused") and batch > 1:
         pytest.skip("the single-launch layer kernel serves batch 1")
     wl = W.tiny_workload(d_model=d, d_ff=f, rank=r, dtype=dt, act=act, mean_p=0.2, name=f"ragged{shape}")
     lw = W.make_layer(wl, device=DEV)

@@ -3,9 +3,12 @@
 //
 // Why one kernel.  At batch 1 a layer moves only tens of MB, a few microseconds
 // of HBM time, so the cost of separate launches and of their dependency gaps is
-// as large as the work.  Here every block works through all phases and the
-// only grid-wide synchronisation is a single bounded barrier between the
-// predictor's hidden layer (h = V x, split over all blocks) and its scores.
+// as large as the work.  Here every block works through all phases, and the
+// only grid-wide dependency is the predictor's hidden layer: block c reduces
+// the rows k = c, c + G, ... of h = V x over all of d and publishes each in a
+// tagged workspace slot; every block then acquires all r slots (bounded
+// polling), which also orders every block's zeroed output slices before the
+// accumulation.
 //
 // Neuron ownership.  Block c of G owns the neurons i = c, c + G, c + 2G, ...
 // It scores exactly its own neurons (their rows of U), so it learns its own
@@ -16,13 +19,14 @@
 // instead of on GPU vs CPU: PowerInfer page, "Politica de colocacion de
 // neuronas").
 //
-// Overlap.  At t = 0 each block issues bulk copies of its U rows into shared
-// memory, an L2 prefetch of the V tiles it will stream, and loads of its
-// biases, so the predictor's 2-3 weight streams are in flight together.  The
-// rows of active neurons follow the same cp.async.bulk + mbarrier ring as the
-// gather kernel.  The down projection's per-block partial output is added into
-// y with vector float atomics (y is zeroed in the first phase, before the
-// barrier), so there is no second grid-wide step.
+// Overlap.  Under programmatic dependent launch the kernel warms L2 with its
+// V rows, U rows, biases and hot rows while the previous kernel finishes; its
+// U rows and biases are staged in shared memory and its hot rows -- the first
+// owned neurons, almost always active -- in the first ring stages before the
+// predictor has decided.  The active rows stream through a ring of
+// one-neuron stages filled by per-thread 16-byte cp.async (each thread copies
+// the chunks it later reads), and the block's partial output is added into y
+// with vector float atomics, so there is no second grid-wide step.
 //
 // Stacked layers: when y_prev is given, the block first forms this layer's
 // input x = round(LayerNorm(x_prev + y_prev)) itself (every block computes the
@@ -692,8 +696,8 @@ __global__ void __launch_bounds__(kLayerThreads, CPT == 3 ? 2 : 1) k_layer(const
   // ---- balancing: each token's active rows fall unevenly on the blocks (a
   // sum of independent Bernoulli draws per block), and the block with the
   // most rows sets the kernel's length.  Every block publishes its count and
-  // list; after a second grid barrier every block computes the same
-  // assignment: the total N gives capacities K or K + 1, each block keeps its
+  // list; once it has seen every block's count of this launch, every block
+  // computes the same assignment: the total N gives capacities K or K + 1, each block keeps its
   // own rows up to max(capacity, prefill) -- its hot rows stay local -- and
   // the rows above that, in block order, fill the other blocks' free
   // capacity in block order.

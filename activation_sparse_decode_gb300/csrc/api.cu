@@ -2,6 +2,7 @@
 // sequence of the predictor-gated sparse FFN (declared in include/sffn.h).
 
 #include <algorithm>
+#include <cstddef>
 #include <cstdarg>
 #include <cstdio>
 #include <cstring>
@@ -614,9 +615,9 @@ size_t sffn_stack_workspace_size(const sffn_layer_t* layers, int32_t n_layers, i
 }
 
 sffn_status sffn_forward_stack(const sffn_layer_t* layers, int32_t n_layers, const void* x0, int32_t batch,
-                               int32_t n_steps, void* x_out, void* x_trace, const float* ln_gamma,
-                               const float* ln_beta, float ln_eps, void* workspace, size_t ws_bytes,
-                               void* stream) {
+                               int32_t n_steps, void* x_out, void* x_trace, uint32_t* mask_trace,
+                               float* y_trace, const float* ln_gamma, const float* ln_beta, float ln_eps,
+                               void* workspace, size_t ws_bytes, void* stream) {
   g_err.clear();
   if (layers == nullptr || n_layers < 1) return fail(SFFN_ERR_INVALID_ARG, "no layers");
   if (n_steps < 1) return fail(SFFN_ERR_INVALID_ARG, "n_steps must be >= 1");
@@ -629,6 +630,8 @@ sffn_status sffn_forward_stack(const sffn_layer_t* layers, int32_t n_layers, con
   SFFN_TRY(check_dev_ptr(x0, "x0"));
   SFFN_TRY(check_dev_ptr(x_out, "x_out"));
   if (x_trace != nullptr) SFFN_TRY(check_dev_ptr(x_trace, "x_trace"));
+  if (mask_trace != nullptr) SFFN_TRY(check_dev_ptr(mask_trace, "mask_trace"));
+  if (y_trace != nullptr) SFFN_TRY(check_dev_ptr(y_trace, "y_trace"));
   if (!(ln_eps >= 0.f)) return fail(SFFN_ERR_INVALID_ARG, "ln_eps must be >= 0");
   const size_t need = sffn_stack_workspace_size(layers, n_layers, batch);
   if (workspace == nullptr || ws_bytes < need || (reinterpret_cast<uintptr_t>(workspace) & 255u))
@@ -648,6 +651,19 @@ sffn_status sffn_forward_stack(const sffn_layer_t* layers, int32_t n_layers, con
   float* ybuf = ybufs[0];
   unsigned char* trace = static_cast<unsigned char*>(x_trace);
   unsigned char* xo = static_cast<unsigned char*>(x_out);
+  // traces of every layer call: mask words (Wmax per token, the widest
+  // layer's count) and outputs; a traced call writes its output in place
+  int Wmax = 0;
+  for (int l = 0; l < n_layers; ++l) Wmax = std::max(Wmax, layers[l]->W);
+  auto mask_slot = [&](int t, int l) -> uint32_t* {
+    return mask_trace == nullptr ? nullptr : mask_trace + ((size_t)t * n_layers + l) * batch * Wmax;
+  };
+  auto y_slot = [&](int t, int l) -> float* {
+    return y_trace == nullptr ? nullptr : y_trace + ((size_t)t * n_layers + l) * batch * d0.d_model;
+  };
+  if (mask_trace != nullptr)  // words past a narrower layer's count stay zero
+    SFFN_CUDA(cudaMemsetAsync(mask_trace, 0, (size_t)n_steps * n_layers * batch * Wmax * sizeof(uint32_t), s),
+              "mask trace clear");
 
   bool all_fused = batch == 1;
   for (int l = 0; l < n_layers; ++l) all_fused = all_fused && layers[l]->fused();
@@ -664,13 +680,14 @@ sffn_status sffn_forward_stack(const sffn_layer_t* layers, int32_t n_layers, con
         const sffn_layer* L = layers[l];
         Ws ws;
         SFFN_TRY(check_ws(L, batch, workspace, per, &ws));
-        float* ycur = ybufs[k & 1];
+        float* ycur = y_trace != nullptr ? y_slot(t, l) : ybufs[k & 1];
+        uint32_t* mcur = mask_slot(t, l);
         void* xin_store;  // where this layer's input lives
         if (k == 0) {
           xin_store = const_cast<void*>(x0);
           if (trace != nullptr)
             SFFN_CUDA(cudaMemcpyAsync(trace, x0, xbytes, cudaMemcpyDeviceToDevice, s), "trace copy");
-          SFFN_TRY(run_layer(L, x0, nullptr, nullptr, nullptr, nullptr, 0.f, ycur, nullptr, ws, s));
+          SFFN_TRY(run_layer(L, x0, nullptr, nullptr, nullptr, nullptr, 0.f, ycur, mcur, ws, s));
         } else {
           if (l == 0)
             xin_store = xo + (size_t)(t - 1) * xbytes;  // last step's output is this step's input
@@ -678,7 +695,7 @@ sffn_status sffn_forward_stack(const sffn_layer_t* layers, int32_t n_layers, con
             xin_store = trace + ((size_t)t * n_layers + l) * xbytes;
           else
             xin_store = xbuf[k & 1];
-          SFFN_TRY(run_layer(L, xprev, yprev, xin_store, ln_gamma, ln_beta, ln_eps, ycur, nullptr, ws, s));
+          SFFN_TRY(run_layer(L, xprev, yprev, xin_store, ln_gamma, ln_beta, ln_eps, ycur, mcur, ws, s));
           if (l == 0 && trace != nullptr)
             SFFN_CUDA(cudaMemcpyAsync(trace + (size_t)t * n_layers * xbytes, xin_store, xbytes,
                                       cudaMemcpyDeviceToDevice, s),
@@ -705,9 +722,15 @@ sffn_status sffn_forward_stack(const sffn_layer_t* layers, int32_t n_layers, con
       Ws ws;
       SFFN_TRY(check_ws(L, batch, workspace, per, &ws));
       SFFN_TRY(run_predictor(L, xin, batch, ws, nullptr, s));
-      SFFN_TRY(run_sparse_ffn(L, xin, batch, ybuf, ws, s));
+      if (mask_trace != nullptr)
+        SFFN_CUDA(cudaMemcpy2DAsync(mask_slot(t, l), (size_t)Wmax * sizeof(uint32_t), ws.mask(),
+                                    (size_t)L->W * sizeof(uint32_t), (size_t)L->W * sizeof(uint32_t), batch,
+                                    cudaMemcpyDeviceToDevice, s),
+                  "mask trace copy");
+      float* ycur = y_trace != nullptr ? y_slot(t, l) : ybuf;
+      SFFN_TRY(run_sparse_ffn(L, xin, batch, ycur, ws, s));
       void* xnext = (l == n_layers - 1) ? static_cast<void*>(xo + (size_t)t * xbytes) : xbuf[l & 1];
-      SFFN_CUDA(launch_residual_layernorm(d0.dtype, xin, ybuf, batch, d0.d_model, ln_gamma, ln_beta, ln_eps,
+      SFFN_CUDA(launch_residual_layernorm(d0.dtype, xin, ycur, batch, d0.d_model, ln_gamma, ln_beta, ln_eps,
                                           xnext, s),
                 "layernorm launch");
       xin = xnext;
@@ -823,8 +846,13 @@ sffn_status sffn_internal_layer_on_scratch(sffn_layer_t L, const void* x, float*
                 scratch_bytes);
   unsigned char* base = static_cast<unsigned char*>(scratch);
   cudaStream_t s = static_cast<cudaStream_t>(stream);
-  // the launch counter and the slots must start at zero: the array keeps whatever the last call left
-  SFFN_CUDA(cudaMemsetAsync(base, 0, need, s), "scratch clear");
+  // The launch counter, the barrier words and the slots must start at zero
+  // (the array keeps whatever the last call left, possibly mid-count after a
+  // timed-out wait); the status word and its detail (the header's first eight
+  // bytes) are kept until sffn_noalloc_read_status reads and clears them.
+  constexpr size_t kKeep = 2 * sizeof(uint32_t);
+  static_assert(offsetof(WsHeader, status) == 0 && offsetof(WsHeader, detail) == 4, "status words first");
+  SFFN_CUDA(cudaMemsetAsync(base + kKeep, 0, need - kKeep, s), "scratch clear");
   LayerArgs a{};
   a.x = x;
   a.V = d.pred_V;

@@ -72,7 +72,7 @@ _c = {
     "dense": _sig("sffn_dense_forward", _i32, _vp, _vp, _i32, _vp, _vp, _sz, _vp),
     "ln": _sig("sffn_residual_layernorm", _i32, _vp, _vp, _i32, _i32, _i32, _vp, _vp, ctypes.c_float, _vp, _vp),
     "stack": _sig("sffn_forward_stack", _i32, ctypes.POINTER(_vp), _i32, _vp, _i32, _i32, _vp, _vp, _vp, _vp,
-                  ctypes.c_float, _vp, _sz, _vp),
+                  _vp, _vp, ctypes.c_float, _vp, _sz, _vp),
     "stack_ws": _sig("sffn_stack_workspace_size", _sz, ctypes.POINTER(_vp), _i32, _i32),
     "profile": _sig("sffn_profile_counts", _i32, _vp, _vp, _i32, _vp, _vp, _sz, _vp),
     "hot_first": _sig("sffn_hot_first_perm", _i32, ctypes.POINTER(_i32), _i32, ctypes.POINTER(_i32)),
@@ -82,6 +82,7 @@ _c = {
     "wait_limit": _sig("sffn_set_wait_limit_ns", _i32, _i64),
     "prof_events": _sig("sffn_set_profile_events", _i32, _vp, _vp),
     "noalloc": _sig("sffn_forward_noalloc", _i32, _vp, _vp, _vp, _vp),
+    "noalloc_status": _sig("sffn_noalloc_read_status", _i32, ctypes.POINTER(_i32), _vp),
     "status_string": _sig("sffn_status_string", ctypes.c_char_p, _i32),
     "last_error": _sig("sffn_last_error", ctypes.c_char_p),
     "version": _sig("sffn_version", _i32),
@@ -92,8 +93,8 @@ EXPORTED = ["sffn_create_layer", "sffn_destroy_layer", "sffn_workspace_size", "s
             "sffn_predict", "sffn_predict_scores", "sffn_forward", "sffn_dense_forward",
             "sffn_residual_layernorm", "sffn_forward_stack", "sffn_stack_workspace_size",
             "sffn_profile_counts", "sffn_hot_first_perm", "sffn_permute_rows", "sffn_read_device_status",
-            "sffn_debug_wait_timeout", "sffn_set_wait_limit_ns", "sffn_set_profile_events", "sffn_forward_noalloc", "sffn_status_string", "sffn_last_error",
-            "sffn_version"]
+            "sffn_debug_wait_timeout", "sffn_set_wait_limit_ns", "sffn_set_profile_events", "sffn_forward_noalloc", "sffn_noalloc_read_status",
+            "sffn_status_string", "sffn_last_error", "sffn_version"]
 
 
 class SffnError(RuntimeError):
@@ -214,6 +215,14 @@ def sffn_forward_noalloc(layer: Layer, x: torch.Tensor, y: torch.Tensor, stream=
     _check(_c["noalloc"](layer.handle, _ptr(x), _ptr(y), _stream(stream)))
 
 
+def sffn_noalloc_read_status(stream=None) -> int:
+    """First device-side error of sffn_forward_noalloc calls on the current
+    device since the last read (0 if none); reading clears it."""
+    st = ctypes.c_int32(0)
+    _check(_c["noalloc_status"](ctypes.byref(st), _stream(stream)))
+    return st.value
+
+
 def sffn_dense_forward(layer: Layer, x: torch.Tensor, y: torch.Tensor, ws: torch.Tensor, stream=None):
     _check(_c["dense"](layer.handle, _ptr(x), x.shape[0], _ptr(y), _ptr(ws), ws.numel(), _stream(stream)))
 
@@ -234,9 +243,11 @@ def sffn_stack_workspace_size(layers: Sequence[Layer], batch: int) -> int:
 
 
 def sffn_forward_stack(layers: Sequence[Layer], x0: torch.Tensor, n_steps: int, x_out: torch.Tensor,
-                       ws: torch.Tensor, x_trace=None, gamma=None, beta=None, eps: float = 1e-5, stream=None):
+                       ws: torch.Tensor, x_trace=None, gamma=None, beta=None, eps: float = 1e-5, stream=None,
+                       mask_trace=None, y_trace=None):
     _check(_c["stack"](_handles(layers), len(layers), _ptr(x0), x0.shape[0], n_steps, _ptr(x_out),
-                       _ptr(x_trace), _ptr(gamma), _ptr(beta), eps, _ptr(ws), ws.numel(), _stream(stream)))
+                       _ptr(x_trace), _ptr(mask_trace), _ptr(y_trace), _ptr(gamma), _ptr(beta), eps, _ptr(ws),
+                       ws.numel(), _stream(stream)))
 
 
 def sffn_profile_counts(layer: Layer, X: torch.Tensor, counts: torch.Tensor, ws: torch.Tensor, stream=None):

@@ -190,17 +190,30 @@ sffn_status sffn_predict(sffn_layer_t layer, const void* x, int32_t batch, int32
  * y ([d_model] float32, device); the kernel's scratch is a fixed 256 KiB array
  * inside the library, held on every device that loads the library until the
  * process exits.  Nothing here calls cudaMalloc or cudaFree.
- *   - Layers needing more scratch than that (header + 128 bytes per SM + the
- *     predictor's split-K partial sums) are rejected with SFFN_ERR_UNSUPPORTED
- *     and a message giving both sizes; so are layers created with
+ *   - Layers needing more scratch than that (a 256-byte header, 128 bytes per
+ *     block of the single-launch kernel for its barrier words, and 128 bytes
+ *     per predictor rank row for the tagged slots through which the blocks
+ *     share the hidden layer h) are rejected with SFFN_ERR_UNSUPPORTED and a
+ *     message giving both sizes; so are layers created with
  *     SFFN_FLAG_MULTI_KERNEL or outside the single-launch kernel's limits.
- *   - The layer's device must be current.  The first call on a device looks up
- *     the array's device address there (cudaGetSymbolAddress); make that first
- *     call before any stream capture.
- *   - Every call shares the one array and clears its barrier words first, so
- *     calls that overlap on the GPU (other streams, other threads) race; order
- *     them.  Device-side wait timeouts are not reported by this entry point. */
+ *   - The layer's device must be current.  Every call looks up the array's
+ *     device address there (cudaGetSymbolAddress); the first lookup on a
+ *     device loads the library's kernels, so make the first call on each
+ *     device before any stream capture.
+ *   - Every call shares the one array and clears its counters first, so calls
+ *     that overlap on the GPU (other streams, other threads) race; order them.
+ *   - A device-side wait that ran out (SFFN_ERR_TIMEOUT: the kernel needs all
+ *     its blocks resident at once, which kernels of other streams holding SMs
+ *     can prevent; y is then incomplete) is recorded in the array's status
+ *     word, which later calls keep; read and clear it with
+ *     sffn_noalloc_read_status. */
 sffn_status sffn_forward_noalloc(sffn_layer_t layer, const void* x, float* y, void* stream);
+
+/* Status word of sffn_forward_noalloc's fixed array on the current device:
+ * synchronises `stream`, copies the first device-side error since the last
+ * read to *status (an sffn_status value, SFFN_OK if none) and clears it.
+ * No counterpart in the paper; allocates nothing. */
+sffn_status sffn_noalloc_read_status(int32_t* status, void* stream);
 
 /* Predictor scores s = U (V x) + pb as float32 [batch][d_ff] (diagnostics:
  * the same kernels as sffn_predict, scores written out). */
@@ -235,15 +248,26 @@ sffn_status sffn_residual_layernorm(const void* x, const float* y, int32_t batch
  * every step runs each layer's sparse FFN followed by residual + LayerNorm,
  * x_{l+1} = round(LN(x_l + y_l)), and the next step starts from the last
  * layer's output.
- *   x0      : [batch][d_model] dtype, first step's input
- *   x_out   : [n_steps][batch][d_model] dtype, last layer's output per step
- *   x_trace : NULL or [n_steps][n_layers][batch][d_model] dtype, the input of
- *             every layer at every step
- *   ln_gamma, ln_beta : NULL or [d_model] float32 shared by all layers */
+ *   x0         : [batch][d_model] dtype, first step's input
+ *   x_out      : [n_steps][batch][d_model] dtype, last layer's output per step
+ *   x_trace    : NULL or [n_steps][n_layers][batch][d_model] dtype, the input
+ *                of every layer at every step
+ *   mask_trace : NULL or [n_steps][n_layers][batch][Wmax] uint32, the mask
+ *                words each layer call used (bit i%32 of word i/32: neuron i
+ *                predicted active), Wmax = ceil(largest d_ff / 32); words past
+ *                a narrower layer's ceil(d_ff/32) are zero
+ *   y_trace    : NULL or [n_steps][n_layers][batch][d_model] float32, each
+ *                layer call's sparse-FFN output (the y that the residual +
+ *                LayerNorm consumed)
+ *   ln_gamma, ln_beta : NULL or [d_model] float32 shared by all layers
+ * The traces record what this run computed (not a recomputation), for checks
+ * of every layer of a long decode; they cost extra writes and are meant for
+ * tests and diagnostics. */
 sffn_status sffn_forward_stack(const sffn_layer_t* layers, int32_t n_layers, const void* x0,
                                int32_t batch, int32_t n_steps, void* x_out, void* x_trace,
-                               const float* ln_gamma, const float* ln_beta, float ln_eps,
-                               void* workspace, size_t workspace_bytes, void* stream);
+                               uint32_t* mask_trace, float* y_trace, const float* ln_gamma,
+                               const float* ln_beta, float ln_eps, void* workspace,
+                               size_t workspace_bytes, void* stream);
 size_t sffn_stack_workspace_size(const sffn_layer_t* layers, int32_t n_layers, int32_t batch);
 
 /* Offline profile pass (hot/cold classification by activation frequency):

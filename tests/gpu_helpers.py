@@ -6,7 +6,9 @@ Comparison rules (readings of the problem statement):
   whose oracle score lies within 1e-4 of tau (the band), which are counted;
 * the output is compared with the oracle's masked FFN over the GPU's own mask,
   so a band neuron decided differently does not count as an output error;
-* relative L2 error <= 1e-5 for fp32 weights, <= 1e-3 for fp16/bf16 weights.
+* relative L2 error <= 1e-5 for fp32 weights, <= 1e-3 for fp16/bf16 weights;
+* and element by element (ELEM_EPS below): the L2 bar alone cannot see one
+  wrong element, e.g. one neuron's contribution added twice or dropped.
 """
 
 import numpy as np
@@ -18,6 +20,53 @@ from activation_sparse_decode_gb300.workloads import to_numpy_stored as st
 
 BAND = 1e-4
 TOL = {"f32": 1e-5, "f16": 1e-3, "bf16": 1e-3}
+
+# Element-wise bound: |y_gpu[j] - y_oracle[j]| <= ELEM_EPS * (|y_oracle[j]| + rms(y_oracle)).
+# Derivation.  The GPU sums in fp32 (unit roundoff u = 2^-24), in tree orders:
+# each output element is a sum of n neuron terms a_i W[i, j] (n = active
+# neurons, 400-13000 here) whose a_i are themselves fp32 dot products over
+# d_model; for random-sign terms the rounding error grows like u * sqrt(terms)
+# times the partial sums, about 1e-6 of rms(y) for the widest layer.  The
+# batch tensor-core path feeds a_i to the second product as a 16-bit high part
+# plus a 16-bit remainder (relative error <= 2^-17 per term for bf16), and the
+# tensor cores' fp32 accumulation may truncate (2u per step); together about
+# 1e-4 of rms(y) at most.  ELEM_EPS is 2^-10 ~ 1e-3 (2^-16 for fp32 weights,
+# which never take the 16-bit split): ten times that estimate, while one
+# neuron's term a_i W[i, j] is about rms(y) / sqrt(n) >= 0.009 rms(y) for every
+# workload here, so a single misplaced term on one element still fails.
+ELEM_EPS = {"f32": 2.0 ** -16, "f16": 2.0 ** -10, "bf16": 2.0 ** -10}
+
+
+def elementwise_ratio(y_gpu, y_ref, fmt):
+    """max over j of |y_gpu[j] - y_ref[j]| / (ELEM_EPS * (|y_ref[j]| + rms(y_ref))); <= 1 passes."""
+    g, r = np.asarray(y_gpu, np.float64), np.asarray(y_ref, np.float64)
+    scale = np.abs(r) + np.sqrt(np.mean(r * r))
+    err = np.abs(g - r)
+    if not np.any(scale > 0):
+        return 0.0 if not np.any(err > 0) else np.inf
+    return float(np.max(err / (ELEM_EPS[fmt] * scale)))
+
+
+def check_elementwise(y_gpu, y_ref, fmt, what="y"):
+    ratio = elementwise_ratio(y_gpu, y_ref, fmt)
+    if ratio > 1.0:
+        g, r = np.asarray(y_gpu, np.float64), np.asarray(y_ref, np.float64)
+        j = int(np.argmax(np.abs(g - r) / (np.abs(r) + np.sqrt(np.mean(r * r)) + 1e-300)))
+        raise AssertionError(f"{what}: element {j} off by {abs(g[j] - r[j]):.3e} (gpu {g[j]:.6e}, oracle {r[j]:.6e}); "
+                             f"{ratio:.2f} x the element-wise bound")
+    return ratio
+
+
+def ulp_distance(a, b, fmt):
+    """Number of representable values of the stored format between a and b
+    (stored bits: float32 / float16 arrays, bf16 as uint16 patterns)."""
+    def ordered(v):
+        if fmt == "f32":
+            i = np.asarray(v, np.float32).view(np.int32).astype(np.int64)
+            return np.where(i < 0, -(i & 0x7FFFFFFF), i)
+        bits = (np.asarray(v, np.float16).view(np.uint16) if fmt == "f16" else np.asarray(v, np.uint16)).astype(np.int64)
+        return np.where(bits & 0x8000, -(bits & 0x7FFF), bits)
+    return np.abs(ordered(a) - ordered(b))
 
 
 def rel_l2(a, b):
@@ -65,6 +114,7 @@ def check_token(ol, x_stored, gpu_mask, y_gpu, tol, tau=0.0):
     ref = oracle.masked_ffn(ol, x_stored, gpu_mask)
     r = rel_l2(y_gpu, ref)
     assert r <= tol, f"rel-L2 {r:.3e} > {tol:g}"
+    check_elementwise(y_gpu, ref, ol.fmt)
     return int(band.sum()), int(((mo != gpu_mask) & band).sum()), r
 
 
@@ -89,14 +139,15 @@ def lazy_oracle_layer(lw, tau=0.0):
         w_gate=None if lw.w_gate is None else DeviceRows(lw.w_gate), tau=tau)
 
 
-def check_next_input(x_next_gpu, x_next_oracle, fmt):
-    """Stored next-layer inputs: equal up to one rounding step of the format on
-    a small fraction of elements (fp32 vs fp64 LayerNorm before rounding)."""
-    g, o = oracle.decode(x_next_gpu, fmt), oracle.decode(x_next_oracle, fmt)
-    ulp = {"f32": 2.0 ** -23, "f16": 2.0 ** -10, "bf16": 2.0 ** -7}[fmt]
-    err = np.abs(g - o) / np.maximum(np.abs(o), 2.0 ** -6)
-    assert err.max() <= 1.01 * ulp + 1e-5, err.max()
-    assert (g != o).mean() < 0.05
+def check_next_input(x_next_gpu, x_next_oracle, fmt, max_frac=0.05):
+    """Stored next-layer inputs: equal up to one rounding step of the format
+    (ulp distance <= 1) on a small fraction of elements.  Where the oracle's
+    value was formed from the GPU's own y, only fp32 against fp64 LayerNorm
+    arithmetic separates the two (a few 2^-24 relative before rounding to a
+    2^-11 or 2^-8 half-step), so callers pass a smaller fraction then."""
+    dist = ulp_distance(x_next_gpu, x_next_oracle, fmt)
+    assert dist.max() <= 1, f"next input: element {int(np.argmax(dist))} is {int(dist.max())} ulps off"
+    assert (dist > 0).mean() < max_frac, (dist > 0).mean()
 
 
 def run_tokens(sffn, layer, X, want_idx=True, device="cuda"):

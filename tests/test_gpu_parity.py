@@ -9,7 +9,7 @@ import torch
 import oracle
 from activation_sparse_decode_gb300 import workloads as W
 from activation_sparse_decode_gb300.workloads import to_numpy_stored as st
-from gpu_helpers import TOL, check_token, hot_first, mask_from_list, oracle_layer, rel_l2, run_tokens
+from gpu_helpers import TOL, check_elementwise, check_token, hot_first, mask_from_list, oracle_layer, rel_l2, run_tokens, ulp_distance
 
 pytestmark = pytest.mark.gpu
 
@@ -148,7 +148,9 @@ def test_dense_forward_matches_oracle(sffn, c3):
     Y = Y.cpu().numpy()
     Xh = st(X)
     for b in range(4):
-        assert rel_l2(Y[b], oracle.dense_ffn(ol, Xh[b])) < TOL[wl.dtype]
+        ref = oracle.dense_ffn(ol, Xh[b])
+        assert rel_l2(Y[b], ref) < TOL[wl.dtype]
+        check_elementwise(Y[b], ref, wl.dtype)
 
 
 SMALL = [  # (d_model, d_ff, rank, dtype, act, batch); batch-1 shapes run both paths
@@ -202,7 +204,9 @@ def test_all_false_and_all_true_masks(sffn, tau, expect, batch):
         Xh = st(X)
         for s in range(2):
             for b in range(batch):
-                assert rel_l2(Y[s, b], oracle.dense_ffn(ol, Xh[s, b])) < TOL["f16"]
+                ref = oracle.dense_ffn(ol, Xh[s, b])
+                assert rel_l2(Y[s, b], ref) < TOL["f16"]
+                check_elementwise(Y[s, b], ref, "f16")
 
 
 @pytest.mark.parametrize("hot_rows,warm_rows", [(0, 0), (10, 0), (100, 0), (1500, 0), (0, 700), (100, 1500)])
@@ -329,14 +333,22 @@ def test_residual_layernorm(sffn, dt):
                                          None if bt is None else bt.cpu().numpy(), 1e-5)
         got_v, want_v = oracle.decode(st(out), dt), oracle.decode(want, dt)
         if dt == "f32":
-            # fp32 arithmetic on O(1) normalised values: absolute error ~1e-7
-            assert np.abs(got_v - want_v).max() <= 1e-5
+            # fp32 arithmetic (u = 2^-24): the residual add and the scaling by
+            # rstd, gamma and beta each round relative to the output (~5u|out|
+            # with rstd's own few u); the mean and variance come from block
+            # sums whose error, carried through (v - mean) * rstd, is an
+            # absolute few u on O(1) values.  So |error| <= 16 u (|out| + 1),
+            # which is ~1e-6 where the output is O(1) and ~6e-8 near zero.
+            bound = 16 * 2.0 ** -24 * (np.abs(want_v) + 1.0)
+            assert np.all(np.abs(got_v - want_v) <= bound), np.max(np.abs(got_v - want_v) / bound)
         else:
-            # one rounding step of the stored format at most, on few elements
-            ulp = {"f16": 2.0 ** -10, "bf16": 2.0 ** -7}[dt]
-            err = np.abs(got_v - want_v) / np.maximum(np.abs(want_v), 2.0 ** -6)
-            assert err.max() <= 1.01 * ulp + 1e-5
-            assert (got_v != want_v).mean() < 0.05
+            # the fp32 value lies within ~1e-6 relative of the fp64 one, so the
+            # two round to the same stored value except next to a rounding
+            # midpoint (half-steps 2^-11 for fp16, 2^-8 for bf16): at most
+            # one format ulp apart, on a small fraction of the elements
+            dist = ulp_distance(st(out), want, dt)
+            assert dist.max() <= 1
+            assert (dist > 0).mean() < 0.01
     # in place
     x2 = x.clone()
     sffn.sffn_residual_layernorm(x2, y, x2)

@@ -2,9 +2,14 @@
 OPT-175B-shaped FFN decode with residual + LayerNorm between layers.
 
 Mask flips inside the band compound over many layers and steps, so parity is
-checked teacher-forced per layer: for sampled (step, layer) pairs the oracle
-takes the GPU's own layer input x_l, and its mask, output and next input
-round(LN(x_l + y_l)) are compared with the GPU's."""
+checked teacher-forced per layer, on what the stack run itself recorded (its
+layer inputs, mask words and outputs, traced by sffn_forward_stack):
+* sampled (step, layer) calls against the oracle: the run's mask outside the
+  band, its y over that mask (rel-L2 and element by element) and the next
+  input it formed, round(LN(x_l + y_l)), from that y;
+* every layer call of the checked steps against a rerun of the same call on
+  the same input: identical mask words, y equal up to the order of float
+  atomic adds -- a race inside the run would show as a difference here."""
 
 import numpy as np
 import pytest
@@ -45,34 +50,87 @@ def build_stack(sffn, wl, n_layers, max_batch):
 
 
 def run_stack(sffn, layers, x0, n_steps):
+    """One traced stack run: per (step, layer) the input, the mask words and
+    the output that this run itself used."""
     B, d = x0.shape
     L = len(layers)
+    Wmax = max((l.d_ff + 31) // 32 for l in layers)
     ws = sffn.new_workspace(sffn.sffn_stack_workspace_size(layers, B), DEV)
     x_out = torch.empty(n_steps, B, d, dtype=x0.dtype, device=DEV)
     trace = torch.empty(n_steps, L, B, d, dtype=x0.dtype, device=DEV)
-    sffn.sffn_forward_stack(layers, x0, n_steps, x_out, ws, x_trace=trace)
+    masks = torch.empty(n_steps, L, B, Wmax, dtype=torch.int32, device=DEV)
+    ys = torch.empty(n_steps, L, B, d, dtype=torch.float32, device=DEV)
+    sffn.sffn_forward_stack(layers, x0, n_steps, x_out, ws, x_trace=trace, mask_trace=masks, y_trace=ys)
     torch.cuda.synchronize()
     assert sffn.sffn_read_device_status(ws) == 0
-    return x_out, trace
+    return x_out, trace, masks, ys
 
 
-def teacher_forced(sffn, wl, lws, layers, x_out, trace, pairs, tokens):
-    B = trace.shape[2]
+def words_to_mask(words, f):
+    """Mask words (int32 view of uint32) -> bool [f]: bit i%32 of word i/32."""
+    w = np.asarray(words).astype(np.int64) & 0xFFFFFFFF
+    bits = (w[:, None] >> np.arange(32)) & 1
+    return bits.reshape(-1)[:f].astype(bool)
+
+
+# Two runs of the same layer call differ only in the order of their float
+# atomic adds: |y1 - y2| <= ATOMIC_EPS * (|y| + rms(y)) element by element
+# (about 150 block partials per element: at most ~1e-4 of rms(y) in the worst
+# order, ~1e-6 typically; one neuron's term is >= ~0.009 rms(y)).
+ATOMIC_EPS = 2.0 ** -12
+
+
+def same_call(y1, y2):
+    y1, y2 = np.asarray(y1, np.float64), np.asarray(y2, np.float64)
+    scale = np.abs(y2) + np.sqrt(np.mean(y2 * y2))
+    return bool(np.all(np.abs(y1 - y2) <= ATOMIC_EPS * scale))
+
+
+def recompute_all(sffn, layers, trace, masks, ys, wl):
+    """Every (step, layer) call of the stack run re-run alone on its own
+    recorded input: the mask words must be identical (the predictor is
+    deterministic) and the output equal up to the order of atomic adds."""
+    n_steps, L, B, d = trace.shape
     ws = sffn.new_workspace(sffn.sffn_workspace_size(layers[0], B), DEV)
+    idx = torch.empty(B, wl.d_ff, dtype=torch.int32, device=DEV)
+    n = torch.empty(B, dtype=torch.int32, device=DEV)
+    y = torch.empty(B, d, dtype=torch.float32, device=DEV)
+    bad = []
+    for t in range(n_steps):
+        for l in range(L):
+            sffn.sffn_forward(layers[l], trace[t, l].contiguous(), y, ws, idx, n)
+            ih, nh, yh = idx.cpu().numpy(), n.cpu().numpy(), y.cpu().numpy()
+            mw = masks[t, l].cpu().numpy()
+            ys_h = ys[t, l].cpu().numpy()
+            for b in range(B):
+                m_run = words_to_mask(mw[b], wl.d_ff)
+                m_re = mask_from_list(ih[b], nh[b], wl.d_ff)
+                if not np.array_equal(m_run, m_re):
+                    bad.append((t, l, b, "mask", np.flatnonzero(m_run != m_re)[:8].tolist()))
+                elif not same_call(ys_h[b], yh[b]):
+                    j = int(np.argmax(np.abs(ys_h[b] - yh[b])))
+                    bad.append((t, l, b, "y", j, float(ys_h[b][j]), float(yh[b][j])))
+    assert sffn.sffn_read_device_status(ws) == 0
+    assert not bad, f"{len(bad)} layer calls of the stack run differ from a rerun: {bad[:4]}"
+
+
+def teacher_forced(sffn, wl, lws, layers, x_out, trace, masks, ys, pairs, tokens):
+    """Sampled (step, layer) calls against the oracle, from the stack run's own
+    records: the mask it used (outside the band), its y over that mask (rel-L2
+    and element-wise), and the next input it formed, round(LN(x_l + y_l)) from
+    its own y (one format ulp on under 1% of the elements)."""
     for t, l in pairs:
         ol = lazy_oracle_layer(lws[l], wl.tau)
-        x_l = trace[t, l].contiguous()
-        idx = torch.empty(B, wl.d_ff, dtype=torch.int32, device=DEV)
-        n = torch.empty(B, dtype=torch.int32, device=DEV)
-        y = torch.empty(B, wl.d_model, dtype=torch.float32, device=DEV)
-        sffn.sffn_forward(layers[l], x_l, y, ws, idx, n)
+        xh = st(trace[t, l])
         nxt = trace[t, l + 1] if l + 1 < len(layers) else x_out[t]
-        xh, yh, ih, nh, nh_next = st(x_l), y.cpu().numpy(), idx.cpu().numpy(), n.cpu().numpy(), st(nxt)
+        nh_next = st(nxt)
+        mw = masks[t, l].cpu().numpy()
+        yh = ys[t, l].cpu().numpy()
         for b in tokens:
-            m = mask_from_list(ih[b], nh[b], wl.d_ff)
+            m = words_to_mask(mw[b], wl.d_ff)
             check_token(ol, xh[b], m, yh[b], TOL[wl.dtype], wl.tau)
-            want = oracle.residual_layernorm(xh[b], oracle.masked_ffn(ol, xh[b], m), wl.dtype)
-            check_next_input(nh_next[b], want, wl.dtype)
+            want = oracle.residual_layernorm(xh[b], yh[b].astype(np.float64), wl.dtype)
+            check_next_input(nh_next[b], want, wl.dtype, max_frac=0.01)
 
 
 @pytest.mark.parametrize("flags", [0, 1, 2], ids=["fused", "multi", "fused-balanced"])
@@ -81,25 +139,28 @@ def test_small_stack_both_paths(sffn, flags):
     lws = [W.make_layer(wl, layer=l, device=DEV) for l in range(3)]
     layers = [sffn.Layer.from_weights(lw, max_batch=1, flags=flags) for lw in lws]
     x0 = W.make_tokens(wl, 1, device=DEV)[0]
-    x_out, trace = run_stack(sffn, layers, x0, 4)
+    x_out, trace, masks, ys = run_stack(sffn, layers, x0, 4)
     assert torch.equal(trace[0, 0], x0)
     for t in range(1, 4):
         assert torch.equal(trace[t, 0], x_out[t - 1])
     pairs = [(t, l) for t in range(4) for l in range(3)]
-    teacher_forced(sffn, wl, lws, layers, x_out, trace, pairs, [0])
+    teacher_forced(sffn, wl, lws, layers, x_out, trace, masks, ys, pairs, [0])
+    recompute_all(sffn, layers, trace, masks, ys, wl)
 
 
 def test_opt13b_stack40_fp16(sffn):
     wl = W.get_workload("c4")
     lws, layers = build_stack(sffn, wl, wl.n_layers, 1)
     x0 = W.make_tokens(wl, 1, device=DEV)[0]
-    x_out, trace = run_stack(sffn, layers, x0, wl.steps)
+    x_out, trace, masks, ys = run_stack(sffn, layers, x0, wl.steps)
     assert torch.equal(trace[0, 0], x0)
     assert torch.equal(trace[1, 0], x_out[0])
     rng = np.random.Generator(np.random.PCG64(4))
     pairs = [(0, 0), (0, wl.n_layers - 1), (wl.steps - 1, wl.n_layers - 1)] + \
         [(int(rng.integers(wl.steps)), int(rng.integers(wl.n_layers))) for _ in range(3)]
-    teacher_forced(sffn, wl, lws, layers, x_out, trace, pairs, [0])
+    teacher_forced(sffn, wl, lws, layers, x_out, trace, masks, ys, pairs, [0])
+    # every layer of the first two steps, against a rerun of the same call
+    recompute_all(sffn, layers, trace[:2], masks[:2], ys[:2], wl)
     xs = x_out.float()
     assert torch.isfinite(xs).all()
     assert abs(xs.var(-1).mean().item() - 1.0) < 0.01
@@ -113,9 +174,10 @@ def test_opt175b_stack48_fp16(sffn, batch):
         test_opt175b_stack48_fp16._stack = build_stack(sffn, wl, wl.n_layers, 8)
     lws, layers = test_opt175b_stack48_fp16._stack
     x0 = W.make_tokens(wl, 1, batch=batch, device=DEV)[0]
-    x_out, trace = run_stack(sffn, layers, x0, steps)
+    x_out, trace, masks, ys = run_stack(sffn, layers, x0, steps)
     pairs = [(0, 0), (1, wl.n_layers - 1), (1, 17)]
-    teacher_forced(sffn, wl, lws, layers, x_out, trace, pairs, [0] if batch == 1 else [0, batch - 1])
+    teacher_forced(sffn, wl, lws, layers, x_out, trace, masks, ys, pairs, [0] if batch == 1 else [0, batch - 1])
+    recompute_all(sffn, layers, trace, masks, ys, wl)
     if batch == 8:
         del test_opt175b_stack48_fp16._stack
         torch.cuda.empty_cache()

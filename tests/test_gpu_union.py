@@ -10,7 +10,7 @@ import torch
 import oracle
 from activation_sparse_decode_gb300 import workloads as W
 from activation_sparse_decode_gb300.workloads import to_numpy_stored as st
-from gpu_helpers import TOL, check_token, mask_from_list, oracle_layer, rel_l2, run_tokens
+from gpu_helpers import TOL, check_elementwise, check_token, mask_from_list, oracle_layer, rel_l2, run_tokens
 
 pytestmark = pytest.mark.gpu
 
@@ -60,7 +60,9 @@ def test_union_ragged(sffn, shape):
             # (sqrt(d) * 2^-24 for the sums, 2^-17 for the bf16 split), far
             # inside the 1e-3 bar.
             assert r < 1e-4
-            assert rel_l2(Yg[s, b], oracle.masked_ffn(ol, Xh[s, b], m)) < 1e-4
+            ref = oracle.masked_ffn(ol, Xh[s, b], m)
+            assert rel_l2(Yg[s, b], ref) < 1e-4
+            check_elementwise(Yg[s, b], ref, dt)
 
 
 @pytest.mark.parametrize("batch", [8, 32])
@@ -81,7 +83,9 @@ def test_union_degenerate_masks(sffn, tau, expect, batch):
         assert (N == wl.d_ff).all()
         Xh = st(X)
         for b in range(batch):
-            assert rel_l2(Y[0, b], oracle.dense_ffn(ol, Xh[0, b])) < TOL["bf16"]
+            ref = oracle.dense_ffn(ol, Xh[0, b])
+            assert rel_l2(Y[0, b], ref) < TOL["bf16"]
+            check_elementwise(Y[0, b], ref, "bf16")
 
 
 def test_union_tokens_keep_their_own_neurons(sffn):

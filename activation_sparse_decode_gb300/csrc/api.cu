@@ -46,7 +46,11 @@ namespace {
 thread_local std::string g_err;
 constexpr int kMinStages2 = 4;  // ring stages a block needs for the two-blocks-per-SM layer kernel
 int64_t g_wait_ns = 1000000000LL;  // 1 s
-cudaEvent_t g_prof_start = nullptr, g_prof_stop = nullptr;  // bracket gather launches when set
+// Profiling hook: the next g_prof_n dominant-kernel launches are bracketed by
+// event pairs g_prof_start[i], g_prof_stop[i], i counting launches from the
+// last sffn_set_profile_events call (host-side, at launch or capture time).
+std::vector<cudaEvent_t> g_prof_start, g_prof_stop;
+size_t g_prof_next = 0;
 
 constexpr int kVersion = 1;
 
@@ -203,6 +207,15 @@ sffn_status record_profile_event(cudaEvent_t ev, cudaStream_t s) {
   return SFFN_OK;
 }
 
+// The profiling pair of the next dominant-kernel launch, if any is left.
+bool profile_pair(cudaEvent_t* start, cudaEvent_t* stop) {
+  if (g_prof_next >= g_prof_start.size()) return false;
+  *start = g_prof_start[g_prof_next];
+  *stop = g_prof_stop[g_prof_next];
+  ++g_prof_next;
+  return true;
+}
+
 // Gather passes of up to max_bt tokens each.
 sffn_status run_gather(const sffn_layer* L, const void* x, int batch, float* y, const Ws& ws, bool dense,
                        cudaStream_t s) {
@@ -231,9 +244,11 @@ sffn_status run_gather(const sffn_layer* L, const void* x, int batch, float* y, 
     a.nstages = L->gcfg[bt_slot(bt)].nstages;
     a.list_cap = L->gcfg[bt_slot(bt)].list_cap;
     a.wait_ns = (uint64_t)g_wait_ns;
-    if (g_prof_start != nullptr) SFFN_TRY(record_profile_event(g_prof_start, s));
+    cudaEvent_t e0, e1;
+    const bool prof = profile_pair(&e0, &e1);
+    if (prof) SFFN_TRY(record_profile_event(e0, s));
     SFFN_CUDA(launch_gather(d.dtype, L->gcfg[bt_slot(bt)], a, L->gather_grid, s), "gather launch");
-    if (g_prof_stop != nullptr) SFFN_TRY(record_profile_event(g_prof_stop, s));
+    if (prof) SFFN_TRY(record_profile_event(e1, s));
   }
   return SFFN_OK;
 }
@@ -272,9 +287,11 @@ sffn_status run_sparse_ffn(const sffn_layer* L, const void* x, int batch, float*
   a.list_cap = uc.list_cap;
   a.ring_bytes = uc.ring_bytes;
   a.wait_ns = (uint64_t)g_wait_ns;
-  if (g_prof_start != nullptr) SFFN_TRY(record_profile_event(g_prof_start, s));
+  cudaEvent_t e0, e1;
+  const bool prof = profile_pair(&e0, &e1);
+  if (prof) SFFN_TRY(record_profile_event(e0, s));
   SFFN_CUDA(launch_union(d.dtype, uc, a, L->gather_grid, s), "union launch");
-  if (g_prof_stop != nullptr) SFFN_TRY(record_profile_event(g_prof_stop, s));
+  if (prof) SFFN_TRY(record_profile_event(e1, s));
   return SFFN_OK;
 }
 
@@ -328,9 +345,11 @@ sffn_status run_layer(const sffn_layer* L, const void* x, const float* y_prev, v
   a.bal_counts = ws.bal_counts();
   a.bal_lists = ws.bal_lists();
   a.wait_ns = (uint64_t)g_wait_ns;
-  if (g_prof_start != nullptr) SFFN_TRY(record_profile_event(g_prof_start, s));
+  cudaEvent_t e0, e1;
+  const bool prof = profile_pair(&e0, &e1);
+  if (prof) SFFN_TRY(record_profile_event(e0, s));
   SFFN_CUDA(launch_layer(d.dtype, L->lcfg, a, L->layer_grid, s), "layer launch");
-  if (g_prof_stop != nullptr) SFFN_TRY(record_profile_event(g_prof_stop, s));
+  if (prof) SFFN_TRY(record_profile_event(e1, s));
   return SFFN_OK;
 }
 
@@ -355,9 +374,19 @@ const char* sffn_status_string(sffn_status st) {
   return "unknown status";
 }
 
-sffn_status sffn_set_profile_events(void* start_event, void* stop_event) {
-  g_prof_start = static_cast<cudaEvent_t>(start_event);
-  g_prof_stop = static_cast<cudaEvent_t>(stop_event);
+sffn_status sffn_set_profile_events(void* const* start_events, void* const* stop_events, int32_t n_pairs) {
+  g_err.clear();
+  if (n_pairs < 0 || (n_pairs > 0 && (start_events == nullptr || stop_events == nullptr)))
+    return fail(SFFN_ERR_INVALID_ARG, "profile events: %d pairs, arrays NULL", n_pairs);
+  g_prof_start.clear();
+  g_prof_stop.clear();
+  for (int i = 0; i < n_pairs; ++i) {
+    if (start_events[i] == nullptr || stop_events[i] == nullptr)
+      return fail(SFFN_ERR_INVALID_ARG, "profile event pair %d is NULL", i);
+    g_prof_start.push_back(static_cast<cudaEvent_t>(start_events[i]));
+    g_prof_stop.push_back(static_cast<cudaEvent_t>(stop_events[i]));
+  }
+  g_prof_next = 0;
   return SFFN_OK;
 }
 

@@ -80,7 +80,7 @@ _c = {
     "status": _sig("sffn_read_device_status", _i32, _vp, ctypes.POINTER(_i32), _vp),
     "debug_wait": _sig("sffn_debug_wait_timeout", _i32, _vp, _sz, _i64, _vp),
     "wait_limit": _sig("sffn_set_wait_limit_ns", _i32, _i64),
-    "prof_events": _sig("sffn_set_profile_events", _i32, _vp, _vp),
+    "prof_events": _sig("sffn_set_profile_events", _i32, ctypes.POINTER(_vp), ctypes.POINTER(_vp), _i32),
     "noalloc": _sig("sffn_forward_noalloc", _i32, _vp, _vp, _vp, _vp),
     "noalloc_status": _sig("sffn_noalloc_read_status", _i32, ctypes.POINTER(_i32), _vp),
     "status_string": _sig("sffn_status_string", ctypes.c_char_p, _i32),
@@ -281,11 +281,15 @@ def sffn_set_wait_limit_ns(ns: int):
     _check(_c["wait_limit"](int(ns)))
 
 
-def sffn_set_profile_events(start: Optional[torch.cuda.Event], stop: Optional[torch.cuda.Event]):
-    """Bracket later gather launches with these (timing-enabled) events; None, None turns it off."""
-    s = None if start is None else ctypes.c_void_p(start.cuda_event)
-    e = None if stop is None else ctypes.c_void_p(stop.cuda_event)
-    _check(_c["prof_events"](s, e))
+def sffn_set_profile_events(starts: Sequence[torch.cuda.Event] = (), stops: Sequence[torch.cuda.Event] = ()):
+    """Bracket the next len(starts) dominant-kernel launches with these
+    (timing-enabled, already created) event pairs, one pair per launch; no
+    arguments turns it off."""
+    n = len(starts)
+    assert len(stops) == n
+    a = (ctypes.c_void_p * max(n, 1))(*[e.cuda_event for e in starts])
+    b = (ctypes.c_void_p * max(n, 1))(*[e.cuda_event for e in stops])
+    _check(_c["prof_events"](a, b, n))
 
 
 def sffn_status_string(st: int) -> str:

@@ -299,12 +299,17 @@ sffn_status sffn_read_device_status(void* workspace, int32_t* status, void* stre
 sffn_status sffn_debug_wait_timeout(void* workspace, size_t workspace_bytes, int64_t timeout_ns,
                                     void* stream);
 
-/* Profiling hook: when both are non-NULL, every later gather launch (the
- * fused row-gather FFN kernel of sffn_forward / sffn_dense_forward /
- * sffn_forward_stack) is bracketed by cudaEventRecord(start_event) and
- * cudaEventRecord(stop_event) on its stream (cudaEvent_t passed as void*).
- * NULL, NULL switches it off.  Process-wide, not thread-safe: for timing. */
-sffn_status sffn_set_profile_events(void* start_event, void* stop_event);
+/* Profiling hook: the next n_pairs launches of a call's dominant kernel (the
+ * single-launch layer kernel at batch 1, the tensor-core union kernel or the
+ * row-gather kernel; of sffn_forward, sffn_dense_forward and
+ * sffn_forward_stack), counted from this call, are each bracketed on their
+ * stream by records of start_events[i] and stop_events[i] (cudaEvent_t passed
+ * as void*), i = 0, 1, ...; later launches are not.  While the stream is being
+ * captured the records become graph nodes, so a graph replay times every
+ * bracketed launch inside the graph.  n_pairs = 0 switches it off.  The arrays
+ * are copied; the events must outlive their use.  Process-wide, not
+ * thread-safe: for timing.  SFFN_ERR_INVALID_ARG for NULL arrays or events. */
+sffn_status sffn_set_profile_events(void* const* start_events, void* const* stop_events, int32_t n_pairs);
 
 /* Limit of every device-side wait, in nanoseconds (default 1e9). */
 sffn_status sffn_set_wait_limit_ns(int64_t ns);

@@ -78,6 +78,7 @@ def words_to_mask(words, f):
 # (about 150 block partials per element: at most ~1e-4 of rms(y) in the worst
 # order, ~1e-6 typically; one neuron's term is >= ~0.009 rms(y)).
 ATOMIC_EPS = 2.0 ** -12
+REPEAT_RUNS = 20
 
 
 def same_call(y1, y2):
@@ -178,6 +179,26 @@ def test_opt175b_stack48_fp16(sffn, batch):
     pairs = [(0, 0), (1, wl.n_layers - 1), (1, 17)]
     teacher_forced(sffn, wl, lws, layers, x_out, trace, masks, ys, pairs, [0] if batch == 1 else [0, batch - 1])
     recompute_all(sffn, layers, trace, masks, ys, wl)
+    # the same two-step decode again and again: every run must record the same
+    # layer inputs and masks and outputs equal up to the order of atomic adds
+    # (an input that differs is followed through the LayerNorm rounding, so
+    # only the first layer where a run departs is reported)
+    for rep in range(REPEAT_RUNS):
+        xo2, tr2, mk2, ys2 = run_stack(sffn, layers, x0, steps)
+        for t in range(steps):
+            for l in range(wl.n_layers):
+                if not torch.equal(tr2[t, l], trace[t, l]):
+                    # legitimate: the previous layer's atomic order moved a
+                    # LayerNorm output across a rounding boundary; from here on
+                    # the runs decode different inputs
+                    break
+                same_m = torch.equal(mk2[t, l], masks[t, l])
+                same_y = all(same_call(ys2[t, l, b].cpu().numpy(), ys[t, l, b].cpu().numpy()) for b in range(batch))
+                assert same_m and same_y, (f"run {rep + 1}, step {t}, layer {l}: same input, but "
+                                           f"mask {'same' if same_m else 'differs'}, y {'same' if same_y else 'differs'}")
+            else:
+                continue
+            break
     if batch == 8:
         del test_opt175b_stack48_fp16._stack
         torch.cuda.empty_cache()

@@ -28,6 +28,11 @@ What it computes, step by step, in the pages' order:
 5. Dense FFN (the no-skip definition): the same with every neuron listed.
 6. Stack: x_{l+1} = round_dtype(LayerNorm(x_l + y_l)), gamma = 1, beta = 0,
    eps = 1e-5, biased variance; the next decode step starts from the last x.
+   Look-ahead variant: an asynchronous predictor forecasts a layer's MLP
+   sparsity before that layer's input exists (sparsity page, section
+   "如何充分利用結構化稀疏性進行加速", the DejaVu design): each layer call's
+   mask comes from its own predictor applied to the input of the call
+   before it, so prediction can overlap the previous layer's work.
 7. Offline profile: per-neuron count of predicted activations over profile
    tokens, sorted descending with ties broken by ascending index (hot-first
    order; PowerInfer page, "Fase fuera de linea": the profiler records neuron
@@ -266,6 +271,33 @@ def stack_decode(layers: Sequence[OracleLayer], x0: np.ndarray, n_steps: int,
             xs.append(x)
         trace.append(xs)
     return trace
+
+
+def lookahead_stack_decode(layers: Sequence[OracleLayer], x0: np.ndarray, n_steps: int,
+                           gamma=None, beta=None, eps: float = 1e-5):
+    """The stack decode with look-ahead masks.  Layer calls are numbered across
+    steps (layer l of step t is call t * n_layers + l).  Call k > 0 keeps the
+    neurons its own predictor (U, V, b, tau of that layer) scores above tau
+    on the input of call k - 1; call 0 has no earlier input and scores its
+    own.  The FFN itself, the residual and the LayerNorm are as in
+    stack_decode.  Returns (inputs [n_steps][n_layers + 1][...], masks
+    [n_steps][n_layers][...]) in stored format / bool."""
+    fmt = layers[0].fmt
+    x = np.asarray(x0)
+    prev = x  # input of the call before the current one
+    trace, masks = [], []
+    for _ in range(n_steps):
+        xs, ms = [x], []
+        for layer in layers:
+            m = predicted_mask(predictor_scores(layer, prev), layer.tau)
+            y = masked_ffn(layer, x, m)
+            prev = x
+            x = residual_layernorm(x, y, fmt, gamma, beta, eps)
+            xs.append(x)
+            ms.append(m)
+        trace.append(xs)
+        masks.append(ms)
+    return trace, masks
 
 
 # --------------------------------------------------------------------------

@@ -355,6 +355,70 @@ def check_stack(o):
         assert np.array_equal(tr[0][l + 1], want)
 
 
+def _lookahead_layers(o):
+    """Two one-neuron fp32 layers on d = 4 built so that the look-ahead masks
+    differ from the exact ones (derivation in check_lookahead_worked).
+    Layer A: predictor s = x0 - x3, gate a = ReLU(x0), W_down^T row (-4, 4, 0, 0).
+    Layer B: predictor s = x0, gate a = ReLU(x1), W_down^T row (1, 0, 0, 0)."""
+    row = lambda *v: np.asarray([v], np.float32)  # one row: [1][n]
+    A = o.OracleLayer(w_up=row(1, 0, 0, 0), w_downT=row(-4, 4, 0, 0), b=np.zeros(1, np.float32), U=row(1),
+                      V=row(1, 0, 0, -1), fmt="f32")
+    Bl = o.OracleLayer(w_up=row(0, 1, 0, 0), w_downT=row(1, 0, 0, 0), b=np.zeros(1, np.float32), U=row(1),
+                       V=row(1, 0, 0, 0), fmt="f32")
+    return [A, Bl], np.asarray([1, -1, 1, -1], np.float32)
+
+
+def check_lookahead_worked(o):
+    """Hand-derived two-step decode (eps = 1e-5, fp32 stored values):
+    step 0, call 0 (A): no earlier input, scores x0 = (1,-1,1,-1): s = 2 > 0,
+      a = 1, y = (-4,4,0,0); x0 + y = (-3,3,1,-1) has mean 0, variance 5, so
+      x1 = (-3,3,1,-1) / sqrt(5 + eps).
+    step 0, call 1 (B): scores the earlier input x0: s = 1 > 0, active (its
+      own input would give s = x1[0] < 0, inactive); a = ReLU(x1[1]) = 3/q,
+      q = sqrt(5 + eps); x1 + y = (0,3,1,-1)/q has mean 0.75/q and centred
+      values (-0.75,2.25,0.25,-1.75)/q of variance 2.1875/q^2, so
+      x2 = (-0.75,2.25,0.25,-1.75) / sqrt(2.1875 + eps q^2).
+    step 1, call 2 (A): scores x1: s = (-3 + 1)/q < 0, inactive (its own input
+      x2 would give s = (-0.75 + 1.75)/... > 0), so y = 0 and x3 = LN(x2).
+    step 1, call 3 (B): scores x2: s = x2[0] < 0, inactive, x4 = LN(x3)."""
+    layers, x0 = _lookahead_layers(o)
+    tr, ms = o.lookahead_stack_decode(layers, x0, 2)
+    assert [[bool(m[0]) for m in step] for step in ms] == [[True, True], [False, False]]
+    eps = 1e-5
+    q = np.sqrt(5 + eps)
+    x1 = np.array([-3, 3, 1, -1]) / q
+    x2 = np.array([-0.75, 2.25, 0.25, -1.75]) / np.sqrt(2.1875 + eps * q * q)
+    assert _rel(tr[0][1], x1) < 1e-6
+    assert _rel(tr[0][2], x2) < 1e-6
+    assert np.array_equal(tr[1][0], tr[0][2])  # the next step starts from the last output
+    x3 = (x2 - x2.mean()) / np.sqrt(x2.var() + eps)
+    assert _rel(tr[1][1], x3) < 1e-6
+    # the exact stack keeps call 1 inactive: it reaches x2 = LN(x1) instead
+    ex = o.stack_decode(layers, x0, 1)
+    assert _rel(ex[0][2], x1 / np.sqrt(1 + eps)) < 1e-6
+
+
+def check_lookahead_fixed_input(o):
+    """Where every layer call sees the same input the look-ahead masks are the
+    exact ones: layers that add nothing (W_down = 0) on a two-point fp16 token
+    +-1, which round(LN(.)) maps to itself (1 / sqrt(1 + 1e-5) rounds to 1),
+    so the look-ahead decode must equal stack_decode."""
+    layers = []
+    for s in range(3):
+        lay = random_layer(o, f=24, d=16, seed=60 + s, fmt="f16")
+        lay.w_downT = np.zeros_like(lay.w_downT)
+        layers.append(lay)
+    x0 = o.round_to(np.array([1.0, -1.0] * 8), "f16")
+    tr, ms = o.lookahead_stack_decode(layers, x0, 2)
+    ex = o.stack_decode(layers, x0, 2)
+    for t in range(2):
+        for l in range(4):
+            assert np.array_equal(tr[t][l], x0) and np.array_equal(ex[t][l], x0)
+        for l, lay in enumerate(layers):
+            assert np.array_equal(ms[t][l], o.predicted_mask(o.predictor_scores(lay, x0), 0.0))
+            assert ms[t][l].any() and not ms[t][l].all()
+
+
 def check_profile_and_perm(o):
     layer = random_layer(o, f=30, seed=40)
     layer.U = np.zeros_like(layer.U)

@@ -115,10 +115,33 @@ def _mutant_bf16_truncate(o):
     o.round_to = r
 
 
+def _mutant_lookahead_own_input(o):
+    def la(layers, x0, n_steps, gamma=None, beta=None, eps=1e-5):
+        tr = o.stack_decode(layers, x0, n_steps, gamma, beta, eps)
+        ms = [[o.predicted_mask(o.predictor_scores(lay, tr[t][l]), lay.tau) for l, lay in enumerate(layers)]
+              for t in range(n_steps)]
+        return tr, ms
+    o.lookahead_stack_decode = la
+
+
+def _mutant_lookahead_restarts_each_step(o):
+    orig = o.lookahead_stack_decode
+    def la(layers, x0, n_steps, gamma=None, beta=None, eps=1e-5):
+        tr, ms = [], []
+        x = x0
+        for _ in range(n_steps):
+            t1, m1 = orig(layers, x, 1, gamma, beta, eps)
+            tr += t1
+            ms += m1
+            x = t1[0][-1]
+        return tr, ms
+    o.lookahead_stack_decode = la
+
+
 MUTANTS = [_mutant_no_bias, _mutant_gate_up_swapped, _mutant_threshold_ge, _mutant_bias_sign,
            _mutant_down_uses_up_rows, _mutant_mask_ignored, _mutant_descending_idx,
            _mutant_unbiased_variance, _mutant_no_residual, _mutant_ties_descending,
-           _mutant_bf16_truncate]
+           _mutant_bf16_truncate, _mutant_lookahead_own_input, _mutant_lookahead_restarts_each_step]
 
 
 @pytest.mark.parametrize("plant", MUTANTS, ids=lambda m: m.__name__[len("_mutant_"):])

@@ -299,9 +299,21 @@ sffn_status check_x(const sffn_layer* L, const void* x) { return check_dev_ptr(x
 
 // One token through the single-launch layer kernel.  With y_prev, the kernel
 // first forms x = round(LN(x_prev + y_prev)) and stores it at x_ln_out.
+// Look-ahead stacks: the call's own rows come from la_in and the predictor of
+// `pred` (the next layer) is evaluated into la_out; predict_only runs only
+// that predictor (no rows, no y, launched without clusters).
+struct LookAhead {
+  const sffn_layer* pred = nullptr;
+  const uint32_t* la_in = nullptr;
+  uint32_t* la_out = nullptr;
+  bool predict_only = false;
+};
+
 sffn_status run_layer(const sffn_layer* L, const void* x, const float* y_prev, void* x_ln_out, const float* gamma,
-                      const float* beta, float eps, float* y, uint32_t* mask, const Ws& ws, cudaStream_t s) {
+                      const float* beta, float eps, float* y, uint32_t* mask, const Ws& ws, cudaStream_t s,
+                      const LookAhead& la = LookAhead()) {
   const auto& d = L->desc;
+  const auto& pd = la.pred != nullptr ? la.pred->desc : L->desc;  // the predictor this launch evaluates
   LayerArgs a{};
   a.x = x;
   a.y_prev = y_prev;
@@ -309,17 +321,20 @@ sffn_status run_layer(const sffn_layer* L, const void* x, const float* y_prev, v
   a.ln_gamma = gamma;
   a.ln_beta = beta;
   a.ln_eps = eps;
-  a.V = d.pred_V;
-  a.U = d.pred_U;
-  a.pb = d.pred_b;
+  a.V = pd.pred_V;
+  a.U = pd.pred_U;
+  a.pb = pd.pred_b;
   a.b = d.b;
-  a.tau = d.tau;
+  a.tau = pd.tau;
   a.w_up = d.w_up;
   a.w_gate = d.w_gate;
   a.w_downT = d.w_downT;
   a.y = y;
   a.h_slots = ws.hl_slots();
   a.mask = mask;
+  a.la_in = la.la_in;
+  a.la_out = la.la_out;
+  a.predict_only = la.predict_only ? 1 : 0;
   a.hdr = ws.hdr();
   a.bar_flags = ws.flags();
   a.d = d.d_model;
@@ -335,8 +350,8 @@ sffn_status run_layer(const sffn_layer* L, const void* x, const float* y_prev, v
   a.hot_stages = L->lcfg.hot_stages;
   const int own_cap = (d.d_ff + L->layer_grid - 1) / L->layer_grid;
   // the balancing exchange holds at most 256 block counts
-  a.balance = L->lcfg.balance && own_cap >= 8 && L->layer_grid <= 256 ? 1 : 0;
-  a.cluster = a.balance == 0 ? L->layer_cluster : 0;
+  a.balance = L->lcfg.balance && own_cap >= 8 && L->layer_grid <= 256 && la.pred == nullptr ? 1 : 0;
+  a.cluster = a.balance == 0 && !la.predict_only ? L->layer_cluster : 0;
   a.static_weights = (d.flags & SFFN_FLAG_STATIC_WEIGHTS) ? 1 : 0;
   int prefill = L->lcfg.hot_stages;
   if (d.expected_active > 0.f)
@@ -640,13 +655,37 @@ size_t sffn_stack_workspace_size(const sffn_layer_t* layers, int32_t n_layers, i
   const auto& d = layers[0]->desc;
   const size_t xb = align_up((size_t)batch * d.d_model * layers[0]->esize, 256);
   const size_t yb = align_up((size_t)batch * d.d_model * sizeof(float), 256);
-  return align_up(per, 256) + 2 * xb + 2 * yb;
+  int Wmax = 0;
+  for (int l = 0; l < n_layers; ++l) Wmax = std::max(Wmax, layers[l]->W);
+  const size_t lab = align_up((size_t)Wmax * sizeof(uint32_t), 256);  // look-ahead mask words, two buffers
+  return align_up(per, 256) + 2 * xb + 2 * yb + 2 * lab;
+}
+
+// Whether a stack can run with look-ahead masks: batch 1, every layer on the
+// single-launch kernel with the same shapes and launch configuration (block
+// c owns the same neurons in every layer, and the U-row staging of the next
+// layer's predictor fits this layer's shared-memory plan), no balancing.
+static sffn_status check_lookahead(const sffn_layer_t* layers, int n_layers, int batch) {
+  if (batch != 1) return fail(SFFN_ERR_UNSUPPORTED, "look-ahead masks are built for batch 1 only");
+  const sffn_layer* L0 = layers[0];
+  for (int l = 0; l < n_layers; ++l) {
+    const sffn_layer* L = layers[l];
+    if (!L->fused() || (L->desc.flags & SFFN_FLAG_BALANCE))
+      return fail(SFFN_ERR_UNSUPPORTED, "look-ahead: layer %d does not run the single-launch kernel without balancing", l);
+    const auto &a = L->desc, &b = L0->desc;
+    if (a.d_ff != b.d_ff || a.rank != b.rank || a.act != b.act || L->layer_grid != L0->layer_grid ||
+        L->layer_cluster != L0->layer_cluster || L->lcfg.nstages != L0->lcfg.nstages ||
+        L->lcfg.u_smem != L0->lcfg.u_smem || L->lcfg.u_off != L0->lcfg.u_off ||
+        L->lcfg.region_bytes != L0->lcfg.region_bytes || L->lcfg.hot_stages != L0->lcfg.hot_stages)
+      return fail(SFFN_ERR_UNSUPPORTED, "look-ahead: layer %d differs in shape or launch configuration", l);
+  }
+  return SFFN_OK;
 }
 
 sffn_status sffn_forward_stack(const sffn_layer_t* layers, int32_t n_layers, const void* x0, int32_t batch,
                                int32_t n_steps, void* x_out, void* x_trace, uint32_t* mask_trace,
                                float* y_trace, const float* ln_gamma, const float* ln_beta, float ln_eps,
-                               void* workspace, size_t ws_bytes, void* stream) {
+                               int32_t options, void* workspace, size_t ws_bytes, void* stream) {
   g_err.clear();
   if (layers == nullptr || n_layers < 1) return fail(SFFN_ERR_INVALID_ARG, "no layers");
   if (n_steps < 1) return fail(SFFN_ERR_INVALID_ARG, "n_steps must be >= 1");
@@ -662,6 +701,9 @@ sffn_status sffn_forward_stack(const sffn_layer_t* layers, int32_t n_layers, con
   if (mask_trace != nullptr) SFFN_TRY(check_dev_ptr(mask_trace, "mask_trace"));
   if (y_trace != nullptr) SFFN_TRY(check_dev_ptr(y_trace, "y_trace"));
   if (!(ln_eps >= 0.f)) return fail(SFFN_ERR_INVALID_ARG, "ln_eps must be >= 0");
+  if (options & ~SFFN_STACK_LOOKAHEAD) return fail(SFFN_ERR_INVALID_ARG, "unknown option bits 0x%x", (unsigned)options);
+  const bool lookahead = (options & SFFN_STACK_LOOKAHEAD) != 0;
+  if (lookahead) SFFN_TRY(check_lookahead(layers, n_layers, batch));
   const size_t need = sffn_stack_workspace_size(layers, n_layers, batch);
   if (workspace == nullptr || ws_bytes < need || (reinterpret_cast<uintptr_t>(workspace) & 255u))
     return fail(SFFN_ERR_WORKSPACE, "stack workspace: %zu bytes needed (256-byte aligned)", need);
@@ -693,6 +735,10 @@ sffn_status sffn_forward_stack(const sffn_layer_t* layers, int32_t n_layers, con
   if (mask_trace != nullptr)  // words past a narrower layer's count stay zero
     SFFN_CUDA(cudaMemsetAsync(mask_trace, 0, (size_t)n_steps * n_layers * batch * Wmax * sizeof(uint32_t), s),
               "mask trace clear");
+  // look-ahead mask words: call k reads buffer k % 2 and predicts into the other
+  const size_t lab = align_up((size_t)Wmax * sizeof(uint32_t), 256);
+  uint32_t* labuf[2] = {reinterpret_cast<uint32_t*>(base + per + 2 * xb + 2 * yb),
+                        reinterpret_cast<uint32_t*>(base + per + 2 * xb + 2 * yb + lab)};
 
   bool all_fused = batch == 1;
   for (int l = 0; l < n_layers; ++l) all_fused = all_fused && layers[l]->fused();
@@ -704,6 +750,15 @@ sffn_status sffn_forward_stack(const sffn_layer_t* layers, int32_t n_layers, con
     const void* xprev = nullptr;  // input of the previous layer
     const float* yprev = nullptr;  // output of the previous layer
     int k = 0;                     // running layer counter (ping-pong index)
+    if (lookahead) {  // call 0's mask: the first layer's predictor on x0
+      Ws ws;
+      SFFN_TRY(check_ws(layers[0], batch, workspace, per, &ws));
+      LookAhead la;
+      la.pred = layers[0];
+      la.la_out = labuf[0];
+      la.predict_only = true;
+      SFFN_TRY(run_layer(layers[0], x0, nullptr, nullptr, nullptr, nullptr, 0.f, nullptr, nullptr, ws, s, la));
+    }
     for (int t = 0; t < n_steps; ++t) {
       for (int l = 0; l < n_layers; ++l, ++k) {
         const sffn_layer* L = layers[l];
@@ -711,12 +766,21 @@ sffn_status sffn_forward_stack(const sffn_layer_t* layers, int32_t n_layers, con
         SFFN_TRY(check_ws(L, batch, workspace, per, &ws));
         float* ycur = y_trace != nullptr ? y_slot(t, l) : ybufs[k & 1];
         uint32_t* mcur = mask_slot(t, l);
+        // look-ahead: this call's mask was predicted by the previous call; this
+        // call predicts the next layer's (the last call's prediction is unused)
+        LookAhead la;
+        if (lookahead) {
+          la.pred = layers[(l + 1) % n_layers];
+          la.la_in = labuf[k & 1];
+          la.la_out = labuf[(k + 1) & 1];
+          mcur = nullptr;
+        }
         void* xin_store;  // where this layer's input lives
         if (k == 0) {
           xin_store = const_cast<void*>(x0);
           if (trace != nullptr)
             SFFN_CUDA(cudaMemcpyAsync(trace, x0, xbytes, cudaMemcpyDeviceToDevice, s), "trace copy");
-          SFFN_TRY(run_layer(L, x0, nullptr, nullptr, nullptr, nullptr, 0.f, ycur, mcur, ws, s));
+          SFFN_TRY(run_layer(L, x0, nullptr, nullptr, nullptr, nullptr, 0.f, ycur, mcur, ws, s, la));
         } else {
           if (l == 0)
             xin_store = xo + (size_t)(t - 1) * xbytes;  // last step's output is this step's input
@@ -724,12 +788,16 @@ sffn_status sffn_forward_stack(const sffn_layer_t* layers, int32_t n_layers, con
             xin_store = trace + ((size_t)t * n_layers + l) * xbytes;
           else
             xin_store = xbuf[k & 1];
-          SFFN_TRY(run_layer(L, xprev, yprev, xin_store, ln_gamma, ln_beta, ln_eps, ycur, mcur, ws, s));
+          SFFN_TRY(run_layer(L, xprev, yprev, xin_store, ln_gamma, ln_beta, ln_eps, ycur, mcur, ws, s, la));
           if (l == 0 && trace != nullptr)
             SFFN_CUDA(cudaMemcpyAsync(trace + (size_t)t * n_layers * xbytes, xin_store, xbytes,
                                       cudaMemcpyDeviceToDevice, s),
                       "trace copy");
         }
+        if (lookahead && mask_trace != nullptr)  // the mask this call used, before call k + 1 reuses the buffer
+          SFFN_CUDA(cudaMemcpyAsync(mask_slot(t, l), labuf[k & 1], (size_t)L->W * sizeof(uint32_t),
+                                    cudaMemcpyDeviceToDevice, s),
+                    "mask trace copy");
         xprev = xin_store;
         yprev = ycur;
       }

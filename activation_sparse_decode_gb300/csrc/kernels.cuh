@@ -108,6 +108,12 @@ struct LayerArgs {
   size_t region_bytes;
   size_t u_off;           // offset of the staged U rows inside the region
   uint64_t wait_ns;
+  // Look-ahead (stacks at batch 1): this call's active rows come from la_in,
+  // predicted by the previous call, and the predictor fields above (V, U,
+  // pb, tau) are the NEXT layer's, evaluated on this call's input into la_out.
+  const uint32_t* la_in;  // NULL, or [ceil(f/32)] mask words of this call
+  uint32_t* la_out;       // [ceil(f/32)] mask words for the next call (zeroed and set here)
+  int predict_only;       // 1: only the predictor, into la_out: no rows read, no y (launched without clusters)
 };
 struct LayerConfig {
   int cpt, act, nstages, u_smem, hot_stages;

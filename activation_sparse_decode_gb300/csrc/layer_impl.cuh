@@ -144,6 +144,11 @@ __global__ void __launch_bounds__(kLayerThreads, CPT == 3 ? 2 : 1) k_layer(const
   const int n_own = c < f ? (f - c + G - 1) / G : 0;
   const int own_cap = (f + G - 1) / G;
   const int nwords = (own_cap + 31) / 32;
+  // look-ahead: this call's rows from la_in, the predictor (the next layer's)
+  // into la_out; predict-only: the predictor into la_out and nothing else
+  const bool lookahead = a.la_in != nullptr;
+  const bool ponly = a.predict_only != 0;
+  uint32_t* const sc_out = (lookahead || ponly) ? a.la_out : a.mask;  // mask words the scores set
 
   // ---- shared memory carve-up (offsets are multiples of 16)
   unsigned char* region = smem;  // U rows (phases 0-4), then the row ring
@@ -222,10 +227,21 @@ __global__ void __launch_bounds__(kLayerThreads, CPT == 3 ? 2 : 1) k_layer(const
     cluster_arrive();
     cluster_wait();
   };
+  // Once this block has sent its rows to the partner (look-ahead sends them
+  // early), an exit only passes phase 2.
+  bool pair_sent = false;
+  auto pair_exit = [&]() {
+    if (!pair_sent) {
+      pair_exit_early();
+    } else {
+      cluster_arrive();
+      cluster_wait();
+    }
+  };
   const int nh = c < r ? (r - c + G - 1) / G : 0;  // h rows of this block: c, c + G, ...
   const uint4* V4 = static_cast<const uint4*>(a.V);
   const unsigned char* Ub = static_cast<const unsigned char*>(a.U);
-  const int n_hot = c < a.hot_rows ? min(a.hot_stages, min(n_own, (a.hot_rows - c + G - 1) / G)) : 0;
+  const int n_hot = !ponly && c < a.hot_rows ? min(a.hot_stages, min(n_own, (a.hot_rows - c + G - 1) / G)) : 0;
   {
     if (tid < nh) bulk_prefetch_l2(V4 + (size_t)(c + tid * G) * NCH, row_bytes);
     for (int j = tid; j < n_own; j += kLayerThreads) {
@@ -237,7 +253,7 @@ __global__ void __launch_bounds__(kLayerThreads, CPT == 3 ? 2 : 1) k_layer(const
       const int j = q / ulines, l = q - j * ulines;
       prefetch_l2(Ub + (size_t)(c + (size_t)j * G) * urow_bytes + l * 128);
     }
-    const int nw = c < a.warm_rows ? min(n_own, (a.warm_rows - c + G - 1) / G) : 0;
+    const int nw = !ponly && c < a.warm_rows ? min(n_own, (a.warm_rows - c + G - 1) / G) : 0;
     const int rlines = (row_bytes + 127) / 128;
     for (int q = tid; q < max(n_hot, nw) * rlines; q += kLayerThreads) {
       const int j = q / rlines, l = q - j * rlines;
@@ -263,10 +279,12 @@ __global__ void __launch_bounds__(kLayerThreads, CPT == 3 ? 2 : 1) k_layer(const
       }
     for (int j = tid; j < n_own; j += kLayerThreads) {
       const int i = c + j * G;
-      if (a.b != nullptr)
-        cp_async4(&ownb[j], &a.b[i]);
-      else
-        ownb[j] = 0.f;
+      if (!lookahead) {  // look-ahead loads them with the mask bits, before the list
+        if (a.b != nullptr)
+          cp_async4(&ownb[j], &a.b[i]);
+        else
+          ownb[j] = 0.f;
+      }
       cp_async4(&ownpb[j], &a.pb[i]);
     }
     if (a.u_smem)  // owned U rows -> shared memory, 16 bytes per copy
@@ -318,14 +336,16 @@ __global__ void __launch_bounds__(kLayerThreads, CPT == 3 ? 2 : 1) k_layer(const
   // row k, so that the slots every block acquires below cover all of them
   for (int j = 0; j < nh; ++j) {
     const int k = c + j * G;
-    float4* y4 = reinterpret_cast<float4*>(a.y);
-    const int N4 = d / 4;
-    const int q1 = (int)((int64_t)N4 * (k + 1) / r);
-    for (int q = (int)((int64_t)N4 * k / r) + tid; q < q1; q += kLayerThreads) y4[q] = make_float4(0.f, 0.f, 0.f, 0.f);
-    if (a.mask != nullptr) {
+    if (a.y != nullptr) {
+      float4* y4 = reinterpret_cast<float4*>(a.y);
+      const int N4 = d / 4;
+      const int q1 = (int)((int64_t)N4 * (k + 1) / r);
+      for (int q = (int)((int64_t)N4 * k / r) + tid; q < q1; q += kLayerThreads) y4[q] = make_float4(0.f, 0.f, 0.f, 0.f);
+    }
+    if (sc_out != nullptr) {
       const int W = (f + 31) / 32;
       const int w1 = (int)((int64_t)W * (k + 1) / r);
-      for (int w = (int)((int64_t)W * k / r) + tid; w < w1; w += kLayerThreads) a.mask[w] = 0u;
+      for (int w = (int)((int64_t)W * k / r) + tid; w < w1; w += kLayerThreads) sc_out[w] = 0u;
     }
   }
   // the token: loaded, or formed from the previous layer by residual + LayerNorm
@@ -381,6 +401,132 @@ __global__ void __launch_bounds__(kLayerThreads, CPT == 3 ? 2 : 1) k_layer(const
     uint4* xo = static_cast<uint4*>(a.x_ln_out);
     for (int ch = (int)((int64_t)NCH * c / G) + tid; ch < (int)((int64_t)NCH * (c + 1) / G); ch += kLayerThreads)
       xo[ch] = reinterpret_cast<const uint4*>(xs)[ch];
+  }
+
+  // ---- the ring's list and its first fills (start_ring), and the pair split
+  // (settle_ring).  Normal calls run both after the scores; look-ahead calls
+  // run start_ring as soon as the token is formed (their rows are known from
+  // la_in) and settle_ring after the predictor.
+  //
+  // The list: positions 0..n_hot-1 are the prefetched rows, active or not (an
+  // inactive one carries the bias -inf, which the activation below turns into
+  // an exact zero: it adds nothing), then the other active owned rows in
+  // ascending order.  Warp 0 takes one 32-row word per step, lane k holding
+  // row k's flag; a ballot forms the word and each active lane writes its row
+  // at its rank.
+  //
+  // Pair exchange (clusters of two blocks): a token's active rows fall
+  // unevenly on the blocks, and the block with the most sets the kernel's
+  // length.  The two blocks of a cluster split their rows evenly -- T rows
+  // in all, capacities ceil(T/2) (rank 0) and floor(T/2), each keeping its
+  // own rows up to max(capacity, prefetched stages) and handing the rest,
+  // its last rows, to the other -- without waiting for each other: each
+  // block keeps at least k_safe = max(count/2, prefetched stages) rows
+  // whatever the partner has, streams those at once, and sends its count and
+  // rows [k_safe, count) into the partner's inbox (shared-memory stores, then
+  // one release-arrive on the partner's barrier).  The split is settled when
+  // the partner's message is in, from this block's own shared memory.
+  //
+  // The rows fetched in phase 0 are list positions 0..n_hot-1, in their
+  // stages already.  List position p uses stage p % S.  Own rows start
+  // streaming at once, up to the prefill count when the rows are balanced
+  // afterwards (every block keeps at least that many of its own; traffic in
+  // flight lengthens the balancing exchange's round trips, so it runs with
+  // the request queues short).
+  const int P = a.hot_stages;
+  // ring stages that do not overlap the staged U rows: the only ones a
+  // look-ahead call may fill before the scores are done
+  const int free_stages = a.u_smem ? min(S, (int)(a.u_off / stage_bytes)) : S;
+  const int early = lookahead ? free_stages : S;
+  int nloc = 0, k_safe = 0, pre = 0;
+  auto start_ring = [&]() {
+    if (warp == 0) {
+      for (int j = lane; j < n_hot; j += 32) {
+        list[j] = c + j * G;
+        lbias[j] = s_act[j] != 0 ? ownb[j] : -INFINITY;
+      }
+      int base = n_hot;
+      for (int q = 0; q < nwords; ++q) {
+        const int j = q * 32 + lane;
+        const bool on = j >= n_hot && j < n_own && s_act[j] != 0;
+        const uint32_t bits = __ballot_sync(0xffffffffu, on);
+        if (on) {
+          const int pos = base + __popc(bits & ((1u << lane) - 1u));
+          list[pos] = c + j * G;
+          lbias[pos] = ownb[j];
+        }
+        base += __popc(bits);
+      }
+      if (lane == 0) s_nloc = base;
+    }
+    __syncthreads();
+    nloc = s_nloc;
+    SFFN_TRACE_VAL(11, nloc);
+    k_safe = nloc;
+    if (a.cluster == 2) {
+      k_safe = min(nloc, max(nloc / 2, a.hot_stages));
+      cluster_wait();  // phase 1: the partner's barrier is initialised
+      const uint32_t peer = cluster_rank() ^ 1u;
+      for (int t = tid; t < nloc - k_safe; t += kLayerThreads)
+        st_peer_v2(peer_smem(inbox + t, peer), list[k_safe + t], __float_as_int(lbias[k_safe + t]));
+      __syncthreads();  // every entry is stored before the release below
+      if (tid == 0) {
+        st_peer_s32(peer_smem(&s_pcnt, peer), nloc);
+        mbar_arrive_remote(peer_smem(&s_xbar, peer));
+      }
+      pair_sent = true;
+    }
+    SFFN_TRACE(5);
+    pre = a.balance ? min(nloc, P) : k_safe;
+    for (int p = n_hot; p < min(early, pre); ++p) fill(p % S, list[p]);
+  };
+  // false: the partner's message never came (status set); the caller returns
+  auto settle_ring = [&]() -> bool {
+    // the stages a look-ahead call could not fill before the scores
+    for (int p = max(n_hot, min(early, pre)); p < min(S, pre); ++p) fill(p % S, list[p]);
+    if (a.cluster != 2) return true;
+    bool got = mbar_try_wait_cluster(&s_xbar, 0);
+    if (!got) got = pair_wait_slow(&s_xbar, a.hdr, a.wait_ns);
+    if (__syncthreads_or(!got)) {
+      cp_async_wait_all();
+      cluster_arrive();
+      cluster_wait();
+      return false;
+    }
+    const int rk = (int)cluster_rank();
+    const int np = s_pcnt;
+    const int tot = nloc + np;
+    const int cap_me = rk == 0 ? (tot + 1) / 2 : tot / 2, cap_peer = tot - cap_me;
+    const int keep_peer = min(np, max(cap_peer, P));
+    if (np > keep_peer) {  // the partner's rows [keep_peer, np), from the inbox
+      const int ks_peer = min(np, max(np / 2, P));
+      for (int t = tid; t < np - keep_peer; t += kLayerThreads) {
+        const int2 e = inbox[keep_peer - ks_peer + t];
+        list[nloc + t] = e.x;
+        lbias[nloc + t] = __int_as_float(e.y);
+      }
+      nloc += np - keep_peer;
+    } else {
+      nloc = min(nloc, max(cap_me, P));
+    }
+    __syncthreads();  // the received entries are in place for every thread
+    cluster_arrive();  // phase 2: no more writes into the partner's shared memory
+    for (int p = max(n_hot, min(S, k_safe)); p < min(S, nloc); ++p) fill(p % S, list[p]);
+    SFFN_TRACE(16);
+    return true;
+  };
+
+  // Look-ahead: this call's active rows are already decided (la_in, written
+  // by the previous call); their biases are read here with them, and the ring
+  // starts before the predictor of the next layer runs.
+  if (lookahead) {
+    for (int j = tid; j < n_own; j += kLayerThreads) {
+      const int i = c + j * G;
+      s_act[j] = (uint8_t)((__ldcg(a.la_in + (i >> 5)) >> (i & 31)) & 1u);
+      ownb[j] = a.b != nullptr ? __ldg(a.b + i) : 0.f;
+    }
+    __syncthreads();
+    start_ring();
   }
 
   SFFN_TRACE(1);
@@ -484,7 +630,7 @@ __global__ void __launch_bounds__(kLayerThreads, CPT == 3 ? 2 : 1) k_layer(const
   SFFN_TRACE_AT(13, 0);
   if (!passed) {
     cp_async_wait_all();  // nothing of this block is left in flight
-    if (a.cluster == 2) pair_exit_early();
+    if (a.cluster == 2) pair_exit();
     return;
   }
   SFFN_TRACE(3);
@@ -498,7 +644,7 @@ __global__ void __launch_bounds__(kLayerThreads, CPT == 3 ? 2 : 1) k_layer(const
   if (!mbar_try_wait(ubar, 0) && !layer_wait_slow(ubar, 0, a.hdr, a.wait_ns)) ok = false;
   if (__syncthreads_or(!ok)) {
     cp_async_wait_all();
-    if (a.cluster == 2) pair_exit_early();
+    if (a.cluster == 2) pair_exit();
     return;
   }
   SFFN_TRACE(8);
@@ -541,10 +687,10 @@ __global__ void __launch_bounds__(kLayerThreads, CPT == 3 ? 2 : 1) k_layer(const
       for (int o = Lr >> 1; o > 0; o >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, o);
       if (sub == 0 && j < n_own) {
         const bool act = acc + ownpb[j] > a.tau;
-        s_act[j] = act ? 1 : 0;
-        if (act && a.mask != nullptr) {
+        if (!lookahead) s_act[j] = act ? 1 : 0;
+        if (act && sc_out != nullptr) {
           const int i = c + j * G;
-          atomicOr(&a.mask[i >> 5], 1u << (i & 31));
+          atomicOr(&sc_out[i >> 5], 1u << (i & 31));
         }
       }
     }
@@ -582,114 +728,21 @@ __global__ void __launch_bounds__(kLayerThreads, CPT == 3 ? 2 : 1) k_layer(const
       }
       const int j = q * 32 + lane;
       const bool act = lane < kn && (mine + ownpb[lane < kn ? j : 0]) > a.tau;
-      if (lane < kn) s_act[j] = act ? 1 : 0;
-      if (act && a.mask != nullptr) {
+      if (lane < kn && !lookahead) s_act[j] = act ? 1 : 0;
+      if (act && sc_out != nullptr) {
         const int i = c + j * G;
-        atomicOr(&a.mask[i >> 5], 1u << (i & 31));
+        atomicOr(&sc_out[i >> 5], 1u << (i & 31));
       }
     }
   }
   __syncthreads();
   SFFN_TRACE(9);
-  // The ring's list: positions 0..n_hot-1 are the prefetched rows, active or
-  // not (an inactive one carries the bias -inf, which the activation below
-  // turns into an exact zero: it adds nothing), then the other active owned
-  // rows in ascending order.  Warp 0 takes one 32-row word per step, lane k
-  // holding row k's flag; a ballot forms the word and each active lane
-  // writes its row at its rank.
-  if (warp == 0) {
-    for (int j = lane; j < n_hot; j += 32) {
-      list[j] = c + j * G;
-      lbias[j] = s_act[j] != 0 ? ownb[j] : -INFINITY;
-    }
-    int base = n_hot;
-    for (int q = 0; q < nwords; ++q) {
-      const int j = q * 32 + lane;
-      const bool on = j >= n_hot && j < n_own && s_act[j] != 0;
-      const uint32_t bits = __ballot_sync(0xffffffffu, on);
-      if (on) {
-        const int pos = base + __popc(bits & ((1u << lane) - 1u));
-        list[pos] = c + j * G;
-        lbias[pos] = ownb[j];
-      }
-      base += __popc(bits);
-    }
-    if (lane == 0) s_nloc = base;
+  if (ponly) {  // the predictor's mask words are out: nothing else to do
+    cp_async_wait_all();
+    return;
   }
-  __syncthreads();
-  int nloc = s_nloc;
-  SFFN_TRACE_VAL(11, nloc);
-
-  // ---- pair exchange (clusters of two blocks): a token's active rows fall
-  // unevenly on the blocks, and the block with the most sets the kernel's
-  // length.  The two blocks of a cluster split their rows evenly -- T rows
-  // in all, capacities ceil(T/2) (rank 0) and floor(T/2), each keeping its
-  // own rows up to max(capacity, prefetched stages) and handing the rest,
-  // its last rows, to the other -- without waiting for each other: each
-  // block keeps at least k_safe = max(count/2, prefetched stages) rows
-  // whatever the partner has, streams those at once, and sends its count and
-  // rows [k_safe, count) into the partner's inbox (shared-memory stores, then
-  // one release-arrive on the partner's barrier).  The split is settled when
-  // the partner's message is in, from this block's own shared memory.
-  int k_safe = nloc;
-  if (a.cluster == 2) {
-    k_safe = min(nloc, max(nloc / 2, a.hot_stages));
-    cluster_wait();  // phase 1: the partner's barrier is initialised
-    const uint32_t peer = cluster_rank() ^ 1u;
-    for (int t = tid; t < nloc - k_safe; t += kLayerThreads)
-      st_peer_v2(peer_smem(inbox + t, peer), list[k_safe + t], __float_as_int(lbias[k_safe + t]));
-    __syncthreads();  // every entry is stored before the release below
-    if (tid == 0) {
-      st_peer_s32(peer_smem(&s_pcnt, peer), nloc);
-      mbar_arrive_remote(peer_smem(&s_xbar, peer));
-    }
-  }
-
-  // ---- phase 5: the active rows stream through a ring of S one-neuron stages,
-  // consumed in groups of up to kGroup neurons per block-wide reduction.
-  SFFN_TRACE(5);
-  // The rows fetched in phase 0 are list positions 0..n_hot-1, in their
-  // stages already.  List position p uses stage p % S.
-  bool failed = false;
-  // Own rows start streaming now, up to the prefill count when the rows are
-  // balanced afterwards (every block keeps at least that many of its own).
-  // Rows every block keeps and streams before the balancing: only the hot
-  // ones.  Traffic in flight lengthens the exchange's round trips (requests
-  // queue behind it), so the exchange runs with the request queues short.
-  const int P = a.hot_stages;
-  const int pre = a.balance ? min(nloc, P) : k_safe;
-  for (int p = n_hot; p < min(S, pre); ++p) fill(p % S, list[p]);
-  if (a.cluster == 2) {  // settle the pair split (see the pair exchange above)
-    bool got = mbar_try_wait_cluster(&s_xbar, 0);
-    if (!got) got = pair_wait_slow(&s_xbar, a.hdr, a.wait_ns);
-    if (__syncthreads_or(!got)) {
-      cp_async_wait_all();
-      cluster_arrive();
-      cluster_wait();
-      return;
-    }
-    const int rk = (int)cluster_rank();
-    const int np = s_pcnt;
-    const int tot = nloc + np;
-    const int cap_me = rk == 0 ? (tot + 1) / 2 : tot / 2, cap_peer = tot - cap_me;
-    const int keep_peer = min(np, max(cap_peer, P));
-    if (np > keep_peer) {  // the partner's rows [keep_peer, np), from the inbox
-      const int ks_peer = min(np, max(np / 2, P));
-      for (int t = tid; t < np - keep_peer; t += kLayerThreads) {
-        const int2 e = inbox[keep_peer - ks_peer + t];
-        list[nloc + t] = e.x;
-        lbias[nloc + t] = __int_as_float(e.y);
-      }
-      nloc += np - keep_peer;
-    } else {
-      nloc = min(nloc, max(cap_me, P));
-    }
-    __syncthreads();  // the received entries are in place for every thread
-    cluster_arrive();  // phase 2: no more writes into the partner's shared memory
-    for (int p = max(n_hot, min(S, k_safe)); p < min(S, nloc); ++p) fill(p % S, list[p]);
-    SFFN_TRACE(16);
-  }
-
+  if (!lookahead) start_ring();
+  if (!settle_ring()) return;
   SFFN_TRACE_VAL(19, nloc);
 
 
@@ -823,6 +876,7 @@ __global__ void __launch_bounds__(kLayerThreads, CPT == 3 ? 2 : 1) k_layer(const
     for (int p = pre; p < min(S, nloc); ++p) fill(p % S, list[p]);
   }
 
+  bool failed = false;
   float xr[CPT][E], yacc[CPT][E];
 #pragma unroll
   for (int cq = 0; cq < CPT; ++cq) {

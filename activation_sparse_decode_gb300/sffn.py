@@ -72,7 +72,7 @@ _c = {
     "dense": _sig("sffn_dense_forward", _i32, _vp, _vp, _i32, _vp, _vp, _sz, _vp),
     "ln": _sig("sffn_residual_layernorm", _i32, _vp, _vp, _i32, _i32, _i32, _vp, _vp, ctypes.c_float, _vp, _vp),
     "stack": _sig("sffn_forward_stack", _i32, ctypes.POINTER(_vp), _i32, _vp, _i32, _i32, _vp, _vp, _vp, _vp,
-                  _vp, _vp, ctypes.c_float, _vp, _sz, _vp),
+                  _vp, _vp, ctypes.c_float, _i32, _vp, _sz, _vp),
     "stack_ws": _sig("sffn_stack_workspace_size", _sz, ctypes.POINTER(_vp), _i32, _i32),
     "profile": _sig("sffn_profile_counts", _i32, _vp, _vp, _i32, _vp, _vp, _sz, _vp),
     "hot_first": _sig("sffn_hot_first_perm", _i32, ctypes.POINTER(_i32), _i32, ctypes.POINTER(_i32)),
@@ -242,12 +242,15 @@ def sffn_stack_workspace_size(layers: Sequence[Layer], batch: int) -> int:
     return int(_c["stack_ws"](_handles(layers), len(layers), batch))
 
 
+SFFN_STACK_LOOKAHEAD = 1
+
+
 def sffn_forward_stack(layers: Sequence[Layer], x0: torch.Tensor, n_steps: int, x_out: torch.Tensor,
                        ws: torch.Tensor, x_trace=None, gamma=None, beta=None, eps: float = 1e-5, stream=None,
-                       mask_trace=None, y_trace=None):
+                       mask_trace=None, y_trace=None, options: int = 0):
     _check(_c["stack"](_handles(layers), len(layers), _ptr(x0), x0.shape[0], n_steps, _ptr(x_out),
-                       _ptr(x_trace), _ptr(mask_trace), _ptr(y_trace), _ptr(gamma), _ptr(beta), eps, _ptr(ws),
-                       ws.numel(), _stream(stream)))
+                       _ptr(x_trace), _ptr(mask_trace), _ptr(y_trace), _ptr(gamma), _ptr(beta), eps, options,
+                       _ptr(ws), ws.numel(), _stream(stream)))
 
 
 def sffn_profile_counts(layer: Layer, X: torch.Tensor, counts: torch.Tensor, ws: torch.Tensor, stream=None):

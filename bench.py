@@ -52,7 +52,9 @@ sys.path.insert(0, ROOT)
 WORKLOAD = "c5"
 DEFAULT_STEPS = {"c1": 300, "c2": 300, "c3": 100, "c4": 10, "c5": 20}
 SUITE_STEPS = {"c1": 40, "c2": 40, "c3": 20, "c4": 4, "c5": 3}  # sub-record steps (timed), each after >= 3 warm-up steps
-SUITE = [("c1", 1), ("c2", 1), ("c3", 1), ("c3", 4), ("c3", 8), ("c3", 32), ("c4", 1), ("c5", 8)]
+# (workload, batch, look-ahead masks): the stacks also at batch 1 with look-ahead masks
+SUITE = [("c1", 1, 0), ("c2", 1, 0), ("c3", 1, 0), ("c3", 4, 0), ("c3", 8, 0), ("c3", 32, 0), ("c4", 1, 0),
+         ("c4", 1, 1), ("c5", 8, 0), ("c5", 1, 1)]
 METRIC = "sparse-FFN decode tokens/s at batch 1 and achieved HBM GB/s vs roofline"
 L2_BYTES = 126 * 2 ** 20
 ESIZE = {"f32": 4, "f16": 2, "bf16": 2}
@@ -68,6 +70,8 @@ def parse():
     p.add_argument("--workload", default=WORKLOAD, choices=["c1", "c2", "c3", "c4", "c5"])
     p.add_argument("--batch", type=int, default=1)
     p.add_argument("--no-suite", action="store_true", help="headline only, no sub-records")
+    p.add_argument("--lookahead", action="store_true",
+                   help="stacks at batch 1: look-ahead masks (each layer's mask predicted from the previous input)")
     p.add_argument("--row-gather", action="store_true", help="batches: CUDA-core row gather, not the union path")
     p.add_argument("--no-dense", action="store_true", help="skip the dense contrast")
     p.add_argument("--no-stats", action="store_true", help="skip band / recall / precision statistics")
@@ -348,7 +352,8 @@ def collect_stats(sffn, torch, model, calls, B, dev):
 
 # ---------------------------------------------------------------- one measurement
 
-def measure(sffn, W, torch, model, B, steps, warmup, dev, world, args, stats=True, dense=True, want_e2e=False):
+def measure(sffn, W, torch, model, B, steps, warmup, dev, world, args, stats=True, dense=True, want_e2e=False,
+            lookahead=False):
     """Times `steps` graph replays of one decode step of `model` at batch B.
     Returns (record, extras) where extras carries what the headline line needs."""
     wl = model.wl
@@ -361,6 +366,8 @@ def measure(sffn, W, torch, model, B, steps, warmup, dev, world, args, stats=Tru
     layers = model.layers
     union_path = B >= 3 and wl.dtype != "f32" and d % 128 == 0 and not args.row_gather
     rank, _, _ = dist_env()
+    lookahead = lookahead and stack and B == 1
+    opts = sffn.SFFN_STACK_LOOKAHEAD if lookahead else 0
 
     X = W.make_tokens(wl, T, batch=B, seed=rank, device=dev)  # [T][B][d]
     if stack:
@@ -372,12 +379,17 @@ def measure(sffn, W, torch, model, B, steps, warmup, dev, world, args, stats=Tru
         Y = torch.empty(T, B, d, dtype=torch.float32, device=dev)
 
     # ---- active counts, unions and predictor statistics, outside any timing
+    la_rec = {}
     if stack:
         Tp = min(T, 2)
         trace = torch.empty(Tp, L, B, d, dtype=X.dtype, device=dev)
         xo = torch.empty(Tp, B, d, dtype=X.dtype, device=dev)
-        sffn.sffn_forward_stack(layers, x0, Tp, xo, ws, x_trace=trace)
+        Wd = (f + 31) // 32
+        mtr = torch.zeros(Tp, L, B, Wd, dtype=torch.int32, device=dev)
+        sffn.sffn_forward_stack(layers, x0, Tp, xo, ws, x_trace=trace, mask_trace=mtr, options=opts)
         calls = [(l, trace[t, l]) for t in range(Tp) for l in range(L)]
+        if lookahead and stats:
+            la_rec = lookahead_stats(sffn, torch, model, trace, mtr, dev)
     else:
         calls = [(t % R, X[t]) for t in range(min(T, 64))]
     st_rec, unions, per_layer_union, n_tok = collect_stats(sffn, torch, model, calls if stats else calls[:4], B, dev)
@@ -389,7 +401,7 @@ def measure(sffn, W, torch, model, B, steps, warmup, dev, world, args, stats=Tru
 
     def step_body():
         if stack:
-            sffn.sffn_forward_stack(layers, x0, T, Y, ws)
+            sffn.sffn_forward_stack(layers, x0, T, Y, ws, options=opts)
         else:
             for t in range(T):
                 sffn.sffn_forward(layers[t % R], X[t], Y[t], ws)
@@ -405,7 +417,9 @@ def measure(sffn, W, torch, model, B, steps, warmup, dev, world, args, stats=Tru
     # path is a driver node, not counted)
     groups = (B + 7) // 8
     if B == 1:
-        launches_per_step = T * L + (1 if stack else 0)  # stacks: LayerNorm folded into the next layer's kernel
+        # stacks: LayerNorm folded into the next layer's kernel, one closing
+        # LayerNorm launch; look-ahead: one predictor-only launch first
+        launches_per_step = T * L + (1 if stack else 0) + (1 if lookahead else 0)
     elif union_path:  # hidden layer, scores (one launch each for the whole batch), union kernel
         launches_per_step = T * L * (3 + (1 if stack else 0))
     else:
@@ -469,7 +483,7 @@ def measure(sffn, W, torch, model, B, steps, warmup, dev, world, args, stats=Tru
     k_s = k_us / 1e6
     us_per_layer = ms_per_step * 1e3 / (T * L)
     rec = {
-        "workload": wl.name, "batch": B, "layers": L, "decode_steps_per_step": T,
+        "workload": wl.name, "batch": B, "layers": L, "decode_steps_per_step": T, "lookahead": lookahead,
         "path": ("tensor-core union" if union_path else "single-launch layer kernel" if B == 1
                  else "CUDA-core row gather"),
         "tokens_per_s": round(value, 1),
@@ -490,6 +504,7 @@ def measure(sffn, W, torch, model, B, steps, warmup, dev, world, args, stats=Tru
         "peak_gbs": peak,
     }
     rec.update(st_rec)
+    rec.update(la_rec)
     if stack and B > 1:
         rec["union_per_layer"] = [round(float(np.mean(per_layer_union[l])), 1) for l in range(L)]
         p = [np.asarray(lw.p) for lw in model.lws]
@@ -503,6 +518,35 @@ def measure(sffn, W, torch, model, B, steps, warmup, dev, world, args, stats=Tru
     if want_e2e:
         extras["e2e"] = e2e_timing(torch, graph, stream, x0 if stack else X, Y, steps, world, T * B)
     return rec, extras
+
+
+def lookahead_stats(sffn, torch, model, trace, mtr, dev):
+    """Look-ahead masks (mtr, what each call of a traced run used) against the
+    masks the exact predictor and the exact ReLU pattern give on the same
+    call's input (trace): recall and precision over every call of the run."""
+    f = model.wl.d_ff
+    ws = sffn.new_workspace(sffn.sffn_workspace_size(model.layers[0], 1), dev)
+    bits = torch.arange(32, device=dev, dtype=torch.int32)
+    tp_p = n_p = n_la = tp_e = n_e = 0.0
+    Tp, L = trace.shape[0], trace.shape[1]
+    for t in range(Tp):
+        for l in range(L):
+            x = trace[t, l]
+            r = predictor_stats(sffn, torch, model.layers[l], model.lws[l], x, ws, model.wl.tau)
+            la = ((mtr[t, l, 0][:, None] >> bits) & 1).reshape(-1)[:f].bool()
+            pred = r["mask"][0]
+            lw = model.lws[l]
+            wg = lw.w_gate if lw.w_gate is not None else lw.w_up
+            xf = x.float()
+            exact = torch.cat([(xf @ wg[i:i + 4096].float().t() + lw.b[i:i + 4096]) > 0
+                               for i in range(0, f, 4096)], 1)[0]
+            tp_p += float((la & pred).sum()); n_p += float(pred.sum()); n_la += float(la.sum())
+            tp_e += float((la & exact).sum()); n_e += float(exact.sum())
+    return {"la_recall_vs_predictor": round(tp_p / max(n_p, 1), 4),
+            "la_precision_vs_predictor": round(tp_p / max(n_la, 1), 4),
+            "la_recall_vs_exact": round(tp_e / max(n_e, 1), 4),
+            "la_precision_vs_exact": round(tp_e / max(n_la, 1), 4),
+            "la_mean_active": round(n_la / (Tp * L), 1)}
 
 
 def time_dominant_kernel(sffn, torch, step_body, stream, n_launches):
@@ -668,13 +712,14 @@ def bench_sffn(args):
     # ---- sub-records first (each workload built, measured and freed), then the headline
     sub = []
     if not args.no_suite:
-        names = [n for i, (n, _) in enumerate(SUITE) if n != head and n not in [m for m, _ in SUITE[:i]]]
+        names = [n for i, (n, _, _) in enumerate(SUITE) if n != head and n not in [m for m, _, _ in SUITE[:i]]]
         for name in names:  # the headline's workload is measured with its own layers below
-            batches = [b for n, b in SUITE if n == name]
-            m = Model(sffn, W, W.get_workload(name), dev, max(batches), args.replicas, args.hot_frac, flags)
-            for b in batches:
+            runs = [(b, la) for n, b, la in SUITE if n == name]
+            m = Model(sffn, W, W.get_workload(name), dev, max(b for b, _ in runs), args.replicas, args.hot_frac,
+                      flags)
+            for b, la in runs:
                 rec, _ = measure(sffn, W, torch, m, b, SUITE_STEPS[name], 3, dev, world, args,
-                                 stats=not args.no_stats, dense=not args.no_dense)
+                                 stats=not args.no_stats, dense=not args.no_dense, lookahead=bool(la))
                 sub.append(rec)
             m.close()
             del m
@@ -684,15 +729,15 @@ def bench_sffn(args):
     wl = W.get_workload(head)
     if args.layers is not None and wl.n_layers > 1:
         wl = wl.with_(n_layers=max(2, min(args.layers, wl.n_layers)))
-    max_b = max([B] + [b for n, b in SUITE if n == head and not args.no_suite])
+    max_b = max([B] + [b for n, b, _ in SUITE if n == head and not args.no_suite])
     model = Model(sffn, W, wl, dev, max_b, args.replicas, args.hot_frac, flags)
     rec, ex = measure(sffn, W, torch, model, B, args.steps, args.warmup, dev, world, args,
-                      stats=not args.no_stats, dense=not args.no_dense, want_e2e=True)
+                      stats=not args.no_stats, dense=not args.no_dense, want_e2e=True, lookahead=args.lookahead)
     if not args.no_suite:
-        for n, b in SUITE:
-            if n == head and b != B:
+        for n, b, la in SUITE:
+            if n == head and (b, bool(la)) != (B, bool(args.lookahead)):
                 r2, _ = measure(sffn, W, torch, model, b, SUITE_STEPS[n], 3, dev, world, args,
-                                stats=not args.no_stats, dense=not args.no_dense)
+                                stats=not args.no_stats, dense=not args.no_dense, lookahead=bool(la))
                 sub.append(r2)
     lw0 = model.lws[0]
 

@@ -266,8 +266,27 @@ sffn_status sffn_residual_layernorm(const void* x, const float* y, int32_t batch
 sffn_status sffn_forward_stack(const sffn_layer_t* layers, int32_t n_layers, const void* x0,
                                int32_t batch, int32_t n_steps, void* x_out, void* x_trace,
                                uint32_t* mask_trace, float* y_trace, const float* ln_gamma,
-                               const float* ln_beta, float ln_eps, void* workspace,
-                               size_t workspace_bytes, void* stream);
+                               const float* ln_beta, float ln_eps, int32_t options,
+                               void* workspace, size_t workspace_bytes, void* stream);
+
+/* options of sffn_forward_stack.
+ *
+ * SFFN_STACK_LOOKAHEAD: look-ahead masks, the asynchronous sparsity predictor
+ * of the DejaVu design (sparsity page, section "如何充分利用結構化稀疏性進行
+ * 加速": the next layer's MLP sparsity is predicted ahead of time, so that
+ * prediction overlaps the current layer's work).  Layer calls are numbered
+ * across steps; call k > 0 uses the neurons that its layer's own predictor
+ * (U, V, pb, tau) scores above tau on the INPUT OF CALL k - 1, and call 0 the
+ * ones it scores on x0.  Each call's kernel reads its rows at once and, while
+ * they stream in, evaluates the next layer's predictor on its own input.
+ * This changes results: a neuron whose score crosses tau between the two
+ * inputs is decided differently than by the exact predictor (the benchmark
+ * reports the recall and precision of these masks against the exact ones).
+ * Requires batch 1 and layers of equal shape and launch configuration (see
+ * sffn_get_layer_info) on the single-launch kernel without
+ * SFFN_FLAG_BALANCE; otherwise SFFN_ERR_UNSUPPORTED.  mask_trace, when given,
+ * records the look-ahead masks the calls used. */
+#define SFFN_STACK_LOOKAHEAD 1
 size_t sffn_stack_workspace_size(const sffn_layer_t* layers, int32_t n_layers, int32_t batch);
 
 /* Offline profile pass (hot/cold classification by activation frequency):

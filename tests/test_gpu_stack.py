@@ -18,7 +18,8 @@ import torch
 import oracle
 from activation_sparse_decode_gb300 import workloads as W
 from activation_sparse_decode_gb300.workloads import to_numpy_stored as st
-from gpu_helpers import TOL, check_next_input, check_token, hot_first, lazy_oracle_layer, mask_from_list
+from gpu_helpers import (BAND, TOL, check_elementwise, check_next_input, check_token, hot_first, lazy_oracle_layer,
+                         mask_from_list, rel_l2)
 
 pytestmark = pytest.mark.gpu
 DEV = "cuda"
@@ -134,6 +135,54 @@ def teacher_forced(sffn, wl, lws, layers, x_out, trace, masks, ys, pairs, tokens
             check_next_input(nh_next[b], want, wl.dtype, max_frac=0.01)
 
 
+def run_stack_lookahead(sffn, layers, x0, n_steps):
+    B, d = x0.shape
+    L = len(layers)
+    Wmax = max((l.d_ff + 31) // 32 for l in layers)
+    ws = sffn.new_workspace(sffn.sffn_stack_workspace_size(layers, B), DEV)
+    x_out = torch.empty(n_steps, B, d, dtype=x0.dtype, device=DEV)
+    trace = torch.empty(n_steps, L, B, d, dtype=x0.dtype, device=DEV)
+    masks = torch.empty(n_steps, L, B, Wmax, dtype=torch.int32, device=DEV)
+    ys = torch.empty(n_steps, L, B, d, dtype=torch.float32, device=DEV)
+    sffn.sffn_forward_stack(layers, x0, n_steps, x_out, ws, x_trace=trace, mask_trace=masks, y_trace=ys,
+                            options=sffn.SFFN_STACK_LOOKAHEAD)
+    torch.cuda.synchronize()
+    assert sffn.sffn_read_device_status(ws) == 0
+    return x_out, trace, masks, ys
+
+
+def lookahead_checks(sffn, wl, lws, layers, x_out, trace, masks, ys, pairs):
+    """Look-ahead calls against the oracle's definition, teacher-forced on the
+    run's own records: call (t, l) must use the neurons its layer's predictor
+    scores above tau on the input of the call before it (the previous layer's
+    input; for layer 0 the last layer's input of the previous step; for the
+    first call its own), outside the band; its y over that mask and the next
+    input it formed are checked as for the exact predictor."""
+    L = len(layers)
+    n = 0
+    for t, l in pairs:
+        ol = lazy_oracle_layer(lws[l], wl.tau)
+        if t == 0 and l == 0:
+            x_prev = trace[0, 0]
+        else:
+            x_prev = trace[t, l - 1] if l > 0 else trace[t - 1, L - 1]
+        xp, xh = st(x_prev)[0], st(trace[t, l])[0]
+        m = words_to_mask(masks[t, l].cpu().numpy()[0], wl.d_ff)
+        s_prev = oracle.predictor_scores(ol, xp)
+        mo = oracle.predicted_mask(s_prev, wl.tau)
+        bad = (mo != m) & ~(np.abs(s_prev - wl.tau) <= BAND)
+        assert not bad.any(), f"call ({t}, {l}): {bad.sum()} neurons outside the band differ from the look-ahead mask"
+        yh = ys[t, l].cpu().numpy()[0]
+        ref = oracle.masked_ffn(ol, xh, m)
+        assert rel_l2(yh, ref) <= TOL[wl.dtype]
+        check_elementwise(yh, ref, wl.dtype)
+        nxt = trace[t, l + 1] if l + 1 < L else x_out[t]
+        want = oracle.residual_layernorm(xh, yh.astype(np.float64), wl.dtype)
+        check_next_input(st(nxt)[0], want, wl.dtype, max_frac=0.01)
+        n += 1
+    return n
+
+
 @pytest.mark.parametrize("flags", [0, 1, 2], ids=["fused", "multi", "fused-balanced"])
 def test_small_stack_both_paths(sffn, flags):
     wl = W.tiny_workload(d_model=512, d_ff=2048, rank=64, dtype="bf16", name="small-stack").with_(n_layers=3)
@@ -202,3 +251,62 @@ def test_opt175b_stack48_fp16(sffn, batch):
     if batch == 8:
         del test_opt175b_stack48_fp16._stack
         torch.cuda.empty_cache()
+
+
+@pytest.mark.parametrize("shape", [(512, 2048, 64, "bf16", "relu", 0), (1024, 4096, 64, "f16", "reglu", 8),
+                                   (12288, 2048, 128, "f16", "relu", 8)],
+                         ids=["bf16-relu", "f16-reglu-static", "f16-wide-pairs"])
+def test_lookahead_small_stack(sffn, shape):
+    """Look-ahead masks on a 3-layer stack over 4 steps: every call against
+    the oracle's look-ahead definition (teacher-forced), on two blocks per SM,
+    with weights staged before the dependency wait, and on pairs of blocks."""
+    d, f, r, dt, act, flags = shape
+    wl = W.tiny_workload(d_model=d, d_ff=f, rank=r, dtype=dt, act=act, mean_p=0.1, name=f"la-{shape}").with_(n_layers=3)
+    lws = [W.make_layer(wl, layer=l, device=DEV) for l in range(3)]
+    layers = [sffn.Layer.from_weights(lw, flags=flags) for lw in lws]
+    x0 = W.make_tokens(wl, 1, device=DEV)[0]
+    x_out, trace, masks, ys = run_stack_lookahead(sffn, layers, x0, 4)
+    assert torch.equal(trace[0, 0], x0)
+    for t in range(1, 4):
+        assert torch.equal(trace[t, 0], x_out[t - 1])
+    assert lookahead_checks(sffn, wl, lws, layers, x_out, trace, masks, ys,
+                            [(t, l) for t in range(4) for l in range(3)]) == 12
+    # the first call has no earlier input: its mask is the exact predictor's
+    idx = torch.empty(1, f, dtype=torch.int32, device=DEV)
+    nn = torch.empty(1, dtype=torch.int32, device=DEV)
+    sffn.sffn_predict(layers[0], x0, idx, nn, sffn.new_workspace(sffn.sffn_workspace_size(layers[0], 1), DEV))
+    m0 = mask_from_list(idx[0].cpu().numpy(), int(nn.item()), f)
+    assert np.array_equal(words_to_mask(masks[0, 0].cpu().numpy()[0], f), m0)
+
+
+def test_lookahead_rejects_what_it_does_not_serve(sffn):
+    wl = W.tiny_workload(d_model=512, d_ff=2048, rank=64, dtype="bf16", name="la-reject").with_(n_layers=2)
+    lws = [W.make_layer(wl, layer=l, device=DEV) for l in range(2)]
+    x_out = torch.empty(1, 2, 512, dtype=torch.bfloat16, device=DEV)
+    for layers, B in (([sffn.Layer.from_weights(lw, max_batch=2) for lw in lws], 2),
+                      ([sffn.Layer.from_weights(lws[0]), sffn.Layer.from_weights(lws[1], flags=1)], 1)):
+        ws = sffn.new_workspace(sffn.sffn_stack_workspace_size(layers, B), DEV)
+        x0 = W.make_tokens(wl, 1, batch=B, device=DEV)[0]
+        with pytest.raises(sffn.SffnError) as e:
+            sffn.sffn_forward_stack(layers, x0, 1, x_out[:, :B], ws, options=sffn.SFFN_STACK_LOOKAHEAD)
+        assert e.value.status == 2
+
+
+def test_opt13b_stack40_lookahead(sffn):
+    """The 40-layer OPT-13B-shaped stack with look-ahead masks: sampled calls
+    against the oracle's definition, and a second run that records the same
+    inputs and masks until the order of atomic adds first moves a LayerNorm
+    rounding."""
+    wl = W.get_workload("c4")
+    lws, layers = build_stack(sffn, wl, wl.n_layers, 1)
+    x0 = W.make_tokens(wl, 1, device=DEV)[0]
+    steps = 4
+    x_out, trace, masks, ys = run_stack_lookahead(sffn, layers, x0, steps)
+    pairs = [(0, 0), (0, 1), (0, wl.n_layers - 1), (1, 0), (steps - 1, 17), (steps - 1, wl.n_layers - 1)]
+    lookahead_checks(sffn, wl, lws, layers, x_out, trace, masks, ys, pairs)
+    xo2, tr2, mk2, ys2 = run_stack_lookahead(sffn, layers, x0, steps)
+    for t in range(steps):
+        for l in range(wl.n_layers):
+            if not torch.equal(tr2[t, l], trace[t, l]):
+                return
+            assert torch.equal(mk2[t, l], masks[t, l]), (t, l)

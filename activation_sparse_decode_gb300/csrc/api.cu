@@ -34,6 +34,7 @@ struct sffn_layer {
   int max_bt = 0;      // tokens per gather pass
   GatherConfig gcfg[3];  // tokens per pass 1, 2, 4
   bool gcfg_ok[3] = {false, false, false};
+  size_t wstride = 0;    // bytes between consecutive neurons' rows of each weight matrix
   LayerConfig lcfg{};    // single-launch batch-1 layer kernel
   bool lcfg_ok = false;
   int layer_grid = 0;    // its blocks: two per SM when two fit, else one
@@ -244,6 +245,7 @@ sffn_status run_gather(const sffn_layer* L, const void* x, int batch, float* y, 
     a.nstages = L->gcfg[bt_slot(bt)].nstages;
     a.list_cap = L->gcfg[bt_slot(bt)].list_cap;
     a.wait_ns = (uint64_t)g_wait_ns;
+    a.wstride = L->wstride;
     cudaEvent_t e0, e1;
     const bool prof = profile_pair(&e0, &e1);
     if (prof) SFFN_TRY(record_profile_event(e0, s));
@@ -287,6 +289,7 @@ sffn_status run_sparse_ffn(const sffn_layer* L, const void* x, int batch, float*
   a.list_cap = uc.list_cap;
   a.ring_bytes = uc.ring_bytes;
   a.wait_ns = (uint64_t)g_wait_ns;
+  a.wstride = L->wstride;
   cudaEvent_t e0, e1;
   const bool prof = profile_pair(&e0, &e1);
   if (prof) SFFN_TRY(record_profile_event(e0, s));
@@ -360,6 +363,7 @@ sffn_status run_layer(const sffn_layer* L, const void* x, const float* y_prev, v
   a.bal_counts = ws.bal_counts();
   a.bal_lists = ws.bal_lists();
   a.wait_ns = (uint64_t)g_wait_ns;
+  a.wstride = L->wstride;
   cudaEvent_t e0, e1;
   const bool prof = profile_pair(&e0, &e1);
   if (prof) SFFN_TRY(record_profile_event(e0, s));
@@ -422,7 +426,8 @@ sffn_status sffn_create_layer(const sffn_layer_desc* desc, sffn_layer_t* out) {
   if (d.d_model <= 0 || d.d_ff <= 0 || d.rank <= 0)
     return fail(SFFN_ERR_INVALID_ARG, "d_model, d_ff and rank must be positive");
   if (d.max_batch < 1 || d.max_batch > 32) return fail(SFFN_ERR_INVALID_ARG, "max_batch must be in [1, 32]");
-  if (d.flags & ~(SFFN_FLAG_MULTI_KERNEL | SFFN_FLAG_BALANCE | SFFN_FLAG_ROW_GATHER | SFFN_FLAG_STATIC_WEIGHTS))
+  if (d.flags & ~(SFFN_FLAG_MULTI_KERNEL | SFFN_FLAG_BALANCE | SFFN_FLAG_ROW_GATHER | SFFN_FLAG_STATIC_WEIGHTS |
+                  SFFN_FLAG_BUNDLED))
     return fail(SFFN_ERR_INVALID_ARG, "unknown flag bits 0x%x", (unsigned)d.flags);
   const int esize = d.dtype == SFFN_F32 ? 4 : 2;
   if (((size_t)d.d_model * esize) % 16 != 0)
@@ -430,14 +435,20 @@ sffn_status sffn_create_layer(const sffn_layer_desc* desc, sffn_layer_t* out) {
   if (((size_t)d.rank * esize) % 16 != 0)
     return fail(SFFN_ERR_INVALID_ARG, "rank * sizeof(dtype) must be a multiple of 16");
   SFFN_TRY(check_dev_ptr(d.w_up, "w_up"));
-  SFFN_TRY(check_dev_ptr(d.w_downT, "w_downT"));
   SFFN_TRY(check_dev_ptr(d.pred_U, "pred_U"));
   SFFN_TRY(check_dev_ptr(d.pred_V, "pred_V"));
   if (d.pred_b == nullptr) return fail(SFFN_ERR_INVALID_ARG, "pred_b is NULL");
-  if (d.act == SFFN_REGLU) {
-    SFFN_TRY(check_dev_ptr(d.w_gate, "w_gate"));
-  } else if (d.w_gate != nullptr) {
-    return fail(SFFN_ERR_INVALID_ARG, "w_gate must be NULL for ReLU layers");
+  const bool bundled = (d.flags & SFFN_FLAG_BUNDLED) != 0;
+  if (bundled) {
+    if (d.w_gate != nullptr || d.w_downT != nullptr)
+      return fail(SFFN_ERR_INVALID_ARG, "bundled layers pass the bundle as w_up; w_gate and w_downT must be NULL");
+  } else {
+    SFFN_TRY(check_dev_ptr(d.w_downT, "w_downT"));
+    if (d.act == SFFN_REGLU) {
+      SFFN_TRY(check_dev_ptr(d.w_gate, "w_gate"));
+    } else if (d.w_gate != nullptr) {
+      return fail(SFFN_ERR_INVALID_ARG, "w_gate must be NULL for ReLU layers");
+    }
   }
   if (d.rank / (16 / esize) > 256) return fail(SFFN_ERR_UNSUPPORTED, "rank too large for the score kernel");
   if (d.hot_rows < 0 || d.hot_rows > d.d_ff) return fail(SFFN_ERR_INVALID_ARG, "hot_rows outside [0, d_ff]");
@@ -448,6 +459,16 @@ sffn_status sffn_create_layer(const sffn_layer_desc* desc, sffn_layer_t* out) {
   if (L == nullptr) return fail(SFFN_ERR_INVALID_ARG, "out of host memory");
   L->desc = d;
   L->esize = esize;
+  L->wstride = (size_t)d.d_model * esize;
+  if (bundled) {  // neuron i's rows side by side: [gate | up | down] (ReGLU) or [up | down] (ReLU)
+    const unsigned char* bnd = static_cast<const unsigned char*>(d.w_up);
+    const size_t rb = (size_t)d.d_model * esize;
+    const int nm = d.act == SFFN_REGLU ? 2 : 1;
+    L->wstride = (size_t)(nm + 1) * rb;
+    L->desc.w_gate = d.act == SFFN_REGLU ? bnd : nullptr;
+    L->desc.w_up = bnd + (size_t)(nm - 1) * rb;
+    L->desc.w_downT = bnd + (size_t)nm * rb;
+  }
   cudaError_t e = cudaGetDevice(&L->device);
   int optin = 0;
   if (e == cudaSuccess) e = cudaDeviceGetAttribute(&L->sms, cudaDevAttrMultiProcessorCount, L->device);
@@ -880,6 +901,31 @@ sffn_status sffn_permute_rows(const void* src, void* dst, const int32_t* perm, i
   return SFFN_OK;
 }
 
+sffn_status sffn_bundle_rows(const void* w_up, const void* w_gate, const void* w_downT, int32_t d_ff,
+                             int32_t d_model, int32_t dtype, void* bundle, void* stream) {
+  g_err.clear();
+  if (dtype != SFFN_F32 && dtype != SFFN_F16 && dtype != SFFN_BF16)
+    return fail(SFFN_ERR_INVALID_ARG, "unknown dtype %d", dtype);
+  const size_t esize = dtype == SFFN_F32 ? 4 : 2;
+  if (d_ff < 1 || d_model < 1 || ((size_t)d_model * esize) % 16 != 0)
+    return fail(SFFN_ERR_INVALID_ARG, "bad d_ff/d_model (d_model * sizeof(dtype) must be a multiple of 16)");
+  SFFN_TRY(check_dev_ptr(w_up, "w_up"));
+  SFFN_TRY(check_dev_ptr(w_downT, "w_downT"));
+  SFFN_TRY(check_dev_ptr(bundle, "bundle"));
+  if (w_gate != nullptr) SFFN_TRY(check_dev_ptr(w_gate, "w_gate"));
+  const size_t rb = (size_t)d_model * esize;
+  const int nrows = w_gate != nullptr ? 3 : 2;
+  const void* src[3] = {w_gate, w_up, w_downT};
+  unsigned char* dst = static_cast<unsigned char*>(bundle);
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  int k = 0;
+  for (int m = w_gate != nullptr ? 0 : 1; m < 3; ++m, ++k)  // matrix m's rows into column block k of the bundle
+    SFFN_CUDA(cudaMemcpy2DAsync(dst + (size_t)k * rb, (size_t)nrows * rb, src[m], rb, rb, (size_t)d_ff,
+                                cudaMemcpyDeviceToDevice, s),
+              "bundle copy");
+  return SFFN_OK;
+}
+
 sffn_status sffn_read_device_status(void* workspace, int32_t* status, void* stream) {
   g_err.clear();
   if (workspace == nullptr || status == nullptr) return fail(SFFN_ERR_INVALID_ARG, "NULL argument");
@@ -980,6 +1026,7 @@ sffn_status sffn_internal_layer_on_scratch(sffn_layer_t L, const void* x, float*
   a.static_weights = (d.flags & SFFN_FLAG_STATIC_WEIGHTS) ? 1 : 0;
   a.prefill = 0;
   a.wait_ns = (uint64_t)g_wait_ns;
+  a.wstride = L->wstride;
   SFFN_CUDA(launch_layer(d.dtype, L->lcfg, a, L->layer_grid, s), "layer launch");
   return SFFN_OK;
 }

@@ -137,7 +137,7 @@ __global__ void __launch_bounds__(kGatherThreads, 1) k_gather(const GatherArgs a
   if (tid == 0) policy = policy_evict_first();
   auto issue = [&](int j) {
     const int s = j % S;
-    const size_t off = (size_t)list[j] * row_bytes;
+    const size_t off = (size_t)list[j] * a.wstride;
     unsigned char* dst = stages + (size_t)s * stage_bytes;
     mbar_arrive_expect_tx(&bars[s], stage_bytes);
     bulk_g2s(dst, gup + off, row_bytes, &bars[s], policy);

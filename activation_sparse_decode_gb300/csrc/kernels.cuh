@@ -62,6 +62,7 @@ struct GatherArgs {
   int nstages;          // pipeline depth (>= 2)
   int list_cap;         // per-block capacity of the local neuron list
   uint64_t wait_ns;
+  size_t wstride;       // bytes from one neuron's row to the next in each weight matrix
 };
 struct GatherConfig {
   int threads, cpt, bt, nstages, list_cap;
@@ -114,6 +115,7 @@ struct LayerArgs {
   const uint32_t* la_in;  // NULL, or [ceil(f/32)] mask words of this call
   uint32_t* la_out;       // [ceil(f/32)] mask words for the next call (zeroed and set here)
   int predict_only;       // 1: only the predictor, into la_out: no rows read, no y (launched without clusters)
+  size_t wstride;         // bytes from one neuron's row to the next in each weight matrix
 };
 struct LayerConfig {
   int cpt, act, nstages, u_smem, hot_stages;
@@ -145,6 +147,7 @@ struct UnionArgs {
   int list_cap;           // >= the most union members one block can get
   size_t ring_bytes;      // shared memory of the copy ring
   uint64_t wait_ns;
+  size_t wstride;         // bytes from one neuron's row to the next in each weight matrix
 };
 constexpr int kUnionThreads = 416;       // 4 epilogue warps, 1 MMA warp, 8 copy warps
 constexpr int kUnionMaxWpt = 4;          // mask words per thread in the union scan

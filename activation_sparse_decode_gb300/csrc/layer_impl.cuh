@@ -177,7 +177,7 @@ __global__ void __launch_bounds__(kLayerThreads, CPT == 3 ? 2 : 1) k_layer(const
   // arrives on the stage barrier when they have landed.  Expected arrivals per
   // phase: one per thread.
   auto fill = [&](int s, int neuron) {
-    const size_t off = (size_t)neuron * row_bytes;
+    const size_t off = (size_t)neuron * a.wstride;
     unsigned char* dst = region + (size_t)s * stage_bytes;
 #pragma unroll
     for (int cq = 0; cq < CPT; ++cq) {
@@ -257,7 +257,7 @@ __global__ void __launch_bounds__(kLayerThreads, CPT == 3 ? 2 : 1) k_layer(const
     const int rlines = (row_bytes + 127) / 128;
     for (int q = tid; q < max(n_hot, nw) * rlines; q += kLayerThreads) {
       const int j = q / rlines, l = q - j * rlines;
-      const size_t off = (size_t)(c + (size_t)j * G) * row_bytes + (size_t)l * 128;
+      const size_t off = (size_t)(c + (size_t)j * G) * a.wstride + (size_t)l * 128;
       prefetch_l2(gup + off);
       if (reglu) prefetch_l2(ggt + off);
       prefetch_l2(gdn + off);

@@ -290,7 +290,7 @@ __global__ void __launch_bounds__(un::kThreads, 1) k_union(UnionArgs a) {
         if (e < KA * per_atom) {
           const int at_i = e / per_atom, rem = e - at_i * per_atom;
           const int m = rem >= R * 8 ? 1 : 0, rem2 = rem - m * R * 8, r = rem2 >> 3, c = rem2 & 7;
-          src[q] = (m ? wg : wu) + (size_t)ti[r] * rowb + c * 16;
+          src[q] = (m ? wg : wu) + (size_t)ti[r] * a.wstride + c * 16;
           dst[q] = at_i * blk + sw128_k(m * R8 + r, c);
           sub[q] = at_i;
           np = q + 1;
@@ -342,7 +342,7 @@ __global__ void __launch_bounds__(un::kThreads, 1) k_union(UnionArgs a) {
         sub[q] = 0;
         if (e < DA * R * 16) {
           const int ot = e / (R * 16), rem = e - ot * R * 16, r = rem >> 4, c16 = rem & 15;
-          src[q] = wd + (size_t)ti[r] * rowb + c16 * 16;
+          src[q] = wd + (size_t)ti[r] * a.wstride + c16 * 16;
           dst[q] = ot * K2 * 256 + sw128_mn(r, c16, K2);
           sub[q] = ot;
           np = q + 1;

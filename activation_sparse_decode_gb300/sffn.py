@@ -51,6 +51,7 @@ SFFN_FLAG_MULTI_KERNEL = 1
 SFFN_FLAG_BALANCE = 2
 SFFN_FLAG_ROW_GATHER = 4
 SFFN_FLAG_STATIC_WEIGHTS = 8
+SFFN_FLAG_BUNDLED = 16
 
 
 def _sig(name, res, *args):
@@ -78,6 +79,7 @@ _c = {
     "hot_first": _sig("sffn_hot_first_perm", _i32, ctypes.POINTER(_i32), _i32, ctypes.POINTER(_i32)),
     "permute": _sig("sffn_permute_rows", _i32, _vp, _vp, _vp, _i32, _i64, _vp),
     "status": _sig("sffn_read_device_status", _i32, _vp, ctypes.POINTER(_i32), _vp),
+    "bundle": _sig("sffn_bundle_rows", _i32, _vp, _vp, _vp, _i32, _i32, _i32, _vp, _vp),
     "debug_wait": _sig("sffn_debug_wait_timeout", _i32, _vp, _sz, _i64, _vp),
     "wait_limit": _sig("sffn_set_wait_limit_ns", _i32, _i64),
     "prof_events": _sig("sffn_set_profile_events", _i32, ctypes.POINTER(_vp), ctypes.POINTER(_vp), _i32),
@@ -92,7 +94,8 @@ EXPORTED = ["sffn_create_layer", "sffn_destroy_layer", "sffn_workspace_size", "s
             "sffn_workspace_init",
             "sffn_predict", "sffn_predict_scores", "sffn_forward", "sffn_dense_forward",
             "sffn_residual_layernorm", "sffn_forward_stack", "sffn_stack_workspace_size",
-            "sffn_profile_counts", "sffn_hot_first_perm", "sffn_permute_rows", "sffn_read_device_status",
+            "sffn_profile_counts", "sffn_hot_first_perm", "sffn_permute_rows", "sffn_bundle_rows",
+            "sffn_read_device_status",
             "sffn_debug_wait_timeout", "sffn_set_wait_limit_ns", "sffn_set_profile_events", "sffn_forward_noalloc", "sffn_noalloc_read_status",
             "sffn_status_string", "sffn_last_error", "sffn_version"]
 
@@ -122,12 +125,16 @@ class Layer:
     """A layer handle plus references to the tensors it borrows."""
 
     def __init__(self, w_up, w_downT, b, U, V, pred_b=None, w_gate=None, tau: float = 0.0, max_batch: int = 1,
-                 flags: int = 0, hot_rows: int = 0, expected_active: float = 0.0, warm_rows: int = 0):
+                 flags: int = 0, hot_rows: int = 0, expected_active: float = 0.0, warm_rows: int = 0,
+                 act: Optional[str] = None):
+        """Bundled layers (flags with SFFN_FLAG_BUNDLED) pass the bundle as
+        w_up, w_downT = w_gate = None and the activation in `act`."""
         self.tensors = [w_up, w_downT, b, U, V, pred_b, w_gate]
-        self.act = "reglu" if w_gate is not None else "relu"
+        self.act = act if act is not None else ("reglu" if w_gate is not None else "relu")
         self.dtype = w_up.dtype
+        nrows = (3 if self.act == "reglu" else 2) if flags & SFFN_FLAG_BUNDLED else 1
         desc = sffn_layer_desc(
-            d_model=w_up.shape[1], d_ff=w_up.shape[0], rank=U.shape[1], max_batch=max_batch,
+            d_model=w_up.shape[1] // nrows, d_ff=w_up.shape[0], rank=U.shape[1], max_batch=max_batch,
             dtype=DTYPE_CODES[w_up.dtype], act=ACT_CODES[self.act],
             w_up=_ptr(w_up), w_gate=_ptr(w_gate), w_downT=_ptr(w_downT), b=_ptr(b),
             pred_U=_ptr(U), pred_V=_ptr(V), pred_b=_ptr(pred_b if pred_b is not None else b), tau=tau,
@@ -140,8 +147,15 @@ class Layer:
 
     @classmethod
     def from_weights(cls, lw, tau: float = 0.0, max_batch: int = 1, flags: int = 0, hot_rows: int = 0,
-                     expected_active: float = 0.0, warm_rows: int = 0) -> "Layer":
-        """From a workloads.LayerWeights already on the GPU."""
+                     expected_active: float = 0.0, warm_rows: int = 0, bundled: bool = False) -> "Layer":
+        """From a workloads.LayerWeights already on the GPU.  bundled: the
+        rows are first copied into the bundled layout (sffn_bundle_rows) and
+        the layer reads that copy."""
+        if bundled:
+            bnd = bundle_rows(lw.w_up, lw.w_gate, lw.w_downT)
+            return cls(bnd, None, lw.b, lw.U, lw.V, pred_b=lw.b, tau=tau, max_batch=max_batch,
+                       flags=flags | SFFN_FLAG_BUNDLED, hot_rows=hot_rows, expected_active=expected_active,
+                       warm_rows=warm_rows, act=lw.act)
         return cls(lw.w_up, lw.w_downT, lw.b, lw.U, lw.V, pred_b=lw.b, w_gate=lw.w_gate, tau=tau,
                    max_batch=max_batch, flags=flags, hot_rows=hot_rows, expected_active=expected_active,
                    warm_rows=warm_rows)
@@ -268,6 +282,22 @@ def sffn_hot_first_perm(counts) -> np.ndarray:
 def sffn_permute_rows(src: torch.Tensor, dst: torch.Tensor, perm: torch.Tensor, stream=None):
     row_bytes = src[0].numel() * src.element_size()
     _check(_c["permute"](_ptr(src), _ptr(dst), _ptr(perm), src.shape[0], row_bytes, _stream(stream)))
+
+
+def sffn_bundle_rows(w_up: torch.Tensor, w_gate: Optional[torch.Tensor], w_downT: torch.Tensor,
+                     bundle: torch.Tensor, stream=None):
+    f, d = w_up.shape
+    _check(_c["bundle"](_ptr(w_up), _ptr(w_gate), _ptr(w_downT), f, d, DTYPE_CODES[w_up.dtype], _ptr(bundle),
+                        _stream(stream)))
+
+
+def bundle_rows(w_up: torch.Tensor, w_gate: Optional[torch.Tensor], w_downT: torch.Tensor, stream=None):
+    """A new [d_ff][(2 or 3) d_model] tensor holding each neuron's rows side by side."""
+    f, d = w_up.shape
+    nrows = 3 if w_gate is not None else 2
+    out = torch.empty(f, nrows * d, dtype=w_up.dtype, device=w_up.device)
+    sffn_bundle_rows(w_up, w_gate, w_downT, out, stream)
+    return out
 
 
 def sffn_read_device_status(ws: torch.Tensor, stream=None) -> int:

@@ -52,9 +52,11 @@ sys.path.insert(0, ROOT)
 WORKLOAD = "c5"
 DEFAULT_STEPS = {"c1": 300, "c2": 300, "c3": 100, "c4": 10, "c5": 20}
 SUITE_STEPS = {"c1": 40, "c2": 40, "c3": 20, "c4": 4, "c5": 3}  # sub-record steps (timed), each after >= 3 warm-up steps
-# (workload, batch, look-ahead masks): the stacks also at batch 1 with look-ahead masks
-SUITE = [("c1", 1, 0), ("c2", 1, 0), ("c3", 1, 0), ("c3", 4, 0), ("c3", 8, 0), ("c3", 32, 0), ("c4", 1, 0),
-         ("c4", 1, 1), ("c5", 8, 0), ("c5", 1, 1)]
+# (workload, batch, variant): the stacks also at batch 1 with look-ahead masks,
+# the ReGLU layer also on the bundled row layout
+SUITE = [("c1", 1, ""), ("c2", 1, ""), ("c3", 1, ""), ("c3", 4, ""), ("c3", 8, ""), ("c3", 32, ""),
+         ("c3", 1, "bundled"), ("c3", 8, "bundled"), ("c3", 32, "bundled"), ("c4", 1, ""), ("c4", 1, "lookahead"),
+         ("c5", 8, ""), ("c5", 1, "lookahead")]
 METRIC = "sparse-FFN decode tokens/s at batch 1 and achieved HBM GB/s vs roofline"
 L2_BYTES = 126 * 2 ** 20
 ESIZE = {"f32": 4, "f16": 2, "bf16": 2}
@@ -72,6 +74,7 @@ def parse():
     p.add_argument("--no-suite", action="store_true", help="headline only, no sub-records")
     p.add_argument("--lookahead", action="store_true",
                    help="stacks at batch 1: look-ahead masks (each layer's mask predicted from the previous input)")
+    p.add_argument("--bundled", action="store_true", help="bundled row layout ([gate | up | down] per neuron)")
     p.add_argument("--row-gather", action="store_true", help="batches: CUDA-core row gather, not the union path")
     p.add_argument("--no-dense", action="store_true", help="skip the dense contrast")
     p.add_argument("--no-stats", action="store_true", help="skip band / recall / precision statistics")
@@ -288,12 +291,23 @@ class Model:
         self.layers = [sffn.Layer.from_weights(x, tau=wl.tau, max_batch=max_batch, flags=flags, hot_rows=h,
                                                expected_active=e)
                        for x, h, e in zip(self.lws, self.hots, self.eas)]
+        self._args = (sffn, max_batch, flags)
+        self.bundled = None
         torch.cuda.synchronize()
 
+    def bundled_layers(self):
+        """The same layers on the bundled row layout (copies of the rows)."""
+        if self.bundled is None:
+            sffn, max_batch, flags = self._args
+            self.bundled = [sffn.Layer.from_weights(x, tau=self.wl.tau, max_batch=max_batch, flags=flags, hot_rows=h,
+                                                    expected_active=e, bundled=True)
+                            for x, h, e in zip(self.lws, self.hots, self.eas)]
+        return self.bundled
+
     def close(self):
-        for l in self.layers:
+        for l in self.layers + (self.bundled or []):
             l.close()
-        self.layers, self.lws = [], []
+        self.layers, self.lws, self.bundled = [], [], None
 
 
 # ---------------------------------------------------------------- statistics outside the timing
@@ -353,7 +367,7 @@ def collect_stats(sffn, torch, model, calls, B, dev):
 # ---------------------------------------------------------------- one measurement
 
 def measure(sffn, W, torch, model, B, steps, warmup, dev, world, args, stats=True, dense=True, want_e2e=False,
-            lookahead=False):
+            variant=""):
     """Times `steps` graph replays of one decode step of `model` at batch B.
     Returns (record, extras) where extras carries what the headline line needs."""
     wl = model.wl
@@ -363,10 +377,10 @@ def measure(sffn, W, torch, model, B, steps, warmup, dev, world, args, stats=Tru
     d, f, r = wl.d_model, wl.d_ff, wl.rank
     esz = ESIZE[wl.dtype]
     nm = 2 if wl.act == "reglu" else 1
-    layers = model.layers
+    layers = model.bundled_layers() if variant == "bundled" else model.layers
     union_path = B >= 3 and wl.dtype != "f32" and d % 128 == 0 and not args.row_gather
     rank, _, _ = dist_env()
-    lookahead = lookahead and stack and B == 1
+    lookahead = variant == "lookahead" and stack and B == 1
     opts = sffn.SFFN_STACK_LOOKAHEAD if lookahead else 0
 
     X = W.make_tokens(wl, T, batch=B, seed=rank, device=dev)  # [T][B][d]
@@ -483,7 +497,7 @@ def measure(sffn, W, torch, model, B, steps, warmup, dev, world, args, stats=Tru
     k_s = k_us / 1e6
     us_per_layer = ms_per_step * 1e3 / (T * L)
     rec = {
-        "workload": wl.name, "batch": B, "layers": L, "decode_steps_per_step": T, "lookahead": lookahead,
+        "workload": wl.name, "batch": B, "layers": L, "decode_steps_per_step": T, "variant": variant or "exact",
         "path": ("tensor-core union" if union_path else "single-launch layer kernel" if B == 1
                  else "CUDA-core row gather"),
         "tokens_per_s": round(value, 1),
@@ -714,12 +728,13 @@ def bench_sffn(args):
     if not args.no_suite:
         names = [n for i, (n, _, _) in enumerate(SUITE) if n != head and n not in [m for m, _, _ in SUITE[:i]]]
         for name in names:  # the headline's workload is measured with its own layers below
-            runs = [(b, la) for n, b, la in SUITE if n == name]
+            runs = [(b, v) for n, b, v in SUITE if n == name]
             m = Model(sffn, W, W.get_workload(name), dev, max(b for b, _ in runs), args.replicas, args.hot_frac,
                       flags)
-            for b, la in runs:
+            for b, v in runs:
                 rec, _ = measure(sffn, W, torch, m, b, SUITE_STEPS[name], 3, dev, world, args,
-                                 stats=not args.no_stats, dense=not args.no_dense, lookahead=bool(la))
+                                 stats=not args.no_stats and v != "bundled", dense=not args.no_dense and not v,
+                                 variant=v)
                 sub.append(rec)
             m.close()
             del m
@@ -731,13 +746,14 @@ def bench_sffn(args):
         wl = wl.with_(n_layers=max(2, min(args.layers, wl.n_layers)))
     max_b = max([B] + [b for n, b, _ in SUITE if n == head and not args.no_suite])
     model = Model(sffn, W, wl, dev, max_b, args.replicas, args.hot_frac, flags)
+    head_variant = "lookahead" if args.lookahead else "bundled" if args.bundled else ""
     rec, ex = measure(sffn, W, torch, model, B, args.steps, args.warmup, dev, world, args,
-                      stats=not args.no_stats, dense=not args.no_dense, want_e2e=True, lookahead=args.lookahead)
+                      stats=not args.no_stats, dense=not args.no_dense, want_e2e=True, variant=head_variant)
     if not args.no_suite:
-        for n, b, la in SUITE:
-            if n == head and (b, bool(la)) != (B, bool(args.lookahead)):
+        for n, b, v in SUITE:
+            if n == head and (b, v) != (B, head_variant):
                 r2, _ = measure(sffn, W, torch, model, b, SUITE_STEPS[n], 3, dev, world, args,
-                                stats=not args.no_stats, dense=not args.no_dense, lookahead=bool(la))
+                                stats=not args.no_stats, dense=not args.no_dense and not v, variant=v)
                 sub.append(r2)
     lw0 = model.lws[0]
 

@@ -144,6 +144,16 @@ typedef struct {
  * them before the wait, so a kernel queued just before the call may still be
  * writing the weights (a reorder, a dequantisation). */
 #define SFFN_FLAG_STATIC_WEIGHTS 8
+/* Bundled rows: neuron i's rows of the FFN matrices are stored side by side
+ * in one matrix, passed as w_up (w_gate and w_downT must be NULL):
+ *   ReGLU: bundle[i] = [ W_gate[i] | W_up[i] | W_down^T[i] ]   ([d_ff][3*d_model])
+ *   ReLU : bundle[i] = [ W_up[i] | W_down^T[i] ]               ([d_ff][2*d_model])
+ * (sffn_bundle_rows builds it).  The rows a neuron needs are then one
+ * contiguous stretch of memory, read as one stream: PowerInfer-2 page, 4.4
+ * "Neuron-Cluster-Level Pipeline" (the i-th neurons of Gate, Up and Down
+ * co-activate in up to 80% of cases, so they are stored together).  Results
+ * are those of the unbundled layer. */
+#define SFFN_FLAG_BUNDLED 16
 
 /* Validates the descriptor and records it with launch settings chosen for the
  * current device.  Allocates only host memory.  Returns INVALID_ARG for bad
@@ -307,6 +317,15 @@ sffn_status sffn_hot_first_perm(const int32_t* counts, int32_t d_ff, int32_t* pe
  * to W_up, W_gate, W_down^T, U and b together. */
 sffn_status sffn_permute_rows(const void* src, void* dst, const int32_t* perm, int32_t rows,
                               int64_t row_bytes, void* stream);
+
+/* Builds the bundled row layout of SFFN_FLAG_BUNDLED on `stream`:
+ * bundle[i] = [W_gate[i] | W_up[i] | W_down^T[i]] when w_gate is given (ReGLU),
+ * [W_up[i] | W_down^T[i]] when it is NULL (ReLU).  All pointers are device
+ * pointers, 16-byte aligned, the matrices [d_ff][d_model] of `dtype`, the
+ * bundle [d_ff][(2 or 3) * d_model], not overlapping them.  Byte copies only
+ * (three strided cudaMemcpy2DAsync). */
+sffn_status sffn_bundle_rows(const void* w_up, const void* w_gate, const void* w_downT, int32_t d_ff,
+                             int32_t d_model, int32_t dtype, void* bundle, void* stream);
 
 /* Synchronises `stream`, copies the workspace status word to *status (an
  * sffn_status value) and clears it. */

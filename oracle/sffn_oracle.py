@@ -33,6 +33,9 @@ What it computes, step by step, in the pages' order:
    "如何充分利用結構化稀疏性進行加速", the DejaVu design): each layer call's
    mask comes from its own predictor applied to the input of the call
    before it, so prediction can overlap the previous layer's work.
+8. Bundled rows: neuron i's rows of Gate, Up and Down stored side by side
+   (PowerInfer-2 page, section 4.4: the i-th neurons of the three matrices
+   co-activate, so they are bundled); a layout, results unchanged.
 7. Offline profile: per-neuron count of predicted activations over profile
    tokens, sorted descending with ties broken by ascending index (hot-first
    order; PowerInfer page, "Fase fuera de linea": the profiler records neuron
@@ -318,6 +321,30 @@ def hot_first_perm(counts: np.ndarray) -> np.ndarray:
     counts = np.asarray(counts)
     order = sorted(range(counts.size), key=lambda i: (-int(counts[i]), i))
     return np.asarray(order, dtype=np.int32)
+
+
+# --------------------------------------------------------------------------
+# bundled row layout
+# --------------------------------------------------------------------------
+
+def bundle_rows(layer: OracleLayer) -> np.ndarray:
+    """Neuron i's rows side by side in one matrix, in the order the
+    PowerInfer-2 page names the matrices whose i-th neurons co-activate
+    (section 4.4, "Neuron-Cluster-Level Pipeline": Gate, Up and Down):
+    [W_gate[i] | W_up[i] | W_down^T[i]] for ReGLU, [W_up[i] | W_down^T[i]]
+    for ReLU.  A storage layout: it changes no result."""
+    parts = ([layer.w_gate] if layer.act == "reglu" else []) + [layer.w_up, layer.w_downT]
+    return np.concatenate([np.asarray(p) for p in parts], axis=1)
+
+
+def unbundle_layer(bundle: np.ndarray, b, U, V, fmt: str, act: str = "relu", tau: float = 0.0) -> OracleLayer:
+    """The layer whose bundled rows are `bundle` (inverse of bundle_rows)."""
+    bundle = np.asarray(bundle)
+    k = 3 if act == "reglu" else 2
+    d = bundle.shape[1] // k
+    cols = [bundle[:, j * d:(j + 1) * d] for j in range(k)]
+    gate = cols[0] if act == "reglu" else None
+    return OracleLayer(w_up=cols[-2], w_downT=cols[-1], b=b, U=U, V=V, fmt=fmt, act=act, w_gate=gate, tau=tau)
 
 
 def permute_layer(layer: OracleLayer, perm: np.ndarray) -> OracleLayer:

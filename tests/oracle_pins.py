@@ -419,6 +419,31 @@ def check_lookahead_fixed_input(o):
             assert ms[t][l].any() and not ms[t][l].all()
 
 
+def check_bundle_layout(o):
+    """The bundled layout written out by hand for a 2-neuron ReGLU layer with
+    d_model 2 (rows [gate | up | down], the page's order Gate, Up, Down) and a
+    ReLU layer ([up | down]); unbundling restores the matrices and the masked
+    FFN of the unbundled layer equals the original's bit for bit."""
+    g = np.array([[1, 2], [3, 4]], np.float32)
+    u = np.array([[5, 6], [7, 8]], np.float32)
+    dn = np.array([[9, 10], [11, 12]], np.float32)
+    lay = o.OracleLayer(w_up=u, w_downT=dn, b=np.zeros(2, np.float32), U=np.ones((2, 1), np.float32),
+                        V=np.ones((1, 2), np.float32), fmt="f32", act="reglu", w_gate=g)
+    bnd = o.bundle_rows(lay)
+    assert bnd.tolist() == [[1, 2, 5, 6, 9, 10], [3, 4, 7, 8, 11, 12]]
+    lay_r = o.OracleLayer(w_up=u, w_downT=dn, b=np.zeros(2, np.float32), U=np.ones((2, 1), np.float32),
+                          V=np.ones((1, 2), np.float32), fmt="f32")
+    assert o.bundle_rows(lay_r).tolist() == [[5, 6, 9, 10], [7, 8, 11, 12]]
+    for act in ("relu", "reglu"):
+        ref = random_layer(o, f=20, d=8, seed=70, act=act, fmt="bf16")
+        ub = o.unbundle_layer(o.bundle_rows(ref), ref.b, ref.U, ref.V, "bf16", act)
+        assert np.array_equal(ub.w_up, ref.w_up) and np.array_equal(ub.w_downT, ref.w_downT)
+        assert act == "relu" or np.array_equal(ub.w_gate, ref.w_gate)
+        x = o.round_to(_rng(71).standard_normal(8), "bf16")
+        m = _rng(72).random(20) < 0.5
+        assert np.array_equal(o.masked_ffn(ub, x, m), o.masked_ffn(ref, x, m))
+
+
 def check_profile_and_perm(o):
     layer = random_layer(o, f=30, seed=40)
     layer.U = np.zeros_like(layer.U)

@@ -424,3 +424,51 @@ def test_boundary_errors(sffn):
     sffn.sffn_forward(layer, x, y, ws)
     torch.cuda.synchronize()
     assert sffn.sffn_read_device_status(ws) == 0
+
+
+# ---------------------------------------------------------------- bundled rows
+
+BUNDLED = [  # (d_model, d_ff, rank, dtype, act, batch): every path on the bundled layout
+    (1024, 3000, 64, "bf16", "reglu", 1),
+    (4096, 11008, 256, "bf16", "reglu", 1),
+    (1024, 3000, 64, "f16", "relu", 2),
+    (1024, 3000, 64, "bf16", "reglu", 8),
+    (2048, 6000, 128, "f16", "relu", 32),
+    (512, 777, 16, "f32", "reglu", 1),
+]
+
+
+@pytest.mark.parametrize("shape", BUNDLED, ids=lambda s: "d%d_f%d_r%d_%s_%s_b%d" % s)
+def test_bundled_rows(sffn, shape):
+    """Layers on the bundled row layout: the bundle holds exactly the oracle's
+    layout (byte for byte), and every path gives the oracle's result and the
+    unbundled layer's (up to the order of atomic adds)."""
+    d, f, r, dt, act, batch = shape
+    wl = W.tiny_workload(d_model=d, d_ff=f, rank=r, dtype=dt, act=act, mean_p=0.12, name=f"bundled{shape}")
+    lw = W.make_layer(wl, device=DEV)
+    ol = oracle_layer(lw)
+    bnd = sffn.bundle_rows(lw.w_up, lw.w_gate, lw.w_downT)
+    torch.cuda.synchronize()
+    assert np.array_equal(st(bnd), oracle.bundle_rows(ol))
+    plain = sffn.Layer.from_weights(lw, max_batch=batch)
+    bl = sffn.Layer(bnd, None, lw.b, lw.U, lw.V, pred_b=lw.b, max_batch=batch, flags=sffn.SFFN_FLAG_BUNDLED,
+                    act=act)
+    X = W.make_tokens(wl, 2, batch=batch, device=DEV)
+    Y, I, N = run_tokens(sffn, bl, X)
+    Yp, Ip, Np = run_tokens(sffn, plain, X)
+    assert np.array_equal(N, Np) and np.array_equal(I, Ip)
+    ob = oracle.unbundle_layer(st(bnd), ol.b, ol.U, ol.V, dt, act)
+    Xh = st(X)
+    for s_ in range(2):
+        for b in range(batch):
+            m = mask_from_list(I[s_, b], N[s_, b], f)
+            check_token(ob, Xh[s_, b], m, Y[s_, b], TOL[dt])
+            check_elementwise(Y[s_, b], Yp[s_, b], dt, "bundled vs unbundled")
+
+
+def test_bundled_rejects_separate_matrices(sffn):
+    wl = W.tiny_workload(d_model=256, d_ff=512, rank=16, dtype="f16", name="bundled-bad")
+    lw = W.make_layer(wl, device=DEV)
+    with pytest.raises(sffn.SffnError) as e:
+        sffn.Layer(lw.w_up, lw.w_downT, lw.b, lw.U, lw.V, flags=sffn.SFFN_FLAG_BUNDLED, act="relu")
+    assert e.value.status == 1

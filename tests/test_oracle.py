@@ -138,10 +138,18 @@ def _mutant_lookahead_restarts_each_step(o):
     o.lookahead_stack_decode = la
 
 
+def _mutant_bundle_up_first(o):
+    def bundle(layer):
+        parts = [layer.w_up] + ([layer.w_gate] if layer.act == "reglu" else []) + [layer.w_downT]
+        return np.concatenate([np.asarray(p) for p in parts], axis=1)
+    o.bundle_rows = bundle
+
+
 MUTANTS = [_mutant_no_bias, _mutant_gate_up_swapped, _mutant_threshold_ge, _mutant_bias_sign,
            _mutant_down_uses_up_rows, _mutant_mask_ignored, _mutant_descending_idx,
            _mutant_unbiased_variance, _mutant_no_residual, _mutant_ties_descending,
-           _mutant_bf16_truncate, _mutant_lookahead_own_input, _mutant_lookahead_restarts_each_step]
+           _mutant_bf16_truncate, _mutant_lookahead_own_input, _mutant_lookahead_restarts_each_step,
+           _mutant_bundle_up_first]
 
 
 @pytest.mark.parametrize("plant", MUTANTS, ids=lambda m: m.__name__[len("_mutant_"):])

@@ -15,7 +15,8 @@ CSRC = os.path.join(HERE, "csrc")
 OUT_DIR = os.path.join(HERE, "_build")
 LIB = os.path.join(HERE, "libsffn.so")
 SOURCES = ["api.cu", "predict.cu", "misc.cu", "gather_f32.cu", "gather_f16.cu", "gather_bf16.cu",
-           "layer_f32.cu", "layer_f16.cu", "layer_bf16.cu", "union_f16.cu", "union_bf16.cu", "noalloc.cu"]
+           "layer_f32.cu", "layer_f16.cu", "layer_bf16.cu", "union_f16.cu", "union_bf16.cu", "noalloc.cu",
+           "dense.cu"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 FLAGS = ["-O3", "-std=c++17", "-lineinfo", "-Xcompiler", "-fPIC", "--expt-relaxed-constexpr",
          "-I", os.path.join(os.path.dirname(HERE), "include")]
@@ -60,7 +61,8 @@ def build(verbose: bool = False, force: bool = False, ptxas_info: bool = False) 
     objs = [os.path.join(OUT_DIR, s.replace(".cu", ".o")) for s in SOURCES]
     if jobs or not os.path.exists(LIB):
         tmp = LIB + ".tmp"
-        r = subprocess.run([nvcc, *ARCH, "-shared", "-o", tmp, *objs, "-lcudart"], capture_output=True, text=True)
+        r = subprocess.run([nvcc, *ARCH, "-shared", "-o", tmp, *objs, "-lcudart", "-lcublasLt"], capture_output=True,
+                           text=True)
         if r.returncode != 0:
             raise RuntimeError(f"link failed:\n{r.stderr}")
         os.replace(tmp, LIB)

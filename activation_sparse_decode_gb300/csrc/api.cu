@@ -11,8 +11,18 @@
 #include <string>
 #include <vector>
 
+#include <cublasLt.h>
+
 #include "../../include/sffn.h"
 #include "kernels.cuh"
+
+// cuBLASLt descriptors of the dense fallback's two GEMMs for one batch size.
+struct DensePlan {
+  bool built = false, ok = false;
+  cublasLtMatmulDesc_t op1 = nullptr, op2 = nullptr;
+  cublasLtMatrixLayout_t w1 = nullptr, x1 = nullptr, d1 = nullptr, w2 = nullptr, a2 = nullptr, y2 = nullptr;
+  cublasLtMatmulAlgo_t algo1{}, algo2{};
+};
 
 using namespace sffn;
 
@@ -39,7 +49,19 @@ struct sffn_layer {
   bool lcfg_ok = false;
   int layer_grid = 0;    // its blocks: two per SM when two fit, else one
   int layer_cluster = 0;  // > 1: launched in clusters of this many blocks (every cluster co-resident)
+  cublasLtHandle_t lt = nullptr;  // dense fallback (created when the layer enables it)
+  DensePlan plans[33];            // per batch size
   bool fused() const { return lcfg_ok && !(desc.flags & SFFN_FLAG_MULTI_KERNEL); }
+  bool dense_for(int batch) const { return lt != nullptr && batch >= desc.dense_min_batch; }
+  ~sffn_layer() {
+    for (auto& p : plans) {
+      if (p.op1) cublasLtMatmulDescDestroy(p.op1);
+      if (p.op2) cublasLtMatmulDescDestroy(p.op2);
+      for (auto l : {p.w1, p.x1, p.d1, p.w2, p.a2, p.y2})
+        if (l) cublasLtMatrixLayoutDestroy(l);
+    }
+    if (lt) cublasLtDestroy(lt);
+  }
 };
 
 namespace {
@@ -76,8 +98,11 @@ size_t align_up(size_t v, size_t a) { return (v + a - 1) / a * a; }
 int bt_slot(int bt) { return bt == 1 ? 0 : bt == 2 ? 1 : 2; }
 
 struct WsLayout {
-  size_t hdr, flags, tickets, h_part, h, h3, mask, y_part, hl_part, bal_counts, bal_lists, total;
+  size_t hdr, flags, tickets, h_part, h, h3, mask, y_part, hl_part, bal_counts, bal_lists;
+  size_t dn_up, dn_gate, dn_a, dn_y2, dn_lt, total;  // dense fallback
 };
+
+constexpr size_t kLtWorkspace = 16u << 20;  // cuBLASLt workspace of the dense fallback
 
 WsLayout layout(const sffn_layer* L, int batch) {
   const auto& d = L->desc;
@@ -102,6 +127,12 @@ WsLayout layout(const sffn_layer* L, int batch) {
   const size_t lown_cap = L->layer_grid > 0 ? (size_t)(d.d_ff + L->layer_grid - 1) / L->layer_grid : own_cap;
   w.bal_counts = take(L->lcfg_ok ? (size_t)lg * sizeof(uint64_t) : 0);
   w.bal_lists = take(L->lcfg_ok ? (size_t)lg * std::max(own_cap, lown_cap) * 2 * sizeof(int32_t) : 0);
+  const bool dn = L->dense_for(batch);
+  w.dn_up = take(dn ? (size_t)batch * d.d_ff * sizeof(float) : 0);
+  w.dn_gate = take(dn && d.act == SFFN_REGLU ? (size_t)batch * d.d_ff * sizeof(float) : 0);
+  w.dn_a = take(dn ? (size_t)2 * batch * d.d_ff * L->esize : 0);
+  w.dn_y2 = take(dn ? (size_t)2 * batch * d.d_model * sizeof(float) : 0);
+  w.dn_lt = take(dn ? kLtWorkspace : 0);
   w.total = off;
   return w;
 }
@@ -120,6 +151,11 @@ struct Ws {
   unsigned long long* hl_slots() const { return reinterpret_cast<unsigned long long*>(base + lay.hl_part); }
   uint64_t* bal_counts() const { return reinterpret_cast<uint64_t*>(base + lay.bal_counts); }
   int32_t* bal_lists() const { return reinterpret_cast<int32_t*>(base + lay.bal_lists); }
+  float* dn_up() const { return reinterpret_cast<float*>(base + lay.dn_up); }
+  float* dn_gate() const { return reinterpret_cast<float*>(base + lay.dn_gate); }
+  void* dn_a() const { return base + lay.dn_a; }
+  float* dn_y2() const { return reinterpret_cast<float*>(base + lay.dn_y2); }
+  void* dn_lt() const { return base + lay.dn_lt; }
 };
 
 sffn_status check_ws(const sffn_layer* L, int batch, void* ws, size_t bytes, Ws* out) {
@@ -266,8 +302,88 @@ bool use_union(const sffn_layer* L, int batch, UnionConfig* cfg) {
   return union_config(d.dtype, d.act, d.d_model, d.d_ff, batch, L->gather_grid, L->smem_optin, cfg);
 }
 
+// The dense fallback's cuBLASLt plan for `batch` tokens, built on first use
+// (host-side descriptors and a heuristic query only).
+sffn_status dense_plan(sffn_layer* L, int batch, DensePlan** out) {
+  DensePlan& p = L->plans[batch];
+  *out = &p;
+  if (p.built) return p.ok ? SFFN_OK : fail(SFFN_ERR_UNSUPPORTED, "no cuBLASLt algorithm for the dense fallback");
+  p.built = true;
+  const auto& d = L->desc;
+  const cudaDataType_t wt = d.dtype == SFFN_BF16 ? CUDA_R_16BF : CUDA_R_16F;
+  const uint64_t ldw = L->wstride / L->esize;
+  const cublasOperation_t opT = CUBLAS_OP_T, opN = CUBLAS_OP_N;
+  bool ok = cublasLtMatmulDescCreate(&p.op1, CUBLAS_COMPUTE_32F, CUDA_R_32F) == CUBLAS_STATUS_SUCCESS &&
+            cublasLtMatmulDescSetAttribute(p.op1, CUBLASLT_MATMUL_DESC_TRANSA, &opT, sizeof(opT)) ==
+                CUBLAS_STATUS_SUCCESS &&
+            cublasLtMatmulDescSetAttribute(p.op1, CUBLASLT_MATMUL_DESC_TRANSB, &opN, sizeof(opN)) ==
+                CUBLAS_STATUS_SUCCESS &&
+            cublasLtMatmulDescCreate(&p.op2, CUBLAS_COMPUTE_32F, CUDA_R_32F) == CUBLAS_STATUS_SUCCESS &&
+            // column-major views of the row-major arrays:
+            // W (d x f, ld ldw), X (d x B), D (f x B); W_down^T (d x f), A (f x 2B), Y2 (d x 2B)
+            cublasLtMatrixLayoutCreate(&p.w1, wt, d.d_model, d.d_ff, ldw) == CUBLAS_STATUS_SUCCESS &&
+            cublasLtMatrixLayoutCreate(&p.x1, wt, d.d_model, batch, d.d_model) == CUBLAS_STATUS_SUCCESS &&
+            cublasLtMatrixLayoutCreate(&p.d1, CUDA_R_32F, d.d_ff, batch, d.d_ff) == CUBLAS_STATUS_SUCCESS &&
+            cublasLtMatrixLayoutCreate(&p.w2, wt, d.d_model, d.d_ff, ldw) == CUBLAS_STATUS_SUCCESS &&
+            cublasLtMatrixLayoutCreate(&p.a2, wt, d.d_ff, 2 * batch, d.d_ff) == CUBLAS_STATUS_SUCCESS &&
+            cublasLtMatrixLayoutCreate(&p.y2, CUDA_R_32F, d.d_model, 2 * batch, d.d_model) == CUBLAS_STATUS_SUCCESS;
+  cublasLtMatmulPreference_t pref = nullptr;
+  if (ok) {
+    const uint64_t wsb = kLtWorkspace;
+    const uint32_t align = 16;  // tokens may start on any 16-byte boundary
+    ok = cublasLtMatmulPreferenceCreate(&pref) == CUBLAS_STATUS_SUCCESS &&
+         cublasLtMatmulPreferenceSetAttribute(pref, CUBLASLT_MATMUL_PREF_MAX_WORKSPACE_BYTES, &wsb, sizeof(wsb)) ==
+             CUBLAS_STATUS_SUCCESS;
+    for (auto attr : {CUBLASLT_MATMUL_PREF_MIN_ALIGNMENT_A_BYTES, CUBLASLT_MATMUL_PREF_MIN_ALIGNMENT_B_BYTES,
+                      CUBLASLT_MATMUL_PREF_MIN_ALIGNMENT_C_BYTES, CUBLASLT_MATMUL_PREF_MIN_ALIGNMENT_D_BYTES})
+      ok = ok && cublasLtMatmulPreferenceSetAttribute(pref, attr, &align, sizeof(align)) == CUBLAS_STATUS_SUCCESS;
+  }
+  if (ok) {
+    cublasLtMatmulHeuristicResult_t r1{}, r2{};
+    int n1 = 0, n2 = 0;
+    ok = cublasLtMatmulAlgoGetHeuristic(L->lt, p.op1, p.w1, p.x1, p.d1, p.d1, pref, 1, &r1, &n1) ==
+             CUBLAS_STATUS_SUCCESS && n1 > 0 &&
+         cublasLtMatmulAlgoGetHeuristic(L->lt, p.op2, p.w2, p.a2, p.y2, p.y2, pref, 1, &r2, &n2) ==
+             CUBLAS_STATUS_SUCCESS && n2 > 0;
+    if (ok) {
+      p.algo1 = r1.algo;
+      p.algo2 = r2.algo;
+    }
+  }
+  if (pref) cublasLtMatmulPreferenceDestroy(pref);
+  p.ok = ok;
+  return ok ? SFFN_OK : fail(SFFN_ERR_UNSUPPORTED, "no cuBLASLt algorithm for the dense fallback");
+}
+
+// Dense fallback: every row of the layer through two tensor-core GEMMs, the
+// tokens' masks applied between them (dense.cu).
+sffn_status run_dense_ffn(const sffn_layer* Lc, const void* x, int batch, float* y, const Ws& ws, cudaStream_t s) {
+  sffn_layer* L = const_cast<sffn_layer*>(Lc);  // plans are built lazily
+  const auto& d = L->desc;
+  DensePlan* p = nullptr;
+  SFFN_TRY(dense_plan(L, batch, &p));
+  const float one = 1.f, zero = 0.f;
+  auto gemm1 = [&](const void* w, float* out) {
+    return cublasLtMatmul(L->lt, p->op1, &one, w, p->w1, x, p->x1, &zero, out, p->d1, out, p->d1, &p->algo1,
+                          ws.dn_lt(), kLtWorkspace, s);
+  };
+  if (gemm1(d.w_up, ws.dn_up()) != CUBLAS_STATUS_SUCCESS)
+    return fail(SFFN_ERR_CUDA, "dense fallback: up GEMM failed");
+  if (d.act == SFFN_REGLU && gemm1(d.w_gate, ws.dn_gate()) != CUBLAS_STATUS_SUCCESS)
+    return fail(SFFN_ERR_CUDA, "dense fallback: gate GEMM failed");
+  SFFN_CUDA(launch_dense_act(d.dtype, ws.dn_up(), d.act == SFFN_REGLU ? ws.dn_gate() : nullptr, d.b, ws.mask(), batch,
+                             d.d_ff, L->W, ws.dn_a(), s),
+            "dense activation launch");
+  if (cublasLtMatmul(L->lt, p->op2, &one, d.w_downT, p->w2, ws.dn_a(), p->a2, &zero, ws.dn_y2(), p->y2, ws.dn_y2(),
+                     p->y2, &p->algo2, ws.dn_lt(), kLtWorkspace, s) != CUBLAS_STATUS_SUCCESS)
+    return fail(SFFN_ERR_CUDA, "dense fallback: down GEMM failed");
+  SFFN_CUDA(launch_dense_combine(ws.dn_y2(), batch, d.d_model, y, s), "dense combine launch");
+  return SFFN_OK;
+}
+
 // The sparse products of a batch whose mask words are in the workspace.
 sffn_status run_sparse_ffn(const sffn_layer* L, const void* x, int batch, float* y, const Ws& ws, cudaStream_t s) {
+  if (L->dense_for(batch)) return run_dense_ffn(L, x, batch, y, ws, s);
   UnionConfig uc{};
   if (!use_union(L, batch, &uc)) return run_gather(L, x, batch, y, ws, false, s);
   const auto& d = L->desc;
@@ -454,6 +570,10 @@ sffn_status sffn_create_layer(const sffn_layer_desc* desc, sffn_layer_t* out) {
   if (d.hot_rows < 0 || d.hot_rows > d.d_ff) return fail(SFFN_ERR_INVALID_ARG, "hot_rows outside [0, d_ff]");
   if (d.warm_rows < 0 || d.warm_rows > d.d_ff) return fail(SFFN_ERR_INVALID_ARG, "warm_rows outside [0, d_ff]");
   if (!(d.expected_active >= 0.f)) return fail(SFFN_ERR_INVALID_ARG, "expected_active must be >= 0");
+  if (d.dense_min_batch < 0 || d.dense_min_batch > 32)
+    return fail(SFFN_ERR_INVALID_ARG, "dense_min_batch outside [0, 32]");
+  if (d.dense_min_batch > 0 && (d.dtype == SFFN_F32 || d.dense_min_batch < 2))
+    return fail(SFFN_ERR_UNSUPPORTED, "the dense fallback takes 16-bit weights and batches of 2 or more");
 
   sffn_layer* L = new (std::nothrow) sffn_layer();
   if (L == nullptr) return fail(SFFN_ERR_INVALID_ARG, "out of host memory");
@@ -546,6 +666,10 @@ sffn_status sffn_create_layer(const sffn_layer_desc* desc, sffn_layer_t* out) {
                                layer_max_clusters(d.dtype, L->lcfg, L->layer_grid, 2) * 2 >= L->layer_grid
                            ? 2
                            : 0;
+  }
+  if (d.dense_min_batch > 0 && cublasLtCreate(&L->lt) != CUBLAS_STATUS_SUCCESS) {
+    delete L;
+    return fail(SFFN_ERR_CUDA, "cublasLtCreate failed");
   }
   *out = L;
   return SFFN_OK;

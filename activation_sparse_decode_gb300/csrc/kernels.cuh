@@ -189,4 +189,11 @@ cudaError_t launch_permute_rows(const void* src, void* dst, const int32_t* perm,
 // ---- test hook: a barrier wait that cannot complete
 cudaError_t launch_wait_timeout(WsHeader* hdr, uint32_t* flags, uint64_t limit_ns, cudaStream_t s);
 
+// ---- dense fallback (every row, two library GEMMs): the masked activation
+// between them (16-bit high part and remainder, [2B][f]) and the sum of the
+// two halves of the second product into y
+cudaError_t launch_dense_act(int dtype, const float* d_up, const float* d_gate, const float* bias,
+                             const uint32_t* mask, int B, int f, int W, void* A, cudaStream_t s);
+cudaError_t launch_dense_combine(const float* y2, int B, int d, float* y, cudaStream_t s);
+
 }  // namespace sffn

@@ -113,12 +113,12 @@ __device__ __forceinline__ void pack_store<__nv_bfloat16>(__nv_bfloat16* dst, co
   *reinterpret_cast<uint4*>(dst) = *reinterpret_cast<const uint4*>(o);
 }
 
-// The three-chunk form (d_model up to 6144 for 16-bit weights) is held to
-// two blocks per SM worth of registers: uncapped it needs 139, and the
-// OPT-13B-shaped layer then runs one block per SM, 2.4% slower.  The smaller
-// forms fit two blocks per SM uncapped; the larger ones run one.
+// The forms up to three chunks (d_model up to 6144 for 16-bit weights) are
+// held to two blocks per SM worth of registers (128): uncapped the three-chunk
+// form needs 139, and the OPT-13B-shaped layer then runs one block per SM,
+// 2.4% slower.  The larger forms run one block per SM.
 template <typename T, int CPT, int ACT>
-__global__ void __launch_bounds__(kLayerThreads, CPT == 3 ? 2 : 1) k_layer(const LayerArgs a) {
+__global__ void __launch_bounds__(kLayerThreads, CPT <= 3 ? 2 : 1) k_layer(const LayerArgs a) {
   constexpr int CPL = 4;  // up to 4 16-byte chunks of a U row per lane (rank <= 128 * elements per chunk)
   constexpr int E = Chunk<T>::N;
   constexpr int ES = sizeof(T);
@@ -356,44 +356,50 @@ __global__ void __launch_bounds__(kLayerThreads, CPT == 3 ? 2 : 1) k_layer(const
       if (ch < NCH) reinterpret_cast<uint4*>(xs)[ch] = xreg[cq];
     }
   } else {
+    // x_prev + y_prev is read once into registers (every chunk's loads in
+    // flight together); mean and biased variance by two block sums over them
     const T* xp = static_cast<const T*>(a.x);
-    auto load = [&](int ch, float* v) {
-      unpack<T>(*reinterpret_cast<const uint4*>(xp + ch * E), v);
-      const float4* yp = reinterpret_cast<const float4*>(a.y_prev + ch * E);
-#pragma unroll
-      for (int e = 0; e < E; e += 4) {
-        const float4 q = __ldcg(&yp[e / 4]);
-        v[e] += q.x; v[e + 1] += q.y; v[e + 2] += q.z; v[e + 3] += q.w;
-      }
-    };
+    float v[CPT][E];
     float s = 0.f;
-    for (int ch = tid; ch < NCH; ch += kLayerThreads) {
-      float v[E];
-      load(ch, v);
 #pragma unroll
-      for (int e = 0; e < E; ++e) s += v[e];
+    for (int cq = 0; cq < CPT; ++cq) {
+      const int ch = tid + cq * kLayerThreads;
+#pragma unroll
+      for (int e = 0; e < E; ++e) v[cq][e] = 0.f;
+      if (ch < NCH) {
+        unpack<T>(*reinterpret_cast<const uint4*>(xp + ch * E), v[cq]);
+        const float4* yp = reinterpret_cast<const float4*>(a.y_prev + ch * E);
+#pragma unroll
+        for (int e = 0; e < E; e += 4) {
+          const float4 q4 = __ldcg(&yp[e / 4]);
+          v[cq][e] += q4.x; v[cq][e + 1] += q4.y; v[cq][e + 2] += q4.z; v[cq][e + 3] += q4.w;
+        }
+      }
+#pragma unroll
+      for (int e = 0; e < E; ++e) s += v[cq][e];
     }
     const float mean = layer_block_sum(s, s_warp) / (float)d;
     float q = 0.f;
-    for (int ch = tid; ch < NCH; ch += kLayerThreads) {
-      float v[E];
-      load(ch, v);
 #pragma unroll
-      for (int e = 0; e < E; ++e) q = fmaf(v[e] - mean, v[e] - mean, q);
-    }
+    for (int cq = 0; cq < CPT; ++cq)
+      if (tid + cq * kLayerThreads < NCH)
+#pragma unroll
+        for (int e = 0; e < E; ++e) q = fmaf(v[cq][e] - mean, v[cq][e] - mean, q);
     const float var = layer_block_sum(q, s_warp) / (float)d;
     const float rstd = 1.0f / sqrtf(var + a.ln_eps);
-    for (int ch = tid; ch < NCH; ch += kLayerThreads) {
-      float v[E];
-      load(ch, v);
 #pragma unroll
-      for (int e = 0; e < E; ++e) {
-        float o = (v[e] - mean) * rstd;
-        if (a.ln_gamma != nullptr) o *= a.ln_gamma[ch * E + e];
-        if (a.ln_beta != nullptr) o += a.ln_beta[ch * E + e];
-        v[e] = o;
+    for (int cq = 0; cq < CPT; ++cq) {
+      const int ch = tid + cq * kLayerThreads;
+      if (ch < NCH) {
+#pragma unroll
+        for (int e = 0; e < E; ++e) {
+          float o = (v[cq][e] - mean) * rstd;
+          if (a.ln_gamma != nullptr) o *= a.ln_gamma[ch * E + e];
+          if (a.ln_beta != nullptr) o += a.ln_beta[ch * E + e];
+          v[cq][e] = o;
+        }
+        pack_store<T>(xs + ch * E, v[cq]);
       }
-      pack_store<T>(xs + ch * E, v);
     }
   }
   __syncthreads();
@@ -706,25 +712,36 @@ __global__ void __launch_bounds__(kLayerThreads, CPT == 3 ? 2 : 1) k_layer(const
       for (int e = 0; e < E; ++e) hreg[cc][e] = ch < NC ? hs[ch * E + e] : 0.f;
     }
     const T* Ug = static_cast<const T*>(a.U);
+    // rows in batches of UB, every load of a batch issued before any is used
+    // (each row is an L2 round trip otherwise); wide forms have the registers
+    constexpr int UB = CPT >= 4 ? 8 : 2;
     for (int q = warp; q < nwords; q += kLayerWarps) {
       const int kn = min(32, n_own - q * 32);
       float mine = 0.f;
-#pragma unroll 2
-      for (int k = 0; k < kn; ++k) {
-        const int j = q * 32 + k;
-        float acc = 0.f;
+      for (int k0 = 0; k0 < kn; k0 += UB) {
+        uint4 raw[UB][CPL];
 #pragma unroll
-        for (int cc = 0; cc < CPL; ++cc) {
-          const int ch = lane + 32 * cc;
-          if (ch < NC) {
+        for (int u = 0; u < UB; ++u)
+#pragma unroll
+          for (int cc = 0; cc < CPL; ++cc) {
+            const int ch = lane + 32 * cc;
+            const int j = q * 32 + k0 + u;
+            raw[u][cc] = k0 + u < kn && ch < NC ? ldg_stream(Ug + (size_t)(c + (size_t)j * G) * r + ch * E)
+                                                : make_uint4(0, 0, 0, 0);
+          }
+#pragma unroll
+        for (int u = 0; u < UB; ++u) {
+          float acc = 0.f;
+#pragma unroll
+          for (int cc = 0; cc < CPL; ++cc) {
             float w[E];
-            unpack<T>(ldg_stream(Ug + (size_t)(c + (size_t)j * G) * r + ch * E), w);
+            unpack<T>(raw[u][cc], w);
 #pragma unroll
             for (int e = 0; e < E; ++e) acc = fmaf(w[e], hreg[cc][e], acc);
           }
+          acc = warp_sum(acc);
+          if (lane == k0 + u) mine = acc;
         }
-        acc = warp_sum(acc);
-        if (lane == k) mine = acc;
       }
       const int j = q * 32 + lane;
       const bool act = lane < kn && (mine + ownpb[lane < kn ? j : 0]) > a.tau;

@@ -45,7 +45,8 @@ class sffn_layer_desc(ctypes.Structure):
                 ("dtype", _i32), ("act", _i32),
                 ("w_up", _vp), ("w_gate", _vp), ("w_downT", _vp), ("b", _vp),
                 ("pred_U", _vp), ("pred_V", _vp), ("pred_b", _vp), ("tau", ctypes.c_float), ("flags", _i32),
-                ("hot_rows", _i32), ("expected_active", ctypes.c_float), ("warm_rows", _i32)]
+                ("hot_rows", _i32), ("expected_active", ctypes.c_float), ("warm_rows", _i32),
+                ("dense_min_batch", _i32)]
 
 SFFN_FLAG_MULTI_KERNEL = 1
 SFFN_FLAG_BALANCE = 2
@@ -126,7 +127,7 @@ class Layer:
 
     def __init__(self, w_up, w_downT, b, U, V, pred_b=None, w_gate=None, tau: float = 0.0, max_batch: int = 1,
                  flags: int = 0, hot_rows: int = 0, expected_active: float = 0.0, warm_rows: int = 0,
-                 act: Optional[str] = None):
+                 act: Optional[str] = None, dense_min_batch: int = 0):
         """Bundled layers (flags with SFFN_FLAG_BUNDLED) pass the bundle as
         w_up, w_downT = w_gate = None and the activation in `act`."""
         self.tensors = [w_up, w_downT, b, U, V, pred_b, w_gate]
@@ -138,7 +139,8 @@ class Layer:
             dtype=DTYPE_CODES[w_up.dtype], act=ACT_CODES[self.act],
             w_up=_ptr(w_up), w_gate=_ptr(w_gate), w_downT=_ptr(w_downT), b=_ptr(b),
             pred_U=_ptr(U), pred_V=_ptr(V), pred_b=_ptr(pred_b if pred_b is not None else b), tau=tau,
-            flags=flags, hot_rows=hot_rows, expected_active=expected_active, warm_rows=warm_rows)
+            flags=flags, hot_rows=hot_rows, expected_active=expected_active, warm_rows=warm_rows,
+            dense_min_batch=dense_min_batch)
         self.desc = desc
         h = ctypes.c_void_p()
         _check(_c["create"](ctypes.byref(desc), ctypes.byref(h)))
@@ -147,7 +149,8 @@ class Layer:
 
     @classmethod
     def from_weights(cls, lw, tau: float = 0.0, max_batch: int = 1, flags: int = 0, hot_rows: int = 0,
-                     expected_active: float = 0.0, warm_rows: int = 0, bundled: bool = False) -> "Layer":
+                     expected_active: float = 0.0, warm_rows: int = 0, bundled: bool = False,
+                     dense_min_batch: int = 0) -> "Layer":
         """From a workloads.LayerWeights already on the GPU.  bundled: the
         rows are first copied into the bundled layout (sffn_bundle_rows) and
         the layer reads that copy."""
@@ -155,10 +158,10 @@ class Layer:
             bnd = bundle_rows(lw.w_up, lw.w_gate, lw.w_downT)
             return cls(bnd, None, lw.b, lw.U, lw.V, pred_b=lw.b, tau=tau, max_batch=max_batch,
                        flags=flags | SFFN_FLAG_BUNDLED, hot_rows=hot_rows, expected_active=expected_active,
-                       warm_rows=warm_rows, act=lw.act)
+                       warm_rows=warm_rows, act=lw.act, dense_min_batch=dense_min_batch)
         return cls(lw.w_up, lw.w_downT, lw.b, lw.U, lw.V, pred_b=lw.b, w_gate=lw.w_gate, tau=tau,
                    max_batch=max_batch, flags=flags, hot_rows=hot_rows, expected_active=expected_active,
-                   warm_rows=warm_rows)
+                   warm_rows=warm_rows, dense_min_batch=dense_min_batch)
 
     def close(self):
         if getattr(self, "handle", None):

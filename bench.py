@@ -53,10 +53,12 @@ WORKLOAD = "c5"
 DEFAULT_STEPS = {"c1": 300, "c2": 300, "c3": 100, "c4": 10, "c5": 20}
 SUITE_STEPS = {"c1": 40, "c2": 40, "c3": 20, "c4": 4, "c5": 3}  # sub-record steps (timed), each after >= 3 warm-up steps
 # (workload, batch, variant): the stacks also at batch 1 with look-ahead masks,
-# the ReGLU layer also on the bundled row layout
+# the ReGLU layer also on the bundled row layout, the batches also through the
+# dense fallback (every row, two GEMMs)
 SUITE = [("c1", 1, ""), ("c2", 1, ""), ("c3", 1, ""), ("c3", 4, ""), ("c3", 8, ""), ("c3", 32, ""),
-         ("c3", 1, "bundled"), ("c3", 8, "bundled"), ("c3", 32, "bundled"), ("c4", 1, ""), ("c4", 1, "lookahead"),
-         ("c5", 8, ""), ("c5", 1, "lookahead")]
+         ("c3", 1, "bundled"), ("c3", 8, "bundled"), ("c3", 32, "bundled"), ("c3", 4, "dense"), ("c3", 8, "dense"),
+         ("c3", 32, "dense"), ("c4", 1, ""), ("c4", 1, "lookahead"), ("c5", 8, ""), ("c5", 8, "dense"),
+         ("c5", 1, "lookahead")]
 METRIC = "sparse-FFN decode tokens/s at batch 1 and achieved HBM GB/s vs roofline"
 L2_BYTES = 126 * 2 ** 20
 ESIZE = {"f32": 4, "f16": 2, "bf16": 2}
@@ -293,7 +295,17 @@ class Model:
                        for x, h, e in zip(self.lws, self.hots, self.eas)]
         self._args = (sffn, max_batch, flags)
         self.bundled = None
+        self.dense = None
         torch.cuda.synchronize()
+
+    def dense_layers(self):
+        """The same weights with the dense fallback for every batch of 2 or more."""
+        if self.dense is None:
+            sffn, max_batch, flags = self._args
+            self.dense = [sffn.Layer.from_weights(x, tau=self.wl.tau, max_batch=max_batch, flags=flags, hot_rows=h,
+                                                  expected_active=e, dense_min_batch=2)
+                          for x, h, e in zip(self.lws, self.hots, self.eas)]
+        return self.dense
 
     def bundled_layers(self):
         """The same layers on the bundled row layout (copies of the rows)."""
@@ -305,9 +317,9 @@ class Model:
         return self.bundled
 
     def close(self):
-        for l in self.layers + (self.bundled or []):
+        for l in self.layers + (self.bundled or []) + (self.dense or []):
             l.close()
-        self.layers, self.lws, self.bundled = [], [], None
+        self.layers, self.lws, self.bundled, self.dense = [], [], None, None
 
 
 # ---------------------------------------------------------------- statistics outside the timing
@@ -377,8 +389,10 @@ def measure(sffn, W, torch, model, B, steps, warmup, dev, world, args, stats=Tru
     d, f, r = wl.d_model, wl.d_ff, wl.rank
     esz = ESIZE[wl.dtype]
     nm = 2 if wl.act == "reglu" else 1
-    layers = model.bundled_layers() if variant == "bundled" else model.layers
-    union_path = B >= 3 and wl.dtype != "f32" and d % 128 == 0 and not args.row_gather
+    layers = (model.bundled_layers() if variant == "bundled" else model.dense_layers() if variant == "dense"
+              else model.layers)
+    dense_path = variant == "dense" and B >= 2
+    union_path = B >= 3 and wl.dtype != "f32" and d % 128 == 0 and not args.row_gather and not dense_path
     rank, _, _ = dist_env()
     lookahead = variant == "lookahead" and stack and B == 1
     opts = sffn.SFFN_STACK_LOOKAHEAD if lookahead else 0
@@ -436,6 +450,8 @@ def measure(sffn, W, torch, model, B, steps, warmup, dev, world, args, stats=Tru
         launches_per_step = T * L + (1 if stack else 0) + (1 if lookahead else 0)
     elif union_path:  # hidden layer, scores (one launch each for the whole batch), union kernel
         launches_per_step = T * L * (3 + (1 if stack else 0))
+    elif dense_path:  # hidden layer, scores, activation, combine (the two GEMMs are library kernels)
+        launches_per_step = T * L * (4 + (1 if stack else 0))
     else:
         launches_per_step = T * L * (2 * groups + (B + 3) // 4 + (1 if stack else 0))
 
@@ -467,7 +483,10 @@ def measure(sffn, W, torch, model, B, steps, warmup, dev, world, args, stats=Tru
     pred_bytes = (r * d + f * r) * esz + f * 4  # V, U, predictor bias
     io_bytes = B * d * esz + B * d * 4         # tokens in, outputs out
     W_words = (f + 31) // 32
-    if union_path:
+    if dense_path:
+        gathered = float(f) * d * esz * (nm + 1)  # every row
+        kernel_bytes = gathered + B * W_words * 4 + io_bytes
+    elif union_path:
         gathered = float(np.mean(unions)) * d * esz * (nm + 1)
         kernel_bytes = gathered + float(np.mean(unions)) * 4 + B * W_words * 4 + io_bytes  # + gated bias, masks
     else:
@@ -485,6 +504,11 @@ def measure(sffn, W, torch, model, B, steps, warmup, dev, world, args, stats=Tru
         k_p10, k_p90 = (float(np.percentile(us_layer_steps, q)) for q in (10, 90))
         ktiming = ("device-timed graph / launches (per-step p10/p90)" +
                    (", the final LayerNorm launch included" if stack else ""))
+    elif dense_path:
+        kname = "dense fallback (two cuBLASLt GEMMs, masked activation and combine kernels)"
+        k_us = ms / (steps * T * L) * 1e3
+        k_p10, k_p90 = (float(np.percentile(us_layer_steps, q)) for q in (10, 90))
+        ktiming = "device-timed graph / layer calls (predictor included)"
     elif union_path:
         kname = "k_union (union gather-GEMM on tcgen05: up/gate, ReLU/ReGLU, down projection)"
         k_us, k_p10, k_p90 = time_dominant_kernel(sffn, torch, step_body, stream, T * L)
@@ -498,14 +522,14 @@ def measure(sffn, W, torch, model, B, steps, warmup, dev, world, args, stats=Tru
     us_per_layer = ms_per_step * 1e3 / (T * L)
     rec = {
         "workload": wl.name, "batch": B, "layers": L, "decode_steps_per_step": T, "variant": variant or "exact",
-        "path": ("tensor-core union" if union_path else "single-launch layer kernel" if B == 1
-                 else "CUDA-core row gather"),
+        "path": ("dense fallback" if dense_path else "tensor-core union" if union_path
+                 else "single-launch layer kernel" if B == 1 else "CUDA-core row gather"),
         "tokens_per_s": round(value, 1),
         "us_per_layer": round(us_per_layer, 3),
         "us_per_layer_p10": round(float(np.percentile(us_layer_steps, 10)), 3),
         "us_per_layer_p90": round(float(np.percentile(us_layer_steps, 90)), 3),
         "steps": steps, "warmup": warmup,
-        "dominant_kernel": kname.split(" ")[0],
+        "dominant_kernel": kname.split(" (")[0],
         "kernel_us_per_launch": round(k_us, 3),
         "kernel_us_p10": round(k_p10, 3), "kernel_us_p90": round(k_p90, 3),
         "kernel_timing": ktiming,

@@ -112,6 +112,22 @@ typedef struct {
                            Speculative: rows that turn out inactive cost DRAM
                            bandwidth only; results do not depend on it.
                            0 = none; must be in [0, d_ff].                  */
+  int32_t dense_min_batch; /* dense fallback: calls of at least this many
+                           tokens (2..32; 16-bit weights) read EVERY row once,
+                           as two tensor-core GEMMs (cuBLASLt, fp32
+                           accumulation) with each token's predicted mask and
+                           the activation applied between them, instead of
+                           gathering the union of the tokens' active rows.
+                           Worth it once that union covers most of the layer
+                           (the sparsity page, section 工程影響: the benefit of
+                           sparsity decays with the batch; PowerInfer-2 page,
+                           4.1.1: low-sparsity prefill runs every neuron as one
+                           dense cluster).  Results are the masked FFN either
+                           way.  The union is only known on the device after
+                           the predictor, so the switch is by batch size; the
+                           benchmark measures the crossover.  The workspace
+                           grows by the GEMMs' buffers and a 16 MiB cuBLASLt
+                           workspace.  0 = never.                            */
 } sffn_layer_desc;
 
 /* Batch-1 calls normally run the whole layer (predictor, threshold, gather,

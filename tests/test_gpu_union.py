@@ -105,3 +105,49 @@ def test_union_tokens_keep_their_own_neurons(sffn):
     Xh = st(X)
     for b in range(16):
         check_token(ol, Xh[0, b], mask_from_list(I[0, b], N[0, b], wl.d_ff), Y[0, b], TOL["f16"])
+
+
+DENSE = [  # (d_model, d_ff, rank, dtype, act, batch, mean activity)
+    (1024, 4097, 64, "bf16", "reglu", 17, 0.1),
+    (2048, 6000, 128, "f16", "relu", 32, 0.12),
+    (512, 3000, 32, "f16", "relu", 2, 0.3),
+    (12288, 500, 256, "f16", "relu", 8, 0.2),
+    (4096, 11008, 256, "bf16", "reglu", 32, 0.12),
+]
+
+
+@pytest.mark.parametrize("shape", DENSE, ids=lambda s: "d%d_f%d_r%d_%s_%s_b%d_p%g" % s)
+def test_dense_fallback(sffn, shape):
+    """The dense fallback (every row, two tensor-core GEMMs, the tokens' masks
+    between them) against the oracle's masked FFN token by token, and against
+    the union path on the same inputs: the masks are the same predictor's,
+    and each token still keeps only its own neurons."""
+    d, f, r, dt, act, batch, p = shape
+    wl = W.tiny_workload(d_model=d, d_ff=f, rank=r, dtype=dt, act=act, mean_p=p, name=f"dense{shape}")
+    lw = W.make_layer(wl, device=DEV)
+    ol = oracle_layer(lw)
+    dense = sffn.Layer.from_weights(lw, max_batch=batch, dense_min_batch=2)
+    union = sffn.Layer.from_weights(lw, max_batch=batch)
+    X = W.make_tokens(wl, 2, batch=batch, device=DEV)
+    Y, I, N = run_tokens(sffn, dense, X)
+    Yu, Iu, Nu = run_tokens(sffn, union, X)
+    assert np.array_equal(N, Nu) and np.array_equal(I, Iu)
+    Xh = st(X)
+    for s in range(2):
+        for b in range(batch):
+            m = mask_from_list(I[s, b], N[s, b], f)
+            check_token(ol, Xh[s, b], m, Y[s, b], TOL[dt])
+            check_elementwise(Y[s, b], Yu[s, b], dt, "dense fallback vs union path")
+
+
+def test_dense_fallback_bounds(sffn):
+    wl = W.tiny_workload(d_model=256, d_ff=512, rank=16, dtype="f32", name="dense-bad")
+    lw = W.make_layer(wl, device=DEV)
+    with pytest.raises(sffn.SffnError) as e:
+        sffn.Layer.from_weights(lw, max_batch=4, dense_min_batch=2)
+    assert e.value.status == 2
+    wl = W.tiny_workload(d_model=256, d_ff=512, rank=16, dtype="f16", name="dense-bad16")
+    lw = W.make_layer(wl, device=DEV)
+    with pytest.raises(sffn.SffnError) as e:
+        sffn.Layer.from_weights(lw, max_batch=4, dense_min_batch=33)
+    assert e.value.status == 1

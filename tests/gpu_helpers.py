@@ -103,6 +103,19 @@ def mask_from_list(idx_row, n, f):
     return m
 
 
+def same_lists(I1, N1, I2, N2):
+    """Two runs' active lists agree: equal counts, and equal first N entries
+    of every list (entries past a list's count are not written)."""
+    if not np.array_equal(N1, N2):
+        return False
+    I1, I2, N1 = np.asarray(I1), np.asarray(I2), np.asarray(N1)
+    for ix in np.ndindex(N1.shape):
+        n = int(N1[ix])
+        if not np.array_equal(I1[ix][:n], I2[ix][:n]):
+            return False
+    return True
+
+
 def check_token(ol, x_stored, gpu_mask, y_gpu, tol, tau=0.0):
     """One token: mask parity outside the band, output parity over the GPU mask.
     Returns (band size, band neurons decided differently, rel-L2)."""

@@ -9,7 +9,8 @@ import torch
 import oracle
 from activation_sparse_decode_gb300 import workloads as W
 from activation_sparse_decode_gb300.workloads import to_numpy_stored as st
-from gpu_helpers import TOL, check_elementwise, check_token, hot_first, mask_from_list, oracle_layer, rel_l2, run_tokens, ulp_distance
+from gpu_helpers import (TOL, check_elementwise, check_token, hot_first, mask_from_list, oracle_layer, rel_l2, run_tokens,
+                         same_lists, ulp_distance)
 
 pytestmark = pytest.mark.gpu
 
@@ -456,7 +457,7 @@ def test_bundled_rows(sffn, shape):
     X = W.make_tokens(wl, 2, batch=batch, device=DEV)
     Y, I, N = run_tokens(sffn, bl, X)
     Yp, Ip, Np = run_tokens(sffn, plain, X)
-    assert np.array_equal(N, Np) and np.array_equal(I, Ip)
+    assert same_lists(I, N, Ip, Np)
     ob = oracle.unbundle_layer(st(bnd), ol.b, ol.U, ol.V, dt, act)
     Xh = st(X)
     for s_ in range(2):

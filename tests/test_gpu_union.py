@@ -10,7 +10,7 @@ import torch
 import oracle
 from activation_sparse_decode_gb300 import workloads as W
 from activation_sparse_decode_gb300.workloads import to_numpy_stored as st
-from gpu_helpers import TOL, check_elementwise, check_token, mask_from_list, oracle_layer, rel_l2, run_tokens
+from gpu_helpers import TOL, check_elementwise, check_token, mask_from_list, oracle_layer, rel_l2, run_tokens, same_lists
 
 pytestmark = pytest.mark.gpu
 
@@ -49,7 +49,7 @@ def test_union_ragged(sffn, shape):
     X = W.make_tokens(wl, 2, batch=batch, device=DEV)
     Y, I, N = run_tokens(sffn, layer, X)
     Yg, Ig, Ng = run_tokens(sffn, gather, X)
-    assert np.array_equal(N, Ng) and np.array_equal(I, Ig)
+    assert same_lists(I, N, Ig, Ng)
     Xh = st(X)
     for s in range(2):
         for b in range(batch):
@@ -131,7 +131,7 @@ def test_dense_fallback(sffn, shape):
     X = W.make_tokens(wl, 2, batch=batch, device=DEV)
     Y, I, N = run_tokens(sffn, dense, X)
     Yu, Iu, Nu = run_tokens(sffn, union, X)
-    assert np.array_equal(N, Nu) and np.array_equal(I, Iu)
+    assert same_lists(I, N, Iu, Nu)
     Xh = st(X)
     for s in range(2):
         for b in range(batch):

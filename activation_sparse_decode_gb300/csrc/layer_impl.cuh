@@ -598,27 +598,28 @@ __global__ void __launch_bounds__(kLayerThreads, CPT <= 3 ? 2 : 1) k_layer(const
     for (int q = 0; q < 32; ++q)
       if (lane + 32 * q < r) pending |= 1u << q;
     uint64_t t0 = 0;
+    const int nq = (r - lane + 31) / 32;  // this lane's slots
     while (true) {
-      uint32_t left = pending;
-      while (left) {
-        // up to 8 loads in flight, then their checks
-        unsigned long long v[8];
-        int qs[8];
-        int n = 0;
-        while (left && n < 8) {
-          const int q = __ffs(left) - 1;
-          left &= left - 1;
-          qs[n] = q;
-          asm volatile("ld.relaxed.gpu.global.u64 %0, [%1];"
-                       : "=l"(v[n])
-                       : "l"(slots + (size_t)(lane + 32 * q) * kSlotStride)
-                       : "memory");
-          ++n;
+      // batches of PB slots, statically indexed so that the values stay in
+      // registers and every load of a batch is in flight before any check
+      // (the wide forms poll up to 1024 slots: all of a lane's 32 at once)
+      constexpr int PB = CPT >= 4 ? 32 : 16;
+      for (int q0 = 0; q0 < nq; q0 += PB) {
+        unsigned long long v[PB];
+#pragma unroll
+        for (int u = 0; u < PB; ++u) {
+          v[u] = 0ull;
+          if (q0 + u < nq && ((pending >> (q0 + u)) & 1u))
+            asm volatile("ld.relaxed.gpu.global.u64 %0, [%1];"
+                         : "=l"(v[u])
+                         : "l"(slots + (size_t)(lane + 32 * (q0 + u)) * kSlotStride)
+                         : "memory");
         }
-        for (int m = 0; m < n; ++m)
-          if ((uint32_t)(v[m] >> 32) == tag) {
-            hs[lane + 32 * qs[m]] = __uint_as_float((uint32_t)v[m]);
-            pending &= ~(1u << qs[m]);
+#pragma unroll
+        for (int u = 0; u < PB; ++u)
+          if (q0 + u < nq && ((pending >> (q0 + u)) & 1u) && (uint32_t)(v[u] >> 32) == tag) {
+            hs[lane + 32 * (q0 + u)] = __uint_as_float((uint32_t)v[u]);
+            pending &= ~(1u << (q0 + u));
           }
       }
       if (!__any_sync(0xffffffffu, pending != 0)) break;

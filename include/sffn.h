@@ -248,6 +248,17 @@ sffn_status sffn_predict_scores(sffn_layer_t layer, const void* x, int32_t batch
 
 /* The sparse FFN for a batch of decode tokens: predict, compact, gather the
  * active rows, apply ReLU / ReGLU, accumulate the down projection.
+ *
+ * Batch-1 calls on the single-launch kernel (and sffn_forward_stack at batch
+ * 1, and sffn_forward_noalloc) need every block of their grid resident at
+ * once: each block waits (bounded) for values all other blocks publish.
+ * Layer creation checks that the grid fits an otherwise idle GPU; if kernels
+ * of other streams or processes hold SMs while such a call runs, the resident
+ * blocks can wait out the limit (sffn_set_wait_limit_ns): the call then leaves
+ * SFFN_ERR_TIMEOUT in the status word and an incomplete y.  Check the status
+ * (sffn_read_device_status) when the GPU is shared with concurrent work.
+ * The same holds for the row-gather kernel (one grid barrier before its
+ * fixed-order reduction) and, within a block only, for the union kernel. */
  *   y            : [batch][d_model] float32, device (overwritten)
  *   idx_out      : NULL or [batch][d_ff] int32 (as sffn_predict)
  *   n_active_out : NULL or [batch] int32

@@ -258,7 +258,8 @@ sffn_status sffn_predict_scores(sffn_layer_t layer, const void* x, int32_t batch
  * SFFN_ERR_TIMEOUT in the status word and an incomplete y.  Check the status
  * (sffn_read_device_status) when the GPU is shared with concurrent work.
  * The same holds for the row-gather kernel (one grid barrier before its
- * fixed-order reduction) and, within a block only, for the union kernel. */
+ * fixed-order reduction) and, within a block only, for the union kernel.
+ *
  *   y            : [batch][d_model] float32, device (overwritten)
  *   idx_out      : NULL or [batch][d_ff] int32 (as sffn_predict)
  *   n_active_out : NULL or [batch] int32

@@ -54,11 +54,12 @@ DEFAULT_STEPS = {"c1": 300, "c2": 300, "c3": 100, "c4": 10, "c5": 20}
 SUITE_STEPS = {"c1": 40, "c2": 40, "c3": 20, "c4": 4, "c5": 3}  # sub-record steps (timed), each after >= 3 warm-up steps
 # (workload, batch, variant): the stacks also at batch 1 with look-ahead masks,
 # the ReGLU layer also on the bundled row layout, the batches also through the
-# dense fallback (every row, two GEMMs)
-SUITE = [("c1", 1, ""), ("c2", 1, ""), ("c3", 1, ""), ("c3", 4, ""), ("c3", 8, ""), ("c3", 16, ""), ("c3", 32, ""),
+# dense fallback (every row, two GEMMs), the batch-1 layers also with global
+# row balancing
+SUITE = [("c1", 1, ""), ("c2", 1, ""), ("c2", 1, "balanced"), ("c3", 1, ""), ("c3", 4, ""), ("c3", 8, ""), ("c3", 16, ""), ("c3", 32, ""),
          ("c3", 1, "bundled"), ("c3", 8, "bundled"), ("c3", 32, "bundled"), ("c3", 4, "dense"), ("c3", 8, "dense"),
-         ("c3", 16, "dense"), ("c3", 32, "dense"), ("c4", 1, ""), ("c4", 1, "lookahead"), ("c5", 8, ""),
-         ("c5", 8, "dense"), ("c5", 1, "lookahead")]
+         ("c3", 16, "dense"), ("c3", 32, "dense"), ("c4", 1, ""), ("c4", 1, "lookahead"), ("c4", 1, "balanced"),
+         ("c5", 8, ""), ("c5", 8, "dense"), ("c5", 1, "lookahead"), ("c5", 1, "balanced")]
 METRIC = "sparse-FFN decode tokens/s at batch 1 and achieved HBM GB/s vs roofline"
 L2_BYTES = 126 * 2 ** 20
 ESIZE = {"f32": 4, "f16": 2, "bf16": 2}
@@ -296,6 +297,7 @@ class Model:
         self._args = (sffn, max_batch, flags)
         self.bundled = None
         self.dense = None
+        self.balanced = None
         torch.cuda.synchronize()
 
     def dense_layers(self):
@@ -307,6 +309,15 @@ class Model:
                           for x, h, e in zip(self.lws, self.hots, self.eas)]
         return self.dense
 
+    def balanced_layers(self):
+        """The same weights with the batch-1 kernel's global row balancing."""
+        if self.balanced is None:
+            sffn, max_batch, flags = self._args
+            self.balanced = [sffn.Layer.from_weights(x, tau=self.wl.tau, max_batch=max_batch,
+                                                     flags=flags | sffn.SFFN_FLAG_BALANCE, hot_rows=h, expected_active=e)
+                             for x, h, e in zip(self.lws, self.hots, self.eas)]
+        return self.balanced
+
     def bundled_layers(self):
         """The same layers on the bundled row layout (copies of the rows)."""
         if self.bundled is None:
@@ -317,9 +328,9 @@ class Model:
         return self.bundled
 
     def close(self):
-        for l in self.layers + (self.bundled or []) + (self.dense or []):
+        for l in self.layers + (self.bundled or []) + (self.dense or []) + (self.balanced or []):
             l.close()
-        self.layers, self.lws, self.bundled, self.dense = [], [], None, None
+        self.layers, self.lws, self.bundled, self.dense, self.balanced = [], [], None, None, None
 
 
 # ---------------------------------------------------------------- statistics outside the timing
@@ -390,7 +401,7 @@ def measure(sffn, W, torch, model, B, steps, warmup, dev, world, args, stats=Tru
     esz = ESIZE[wl.dtype]
     nm = 2 if wl.act == "reglu" else 1
     layers = (model.bundled_layers() if variant == "bundled" else model.dense_layers() if variant == "dense"
-              else model.layers)
+              else model.balanced_layers() if variant == "balanced" else model.layers)
     dense_path = variant == "dense" and B >= 2
     union_path = B >= 3 and wl.dtype != "f32" and d % 128 == 0 and not args.row_gather and not dense_path
     rank, _, _ = dist_env()
@@ -757,7 +768,8 @@ def bench_sffn(args):
                       flags)
             for b, v in runs:
                 rec, _ = measure(sffn, W, torch, m, b, SUITE_STEPS[name], 3, dev, world, args,
-                                 stats=not args.no_stats and v != "bundled", dense=not args.no_dense and not v,
+                                 stats=not args.no_stats and v not in ("bundled", "balanced"),
+                                 dense=not args.no_dense and not v,
                                  variant=v)
                 sub.append(rec)
             m.close()

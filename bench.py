@@ -54,12 +54,11 @@ DEFAULT_STEPS = {"c1": 300, "c2": 300, "c3": 100, "c4": 10, "c5": 20}
 SUITE_STEPS = {"c1": 40, "c2": 40, "c3": 20, "c4": 4, "c5": 3}  # sub-record steps (timed), each after >= 3 warm-up steps
 # (workload, batch, variant): the stacks also at batch 1 with look-ahead masks,
 # the ReGLU layer also on the bundled row layout, the batches also through the
-# dense fallback (every row, two GEMMs), the batch-1 layers also with global
-# row balancing
-SUITE = [("c1", 1, ""), ("c2", 1, ""), ("c2", 1, "balanced"), ("c3", 1, ""), ("c3", 4, ""), ("c3", 8, ""), ("c3", 16, ""), ("c3", 32, ""),
+# dense fallback (every row, two GEMMs)
+SUITE = [("c1", 1, ""), ("c2", 1, ""), ("c3", 1, ""), ("c3", 4, ""), ("c3", 8, ""), ("c3", 16, ""), ("c3", 32, ""),
          ("c3", 1, "bundled"), ("c3", 8, "bundled"), ("c3", 32, "bundled"), ("c3", 4, "dense"), ("c3", 8, "dense"),
-         ("c3", 16, "dense"), ("c3", 32, "dense"), ("c4", 1, ""), ("c4", 1, "lookahead"), ("c4", 1, "balanced"),
-         ("c5", 8, ""), ("c5", 8, "dense"), ("c5", 1, "lookahead"), ("c5", 1, "balanced")]
+         ("c3", 16, "dense"), ("c3", 32, "dense"), ("c4", 1, ""), ("c4", 1, "lookahead"),
+         ("c5", 8, ""), ("c5", 8, "dense"), ("c5", 1, "lookahead")]
 METRIC = "sparse-FFN decode tokens/s at batch 1 and achieved HBM GB/s vs roofline"
 L2_BYTES = 126 * 2 ** 20
 ESIZE = {"f32": 4, "f16": 2, "bf16": 2}

@@ -1069,6 +1069,19 @@ sffn_status sffn_read_device_status(void* workspace, int32_t* status, void* stre
   return SFFN_OK;
 }
 
+sffn_status sffn_debug_occupy(int64_t ns, int32_t blocks, int32_t smem_bytes, void* stream) {
+  g_err.clear();
+  if (ns <= 0 || ns > 2000000000LL) return fail(SFFN_ERR_INVALID_ARG, "ns outside (0, 2e9]");
+  if (blocks < 1 || blocks > 65535) return fail(SFFN_ERR_INVALID_ARG, "blocks outside [1, 65535]");
+  int dev = 0, optin = 0;
+  SFFN_CUDA(cudaGetDevice(&dev), "device query");
+  SFFN_CUDA(cudaDeviceGetAttribute(&optin, cudaDevAttrMaxSharedMemoryPerBlockOptin, dev), "device query");
+  if (smem_bytes < 0 || smem_bytes > optin) return fail(SFFN_ERR_INVALID_ARG, "smem_bytes outside [0, %d]", optin);
+  SFFN_CUDA(launch_occupy((uint64_t)ns, blocks, (size_t)smem_bytes, static_cast<cudaStream_t>(stream)),
+            "occupy launch");
+  return SFFN_OK;
+}
+
 sffn_status sffn_debug_wait_timeout(void* workspace, size_t ws_bytes, int64_t timeout_ns, void* stream) {
   g_err.clear();
   if (workspace == nullptr || ws_bytes < sizeof(WsHeader) + barrier_flag_bytes(2))

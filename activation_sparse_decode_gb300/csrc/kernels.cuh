@@ -188,6 +188,7 @@ cudaError_t launch_permute_rows(const void* src, void* dst, const int32_t* perm,
 
 // ---- test hook: a barrier wait that cannot complete
 cudaError_t launch_wait_timeout(WsHeader* hdr, uint32_t* flags, uint64_t limit_ns, cudaStream_t s);
+cudaError_t launch_occupy(uint64_t ns, int blocks, size_t smem, cudaStream_t s);
 
 // ---- dense fallback (every row, two library GEMMs): the masked activation
 // between them (16-bit high part and remainder, [2B][f]) and the sum of the

@@ -92,25 +92,32 @@ __device__ __forceinline__ float layer_block_sum(float v, float* s_warp) {
   return t;
 }
 
+// One 16-byte chunk of values rounded to the stored format (round to nearest even).
 template <typename T>
-__device__ __forceinline__ void pack_store(T* dst, const float* v);
+__device__ __forceinline__ uint4 pack_chunk(const float* v);
 template <>
-__device__ __forceinline__ void pack_store<float>(float* dst, const float* v) {
-  *reinterpret_cast<float4*>(dst) = make_float4(v[0], v[1], v[2], v[3]);
+__device__ __forceinline__ uint4 pack_chunk<float>(const float* v) {
+  return make_uint4(__float_as_uint(v[0]), __float_as_uint(v[1]), __float_as_uint(v[2]), __float_as_uint(v[3]));
 }
 template <>
-__device__ __forceinline__ void pack_store<__half>(__half* dst, const float* v) {
-  __half o[8];
+__device__ __forceinline__ uint4 pack_chunk<__half>(const float* v) {
+  uint32_t w[4];
 #pragma unroll
-  for (int e = 0; e < 8; ++e) o[e] = __float2half_rn(v[e]);
-  *reinterpret_cast<uint4*>(dst) = *reinterpret_cast<const uint4*>(o);
+  for (int i = 0; i < 4; ++i) {
+    const __half2 h = __floats2half2_rn(v[2 * i], v[2 * i + 1]);
+    w[i] = *reinterpret_cast<const uint32_t*>(&h);
+  }
+  return make_uint4(w[0], w[1], w[2], w[3]);
 }
 template <>
-__device__ __forceinline__ void pack_store<__nv_bfloat16>(__nv_bfloat16* dst, const float* v) {
-  __nv_bfloat16 o[8];
+__device__ __forceinline__ uint4 pack_chunk<__nv_bfloat16>(const float* v) {
+  uint32_t w[4];
 #pragma unroll
-  for (int e = 0; e < 8; ++e) o[e] = __float2bfloat16_rn(v[e]);
-  *reinterpret_cast<uint4*>(dst) = *reinterpret_cast<const uint4*>(o);
+  for (int i = 0; i < 4; ++i) {
+    const __nv_bfloat162 h = __floats2bfloat162_rn(v[2 * i], v[2 * i + 1]);
+    w[i] = *reinterpret_cast<const uint32_t*>(&h);
+  }
+  return make_uint4(w[0], w[1], w[2], w[3]);
 }
 
 // The forms up to three chunks (d_model up to 6144 for 16-bit weights) are
@@ -152,8 +159,7 @@ __global__ void __launch_bounds__(kLayerThreads, CPT <= 3 ? 2 : 1) k_layer(const
 
   // ---- shared memory carve-up (offsets are multiples of 16)
   unsigned char* region = smem;  // U rows (phases 0-4), then the row ring
-  T* xs = reinterpret_cast<T*>(smem + a.region_bytes);
-  float* hs = reinterpret_cast<float*>(reinterpret_cast<unsigned char*>(xs) + (size_t)d * ES);
+  float* hs = reinterpret_cast<float*>(smem + a.region_bytes);
   uint64_t* bars = reinterpret_cast<uint64_t*>(hs + ((r + 3) & ~3));
   float* ownb = reinterpret_cast<float*>(bars + S + 1);
   float* ownpb = ownb + own_cap;
@@ -348,13 +354,15 @@ __global__ void __launch_bounds__(kLayerThreads, CPT <= 3 ? 2 : 1) k_layer(const
       for (int w = (int)((int64_t)W * k / r) + tid; w < w1; w += kLayerThreads) sc_out[w] = 0u;
     }
   }
-  // the token: loaded, or formed from the previous layer by residual + LayerNorm
+  // The token: loaded, or formed from the previous layer by residual +
+  // LayerNorm.  Thread tid only ever uses chunks tid, tid + 256, ... of it
+  // (the h rows and the ring read the same chunks of every row), so it stays
+  // in registers, packed in the stored format (xpk), and no shared memory
+  // holds it.
+  uint4 xpk[CPT];
   if (a.y_prev == nullptr) {
 #pragma unroll
-    for (int cq = 0; cq < CPT; ++cq) {
-      const int ch = tid + cq * kLayerThreads;
-      if (ch < NCH) reinterpret_cast<uint4*>(xs)[ch] = xreg[cq];
-    }
+    for (int cq = 0; cq < CPT; ++cq) xpk[cq] = xreg[cq];
   } else {
     // x_prev + y_prev is read once into registers (every chunk's loads in
     // flight together); mean and biased variance by two block sums over them
@@ -398,16 +406,19 @@ __global__ void __launch_bounds__(kLayerThreads, CPT <= 3 ? 2 : 1) k_layer(const
           if (a.ln_beta != nullptr) o += a.ln_beta[ch * E + e];
           v[cq][e] = o;
         }
-        pack_store<T>(xs + ch * E, v[cq]);
+      }
+      xpk[cq] = ch < NCH ? pack_chunk<T>(v[cq]) : make_uint4(0, 0, 0, 0);
+    }
+    if (a.x_ln_out != nullptr) {  // chunk ch of the new x is stored by block ch mod G
+      uint4* xo = static_cast<uint4*>(a.x_ln_out);
+#pragma unroll
+      for (int cq = 0; cq < CPT; ++cq) {
+        const int ch = tid + cq * kLayerThreads;
+        if (ch < NCH && ch % G == c) xo[ch] = xpk[cq];
       }
     }
   }
   __syncthreads();
-  if (a.y_prev != nullptr && a.x_ln_out != nullptr) {  // each block stores its slice of the new x
-    uint4* xo = static_cast<uint4*>(a.x_ln_out);
-    for (int ch = (int)((int64_t)NCH * c / G) + tid; ch < (int)((int64_t)NCH * (c + 1) / G); ch += kLayerThreads)
-      xo[ch] = reinterpret_cast<const uint4*>(xs)[ch];
-  }
 
   // ---- the ring's list and its first fills (start_ring), and the pair split
   // (settle_ring).  Normal calls run both after the scores; look-ahead calls
@@ -562,7 +573,7 @@ __global__ void __launch_bounds__(kLayerThreads, CPT <= 3 ? 2 : 1) k_layer(const
         if (j0 + jj < nh && ch < NCH) {
           float w[E], xv[E];
           unpack<T>(vr[jj][cq], w);
-          unpack<T>(reinterpret_cast<const uint4*>(xs)[ch], xv);
+          unpack<T>(xpk[cq], xv);
 #pragma unroll
           for (int e = 0; e < E; e += 2) {
             acc0 = fmaf(w[e], xv[e], acc0);
@@ -899,9 +910,7 @@ __global__ void __launch_bounds__(kLayerThreads, CPT <= 3 ? 2 : 1) k_layer(const
 #pragma unroll
   for (int cq = 0; cq < CPT; ++cq) {
     const int ch = tid + cq * kLayerThreads;
-    uint4 raw = make_uint4(0, 0, 0, 0);
-    if (ch < NCH) raw = reinterpret_cast<const uint4*>(xs)[ch];
-    unpack<T>(raw, xr[cq]);
+    unpack<T>(ch < NCH ? xpk[cq] : make_uint4(0, 0, 0, 0), xr[cq]);
 #pragma unroll
     for (int e = 0; e < E; ++e) yacc[cq][e] = 0.f;
   }

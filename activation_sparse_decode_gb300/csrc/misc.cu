@@ -99,6 +99,19 @@ __global__ void k_wait_timeout(WsHeader* hdr, uint32_t* flags, uint64_t limit_ns
   grid_barrier(hdr, flags, gridDim.x + 1u, barrier_generation(flags), limit_ns, 0x900u);
 }
 
+// Test hook: every block holds its SM's resources (its dynamic shared
+// memory) for `ns` nanoseconds of wall time, then exits.  Bounded; touches
+// no memory.
+__global__ void k_occupy(uint64_t ns) {
+  extern __shared__ unsigned char hold[];
+  if (threadIdx.x == 0) {
+    const uint64_t t0 = globaltimer_ns();
+    while (globaltimer_ns() - t0 < ns) __nanosleep(2000);
+    hold[0] = 0;
+  }
+  __syncthreads();
+}
+
 template <typename T>
 cudaError_t ln_launch(const void* x, const float* y, int B, int d, const float* gamma, const float* beta,
                       float eps, void* out, cudaStream_t s) {
@@ -142,6 +155,14 @@ cudaError_t launch_permute_rows(const void* src, void* dst, const int32_t* perm,
 
 cudaError_t launch_wait_timeout(WsHeader* hdr, uint32_t* flags, uint64_t limit_ns, cudaStream_t s) {
   k_wait_timeout<<<1, 32, 0, s>>>(hdr, flags, limit_ns);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_occupy(uint64_t ns, int blocks, size_t smem, cudaStream_t s) {
+  static int cur = 48 * 1024;
+  const cudaError_t e = ensure_dyn_smem(k_occupy, smem, &cur);
+  if (e != cudaSuccess) return e;
+  k_occupy<<<blocks, 32, smem, s>>>(ns);
   return cudaGetLastError();
 }
 
@@ -189,12 +210,12 @@ bool layer_config(int dtype, int act, int d, int f, int r, int grid, size_t smem
   if (nwords > 256 || grid > 1024) return false;
   if (r > 32 * 32) return false;  // h slots: at most 32 per lane of the polling warp
   const size_t stage = (size_t)(act == kReglu ? 3 : 2) * d * esize;
-  // x, h, stage barriers, own biases (2), list + list biases, words, activity
+  // h, stage barriers, own biases (2), list + list biases, words, activity
   // flags, the pair-exchange inbox, and the balancing scratch (3 x grid) when
-  // the launches balance
+  // the launches balance (the token stays in registers)
   const size_t bal = balance ? (size_t)grid * 12 : 0;
   const size_t inbox = (size_t)((own_cap + 1) & ~1) * 8 + 16;  // pair exchange entries, 16-byte aligned
-  const size_t fixed = (size_t)d * esize + (size_t)((r + 3) & ~3) * 4 + 17 * 8 + (size_t)own_cap * 16 + nwords * 4 +
+  const size_t fixed = (size_t)((r + 3) & ~3) * 4 + 17 * 8 + (size_t)own_cap * 16 + nwords * 4 +
                        bal + (size_t)(own_cap + 15) / 16 * 16 + inbox + 80;
   const size_t reserve = 2048;  // static shared memory of the kernel
   if (smem_optin < fixed + reserve + 2 * stage) return false;
@@ -210,7 +231,7 @@ bool layer_config(int dtype, int act, int d, int f, int r, int grid, size_t smem
   cfg->u_off = cfg->u_smem ? cfg->region_bytes - u_round : 0;  // U rows sit at the end of the region
   cfg->hot_stages = (int)std::min<size_t>(4, cfg->u_smem ? cfg->u_off / stage : s);
   cfg->balance = balance ? 1 : 0;
-  cfg->smem = cfg->region_bytes + (size_t)d * esize + (size_t)((r + 3) & ~3) * 4 + (s + 1) * 8 +
+  cfg->smem = cfg->region_bytes + (size_t)((r + 3) & ~3) * 4 + (s + 1) * 8 +
               (size_t)own_cap * 16 + nwords * 4 + (size_t)(own_cap + 15) / 16 * 16 + inbox + bal + 80;
   return cfg->smem + reserve <= smem_optin;
 }

@@ -82,6 +82,7 @@ _c = {
     "status": _sig("sffn_read_device_status", _i32, _vp, ctypes.POINTER(_i32), _vp),
     "bundle": _sig("sffn_bundle_rows", _i32, _vp, _vp, _vp, _i32, _i32, _i32, _vp, _vp),
     "debug_wait": _sig("sffn_debug_wait_timeout", _i32, _vp, _sz, _i64, _vp),
+    "debug_occupy": _sig("sffn_debug_occupy", _i32, _i64, _i32, _i32, _vp),
     "wait_limit": _sig("sffn_set_wait_limit_ns", _i32, _i64),
     "prof_events": _sig("sffn_set_profile_events", _i32, ctypes.POINTER(_vp), ctypes.POINTER(_vp), _i32),
     "noalloc": _sig("sffn_forward_noalloc", _i32, _vp, _vp, _vp, _vp),
@@ -97,7 +98,7 @@ EXPORTED = ["sffn_create_layer", "sffn_destroy_layer", "sffn_workspace_size", "s
             "sffn_residual_layernorm", "sffn_forward_stack", "sffn_stack_workspace_size",
             "sffn_profile_counts", "sffn_hot_first_perm", "sffn_permute_rows", "sffn_bundle_rows",
             "sffn_read_device_status",
-            "sffn_debug_wait_timeout", "sffn_set_wait_limit_ns", "sffn_set_profile_events", "sffn_forward_noalloc", "sffn_noalloc_read_status",
+            "sffn_debug_wait_timeout", "sffn_debug_occupy", "sffn_set_wait_limit_ns", "sffn_set_profile_events", "sffn_forward_noalloc", "sffn_noalloc_read_status",
             "sffn_status_string", "sffn_last_error", "sffn_version"]
 
 
@@ -311,6 +312,10 @@ def sffn_read_device_status(ws: torch.Tensor, stream=None) -> int:
 
 def sffn_debug_wait_timeout(ws: torch.Tensor, timeout_ns: int, stream=None):
     _check(_c["debug_wait"](_ptr(ws), ws.numel(), int(timeout_ns), _stream(stream)))
+
+
+def sffn_debug_occupy(ns: int, blocks: int, smem_bytes: int, stream=None):
+    _check(_c["debug_occupy"](int(ns), int(blocks), int(smem_bytes), _stream(stream)))
 
 
 def sffn_set_wait_limit_ns(ns: int):

@@ -365,6 +365,14 @@ sffn_status sffn_read_device_status(void* workspace, int32_t* status, void* stre
 sffn_status sffn_debug_wait_timeout(void* workspace, size_t workspace_bytes, int64_t timeout_ns,
                                     void* stream);
 
+/* Test hook for the co-residency requirement of sffn_forward: queues
+ * `blocks` one-warp blocks that each hold smem_bytes of dynamic shared memory
+ * (0..the per-block opt-in maximum) on their SM for ns nanoseconds of wall
+ * time (at most 2e9) and then exit; they touch no memory.  Launched on one
+ * stream while a batch-1 call runs on another, they keep part of the call's
+ * grid from being resident.  Errors: SFFN_ERR_INVALID_ARG outside the ranges. */
+sffn_status sffn_debug_occupy(int64_t ns, int32_t blocks, int32_t smem_bytes, void* stream);
+
 /* Profiling hook: the next n_pairs launches of a call's dominant kernel (the
  * single-launch layer kernel at batch 1, the tensor-core union kernel or the
  * row-gather kernel; of sffn_forward, sffn_dense_forward and

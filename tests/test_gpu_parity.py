@@ -396,6 +396,50 @@ def test_bounded_wait_reports_timeout(sffn):
     check_token(oracle_layer(lw), st(X)[0, 0], mask_from_list(I[0, 0], N[0, 0], 256), Y[0, 0], 1e-5)
 
 
+def test_batch1_call_reports_timeout_when_its_grid_cannot_be_resident(sffn):
+    """The batch-1 kernel's blocks wait for each other's h values, so its whole
+    grid must be resident at once.  Half of the SMs are held by a bounded
+    occupier kernel on another stream while a call runs with a 2 ms wait
+    limit: the call must either give the oracle's result (the scheduler ran it
+    first) or leave SFFN_ERR_TIMEOUT in the status word; nothing faults or
+    hangs, and afterwards the context is usable and a normal call gives the
+    oracle's result."""
+    import time
+    wl = W.tiny_workload(d_model=4096, d_ff=8192, rank=128, dtype="f16", mean_p=0.1, name="coresidency")
+    lw = W.make_layer(wl, device=DEV)
+    ol = oracle_layer(lw)
+    layer = sffn.Layer.from_weights(lw)
+    info = sffn.sffn_get_layer_info(layer)
+    assert info["fused"] == 1 and info["cluster"] == 0
+    nsm = torch.cuda.get_device_properties(0).multi_processor_count
+    x = W.make_tokens(wl, 1, device=DEV)[0]
+    y = torch.empty(1, wl.d_model, dtype=torch.float32, device=DEV)
+    idx = torch.empty(1, wl.d_ff, dtype=torch.int32, device=DEV)
+    n = torch.empty(1, dtype=torch.int32, device=DEV)
+    ws = sffn.new_workspace(sffn.sffn_workspace_size(layer, 1), DEV)
+    s_occ, s_call = torch.cuda.Stream(), torch.cuda.Stream()
+    torch.cuda.synchronize()
+    sffn.sffn_set_wait_limit_ns(2_000_000)
+    try:
+        # 200 KB of shared memory per occupier block: one per SM, and no room
+        # left beside it for a layer block
+        sffn.sffn_debug_occupy(300_000_000, nsm // 2, 200 * 1024, stream=s_occ)
+        time.sleep(0.02)
+        sffn.sffn_forward(layer, x, y, ws, idx, n, stream=s_call)
+        torch.cuda.synchronize()
+    finally:
+        sffn.sffn_set_wait_limit_ns(1_000_000_000)
+    status = sffn.sffn_read_device_status(ws)
+    assert status in (0, 5), status
+    if status == 0:
+        check_token(ol, st(x)[0], mask_from_list(idx[0].cpu().numpy(), int(n.item()), wl.d_ff), y[0].cpu().numpy(),
+                    TOL["f16"])
+    # the context is usable: a fresh workspace, a normal call, the oracle's result
+    X = x.unsqueeze(0)
+    Y, I, N = run_tokens(sffn, layer, X)
+    check_token(ol, st(X)[0, 0], mask_from_list(I[0, 0], N[0, 0], wl.d_ff), Y[0, 0], TOL["f16"])
+
+
 def test_boundary_errors(sffn):
     wl = W.tiny_workload(d_model=64, d_ff=256, rank=8, dtype="f16", name="boundary")
     lw = W.make_layer(wl, device=DEV)

@@ -254,7 +254,10 @@ __global__ void __launch_bounds__(kLayerThreads, CPT <= 3 ? 2 : 1) k_layer(const
       if (a.b != nullptr) prefetch_l2(&a.b[c + j * G]);
       prefetch_l2(&a.pb[c + j * G]);
     }
-    const int ulines = (urow_bytes + 127) / 128;
+    // (U rows too many to stage are not warmed: the scores stream them once,
+    // and 100 MB of prefetches queued ahead of the token's loads cost more
+    // than they saved -- 81.9 against 81.5 us per layer on the OPT-175B shape)
+    const int ulines = a.u_smem ? (urow_bytes + 127) / 128 : 0;
     for (int q = tid; q < n_own * ulines; q += kLayerThreads) {
       const int j = q / ulines, l = q - j * ulines;
       prefetch_l2(Ub + (size_t)(c + (size_t)j * G) * urow_bytes + l * 128);

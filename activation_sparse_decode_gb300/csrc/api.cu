@@ -205,11 +205,14 @@ sffn_status run_predictor(const sffn_layer* L, const void* x, int batch, const W
     // one hidden-layer launch for the whole batch (h also as three 16-bit
     // parts), then the scores and threshold as one tensor-core product
     const int bt = batch <= 8 ? 8 : batch <= 16 ? 16 : 32;
-    // above 16 tokens the lane-per-token kernel (K-chunks of 256); below it
-    // would leave most lanes idle
+    // the cluster kernel where d splits into its eighths; otherwise, above
+    // 16 tokens the lane-per-token kernel (K-chunks of 256), below it the
+    // token-group kernel
     const bool tok = batch > 16;
     PredHiddenArgs ha{d.pred_V, x, batch, d.rank, d.d_model, tok ? 256 : L->kc32, tok ? L->KStok : L->KS32,
                       ws.h_part(), ws.h(), ws.tickets(), ws.h3(), bt};
+    const size_t hc = pred_hidden_cluster_smem(d.d_model, bt);
+    ha.cluster = hc > 0 && hc <= L->smem_optin ? 1 : 0;
     SFFN_CUDA(launch_pred_hidden(d.dtype, ha, s), "predictor hidden launch");
     ScoreMmaArgs sa{d.pred_U, ws.h3(), d.pred_b, d.tau, batch, d.d_ff, d.rank, L->W, ws.mask(), ws.hdr(), ring,
                     (uint64_t)g_wait_ns};

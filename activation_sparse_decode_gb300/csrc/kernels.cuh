@@ -20,8 +20,11 @@ struct PredHiddenArgs {
   uint32_t* tickets;   // [row groups][token groups] arrival counters (zeroed)
   void* h3;            // NULL, or [3*bt][r] dtype: h split into hi, mid, lo 16-bit parts (rows part*bt + b)
   int bt;              // 0: tokens per block chosen from B; else 8, 16 or 32 (one token group)
+  int cluster = 0;     // 1: the cluster kernel (16-bit weights, h3 set, bt >= B, d a multiple of 512)
 };
 int pred_hidden_row_groups(int r);
+// Dynamic shared memory of the cluster hidden-layer kernel (0: d does not fit its split).
+size_t pred_hidden_cluster_smem(int d, int bt);
 cudaError_t launch_pred_hidden(int dtype, const PredHiddenArgs& a, cudaStream_t s);
 
 // ---- predictor scores + threshold: mask[b][w] bit j  <=>  U[32w+j].h[b] + pb > tau

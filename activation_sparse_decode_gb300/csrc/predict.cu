@@ -242,6 +242,173 @@ __global__ void __launch_bounds__(256)
   }
 }
 
+// Hidden layer for a batch of 8 to 32 tokens, 16-bit weights, feeding the
+// tensor-core score product (h also as three 16-bit parts).  Clusters of
+// eight blocks: cluster y owns rows [16y, 16y + 16) of V and block q of it the
+// q-th eighth of d.  A block copies its V rows and the tokens' columns into
+// shared memory with cp.async in four groups along d, and works on each group
+// as soon as it has landed, so the copies of the later groups overlap the
+// arithmetic of the earlier ones.  Every lane owns a micro-tile of 4 rows x 4
+// tokens and a share of the 16-byte column pieces (the lanes of a warp that
+// hold the same micro-tile take neighbouring pieces and are summed by
+// shuffles at the end); pieces are stored at permuted positions so that the
+// distinct addresses of one warp-wide load fall in distinct banks as far as
+// their number allows.  The warps' partial sums are added in shared memory,
+// and after a cluster barrier block q sums rows 2q, 2q + 1 of the cluster's
+// tile over the eight blocks' shared memory.  Every sum runs in a fixed
+// order, so h is the same from run to run; there are no global partial sums
+// and no arrival counters.
+constexpr int kHcCL = 8;         // blocks per cluster: the split of d
+constexpr int kHcRows = 16;      // rows of V per cluster
+constexpr int kHcThreads = 256;  // eight warps
+constexpr int kHcPieces = 12;    // 16-byte loads in flight per thread
+
+__device__ __forceinline__ float ld_peer_f32(uint32_t addr) {
+  float v;
+  asm volatile("ld.shared::cluster.f32 %0, [%1];" : "=f"(v) : "r"(addr) : "memory");
+  return v;
+}
+
+template <int BT> struct HcTile {
+  static constexpr int MR = 4, MB = 4;       // micro-tile: rows x tokens per lane
+  static constexpr int NRG = kHcRows / MR;   // row groups (4)
+  static constexpr int NTG = BT / MB;        // token groups (2, 4, 8)
+  static constexpr int LPC = NRG * NTG;      // lanes per column piece
+  static constexpr int KQ = 32 / LPC;        // lanes holding the same micro-tile (4, 2, 1)
+  static_assert(LPC * KQ == 32, "whole warps");
+};
+
+// Piece positions: V row rr, piece c at c ^ vperm(rr); token b at c ^ xperm(b).
+__device__ __forceinline__ int hc_vperm(int rr) { return (rr >> 1) & 6; }
+template <int BT> __device__ __forceinline__ int hc_xperm(int b) { return ((b >> 2) * HcTile<BT>::KQ) & 7; }
+
+template <int BT>
+size_t hidden_cl_smem(int d) {
+  const size_t nchk = (size_t)d / kHcCL / 8;
+  return (kHcRows + BT) * nchk * 16 + (size_t)(kHcThreads / 32 + 1) * kHcRows * BT * 4;
+}
+
+template <typename T, int BT>
+__global__ void __cluster_dims__(kHcCL, 1, 1) __launch_bounds__(kHcThreads)
+    k_pred_hidden_cl(const T* __restrict__ V, const T* __restrict__ x, int B, int r, int d,
+                     float* __restrict__ h, T* __restrict__ h3) {
+  using Tile = HcTile<BT>;
+  constexpr int MR = Tile::MR, MB = Tile::MB, NTG = Tile::NTG, LPC = Tile::LPC, KQ = Tile::KQ;
+  constexpr int kWarps = kHcThreads / 32;
+  extern __shared__ __align__(16) unsigned char hc_smem[];
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  const int q = (int)cluster_rank();
+  const int row0 = blockIdx.y * kHcRows;
+  const int Kc = d / kHcCL;   // a multiple of 64
+  const int nchk = Kc / 8;    // 16-byte pieces of a row's part (a multiple of 8)
+  const int k0 = q * Kc;
+  uint4* vs = reinterpret_cast<uint4*>(hc_smem);           // [kHcRows][nchk]
+  uint4* xs = vs + kHcRows * nchk;                          // [BT][nchk]
+  float* part = reinterpret_cast<float*>(xs + BT * nchk);  // [warp][row][token]
+  float* P = part + kWarps * kHcRows * BT;                 // [row][token], this block's part of d
+
+  // copies: every piece through registers (16-byte loads, up to kHcPieces
+  // in flight per thread per round), then into its permuted position
+  const int npieces = (kHcRows + BT) * nchk;
+  for (int p0 = 0; p0 < npieces; p0 += kHcPieces * kHcThreads) {
+    uint4 reg[kHcPieces];
+#pragma unroll
+    for (int u = 0; u < kHcPieces; ++u) {
+      const int i = p0 + u * kHcThreads + tid;
+      const int rowi = i / nchk, c = i - rowi * nchk;
+      reg[u] = make_uint4(0, 0, 0, 0);
+      if (i < npieces) {
+        if (rowi < kHcRows) {
+          if (row0 + rowi < r) reg[u] = ldg_stream(V + (size_t)(row0 + rowi) * d + k0 + c * 8);
+        } else if (rowi - kHcRows < B) {
+          reg[u] = __ldg(reinterpret_cast<const uint4*>(x + (size_t)(rowi - kHcRows) * d + k0 + c * 8));
+        }
+      }
+    }
+#pragma unroll
+    for (int u = 0; u < kHcPieces; ++u) {
+      const int i = p0 + u * kHcThreads + tid;
+      const int rowi = i / nchk, c = i - rowi * nchk;
+      if (i < npieces) {
+        if (rowi < kHcRows)
+          vs[rowi * nchk + (c ^ hc_vperm(rowi))] = reg[u];
+        else
+          xs[(rowi - kHcRows) * nchk + (c ^ hc_xperm<BT>(rowi - kHcRows))] = reg[u];
+      }
+    }
+  }
+  __syncthreads();
+
+  const int kq = lane / LPC, within = lane - kq * LPC;
+  const int rg = within / NTG, tg = within - rg * NTG;
+  const int vp = hc_vperm(rg * MR), xp = hc_xperm<BT>(tg * MB);
+  float acc[MR][MB];
+#pragma unroll
+  for (int i = 0; i < MR; ++i)
+#pragma unroll
+    for (int j = 0; j < MB; ++j) acc[i][j] = 0.f;
+  for (int c = warp * KQ + kq; c < nchk; c += kWarps * KQ) {
+    float w[MR][8], xv[MB][8];
+#pragma unroll
+    for (int i = 0; i < MR; ++i) unpack<T>(vs[(rg * MR + i) * nchk + (c ^ vp)], w[i]);
+#pragma unroll
+    for (int j = 0; j < MB; ++j) unpack<T>(xs[(tg * MB + j) * nchk + (c ^ xp)], xv[j]);
+#pragma unroll
+    for (int e = 0; e < 8; ++e)
+#pragma unroll
+      for (int i = 0; i < MR; ++i)
+#pragma unroll
+        for (int j = 0; j < MB; ++j) acc[i][j] = fmaf(w[i][e], xv[j][e], acc[i][j]);
+  }
+
+  // the lanes holding the same micro-tile, then the warps, in a fixed order
+#pragma unroll
+  for (int i = 0; i < MR; ++i)
+#pragma unroll
+    for (int j = 0; j < MB; ++j)
+#pragma unroll
+      for (int o = LPC; o < 32; o <<= 1) acc[i][j] += __shfl_xor_sync(0xffffffffu, acc[i][j], o);
+  if (kq == 0)
+#pragma unroll
+    for (int i = 0; i < MR; ++i)
+#pragma unroll
+      for (int j = 0; j < MB; ++j) part[(warp * kHcRows + rg * MR + i) * BT + tg * MB + j] = acc[i][j];
+  __syncthreads();
+  for (int o = tid; o < kHcRows * BT; o += kHcThreads) {
+    float sum = 0.f;
+#pragma unroll
+    for (int w = 0; w < kWarps; ++w) sum += part[w * kHcRows * BT + o];
+    P[o] = sum;
+  }
+  cluster_arrive();  // release: this block's P is complete
+  cluster_wait();    // acquire: every block's P is complete
+
+  constexpr int kRowsPerBlock = kHcRows / kHcCL;
+  if (tid < kRowsPerBlock * BT) {
+    const int rr = q * kRowsPerBlock + tid / BT, b = tid % BT;
+    float v[kHcCL];
+#pragma unroll
+    for (int p = 0; p < kHcCL; ++p) v[p] = ld_peer_f32(peer_smem(P + rr * BT + b, (uint32_t)p));
+    float sum = 0.f;
+#pragma unroll
+    for (int p = 0; p < kHcCL; ++p) sum += v[p];
+    const int row = row0 + rr;
+    if (row < r && b < B) {
+      h[(size_t)b * r + row] = sum;
+      // three 16-bit parts whose sum carries the fp32 value
+      const T hi = from_float<T>(sum);
+      const float rest = sum - static_cast<float>(hi);
+      const T mid = from_float<T>(rest);
+      const T lo = from_float<T>(rest - static_cast<float>(mid));
+      h3[(size_t)(0 * BT + b) * r + row] = hi;
+      h3[(size_t)(1 * BT + b) * r + row] = mid;
+      h3[(size_t)(2 * BT + b) * r + row] = lo;
+    }
+  }
+  cluster_arrive();  // no block leaves while another may still read its P
+  cluster_wait();
+}
+
 // Scores.  A block owns 64-row blocks (two mask words) in a grid-stride loop;
 // each warp streams 8 rows of U, lane l holding the 16-byte chunks l, l+32, ...
 // of every row (CPL chunks), and rows are summed with a warp all-reduce.
@@ -405,8 +572,38 @@ cudaError_t hidden_launch(const PredHiddenArgs& a, cudaStream_t s) {
   return cudaGetLastError();
 }
 
+template <typename T, int BT>
+cudaError_t hidden_cl_launch(const PredHiddenArgs& a, cudaStream_t s) {
+  const size_t smem = hidden_cl_smem<BT>(a.d);
+  static int cur = 48 * 1024;
+  const cudaError_t e = ensure_dyn_smem(k_pred_hidden_cl<T, BT>, smem, &cur);
+  if (e != cudaSuccess) return e;
+  const dim3 grid(kHcCL, (a.r + kHcRows - 1) / kHcRows);
+  k_pred_hidden_cl<T, BT><<<grid, kHcThreads, smem, s>>>(static_cast<const T*>(a.V), static_cast<const T*>(a.x),
+                                                          a.B, a.r, a.d, a.h, static_cast<T*>(a.h3));
+  return cudaGetLastError();
+}
+
+template <typename T>
+cudaError_t hidden_cl_dispatch(const PredHiddenArgs& a, cudaStream_t s) {
+  switch (a.bt) {
+    case 8: return hidden_cl_launch<T, 8>(a, s);
+    case 16: return hidden_cl_launch<T, 16>(a, s);
+    case 32: return hidden_cl_launch<T, 32>(a, s);
+  }
+  return cudaErrorInvalidValue;
+}
+
 template <typename T>
 cudaError_t hidden_dispatch(const PredHiddenArgs& a, cudaStream_t s) {
+  if (a.cluster) {
+    if constexpr (sizeof(T) == 2) {
+      if (a.h3 == nullptr || a.B > a.bt || a.d % (kHcCL * 64) != 0) return cudaErrorInvalidValue;
+      return hidden_cl_dispatch<T>(a, s);
+    } else {
+      return cudaErrorInvalidValue;
+    }
+  }
   if (a.bt == 32 && a.B > 16) {  // one group of 17-32 tokens: lane = token kernel, K-chunks of 256
     if (a.B > 32 || a.kc_elems != kTokKc) return cudaErrorInvalidValue;
     const dim3 grid(a.KS, (a.r + kTokRows - 1) / kTokRows);
@@ -463,6 +660,16 @@ cudaError_t score_dispatch(const PredScoreArgs& a, cudaStream_t s) {
 // Row groups of the hidden-layer kernel at its smallest group size: an upper
 // bound on the arrival tickets any launch uses per token group.
 int pred_hidden_row_groups(int r) { return (r + kHiddenRowsPerBlockMin - 1) / kHiddenRowsPerBlockMin; }
+
+size_t pred_hidden_cluster_smem(int d, int bt) {
+  if (d % (kHcCL * 64) != 0) return 0;
+  switch (bt) {
+    case 8: return hidden_cl_smem<8>(d);
+    case 16: return hidden_cl_smem<16>(d);
+    case 32: return hidden_cl_smem<32>(d);
+  }
+  return 0;
+}
 
 cudaError_t launch_pred_hidden(int dtype, const PredHiddenArgs& a, cudaStream_t s) {
   switch (dtype) {

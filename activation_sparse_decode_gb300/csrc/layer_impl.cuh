@@ -752,9 +752,13 @@ __global__ void __launch_bounds__(kLayerThreads, CPT <= 3 ? 2 : 1) k_layer(const
       }
     }
   } else {
-    // Rows too many to stage: one warp per 32-row word reads each row from
-    // L2 (warmed in phase 0), lane l holding chunks l, l+32, ...; rows are
-    // summed with a warp all-reduce and lane k keeps row k's score.
+    // Rows too many to stage: one warp per task reads each row from L2
+    // (warmed in phase 0), lane l holding chunks l, l+32, ...; rows are
+    // summed with a warp all-reduce and lane k keeps row k's score.  A task
+    // is a whole 32-row word while a round of eight words is left, then a
+    // quarter of a word: one warp per word left three warps working through
+    // the last three words' round trips while five idled (the OPT-175B
+    // shape: 11 words a block).
     float hreg[CPL][E];
 #pragma unroll
     for (int cc = 0; cc < CPL; ++cc) {
@@ -766,10 +770,15 @@ __global__ void __launch_bounds__(kLayerThreads, CPT <= 3 ? 2 : 1) k_layer(const
     // rows in batches of UB, every load of a batch issued before any is used
     // (each row is an L2 round trip otherwise); wide forms have the registers
     constexpr int UB = CPT >= 4 ? 8 : 2;
-    for (int q = warp; q < nwords; q += kLayerWarps) {
-      const int kn = min(32, n_own - q * 32);
+    const int nfull = nwords / kLayerWarps * kLayerWarps;
+    const int ntask = nfull + 4 * (nwords - nfull);
+    for (int t = warp; t < ntask; t += kLayerWarps) {
+      const int q = t < nfull ? t : nfull + (t - nfull) / 4;
+      const int kb = t < nfull ? 0 : ((t - nfull) % 4) * 8;
+      const int ke = t < nfull ? 32 : kb + 8;
+      const int kn = min(ke, n_own - q * 32);
       float mine = 0.f;
-      for (int k0 = 0; k0 < kn; k0 += UB) {
+      for (int k0 = kb; k0 < kn; k0 += UB) {
         uint4 raw[UB][CPL];
 #pragma unroll
         for (int u = 0; u < UB; ++u)
@@ -795,8 +804,9 @@ __global__ void __launch_bounds__(kLayerThreads, CPT <= 3 ? 2 : 1) k_layer(const
         }
       }
       const int j = q * 32 + lane;
-      const bool act = lane < kn && (mine + ownpb[lane < kn ? j : 0]) > a.tau;
-      if (lane < kn && !lookahead) s_act[j] = act ? 1 : 0;
+      const bool mine_ok = lane >= kb && lane < kn;
+      const bool act = mine_ok && (mine + ownpb[mine_ok ? j : 0]) > a.tau;
+      if (mine_ok && !lookahead) s_act[j] = act ? 1 : 0;
       if (act && sc_out != nullptr) {
         const int i = c + j * G;
         atomicOr(&sc_out[i >> 5], 1u << (i & 31));

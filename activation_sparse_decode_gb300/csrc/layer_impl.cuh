@@ -820,8 +820,14 @@ __global__ void __launch_bounds__(kLayerThreads, CPT <= 3 ? 2 : 1) k_layer(const
     return;
   }
   if (!lookahead) start_ring();
-  if (!settle_ring()) return;
-  SFFN_TRACE_VAL(19, nloc);
+  // The pair split is settled when the ring first needs a list position it
+  // may give away (k_safe and beyond): the rows below k_safe are this
+  // block's whatever the partner sends, so the ring starts on them without
+  // waiting for the partner's message, which has long arrived when the split
+  // is settled.  Look-ahead calls settle here (their ring began earlier).
+  bool settled = a.cluster != 2 || lookahead;
+  if (lookahead && !settle_ring()) return;
+  if (settled) SFFN_TRACE_VAL(19, nloc);
 
 
   // ---- balancing: each token's active rows fall unevenly on the blocks (a
@@ -968,7 +974,17 @@ __global__ void __launch_bounds__(kLayerThreads, CPT <= 3 ? 2 : 1) k_layer(const
   const int ng_max = max(1, min(kGroup, S / 2));
   int grp = 0, st0 = 0;
   uint32_t ph0 = 0;
-  for (int p0 = 0, ng = 0; p0 < nloc; p0 += ng, ++grp) {
+  for (int p0 = 0, ng = 0; !settled || p0 < nloc; p0 += ng, ++grp) {
+    // this group's positions and refills stay below k_safe, or the split is
+    // settled first (at the latest when p0 reaches k_safe)
+    if (!settled && p0 + ng_max + S > k_safe) {
+      if (!settle_ring()) return;
+      settled = true;
+      SFFN_TRACE_VAL(19, nloc);
+      // the refills the ring deferred: positions [k_safe, p0 + S)
+      for (int q = max(k_safe, S); q < min(p0 + S, nloc); ++q) fill(q % S, list[q]);
+      if (p0 >= nloc) break;
+    }
     // the first group is the prefetched hot rows alone, so it need not wait for a cold row
     ng = (grp == 0 && n_hot > 0) ? min(n_hot, ng_max) : min(ng_max, nloc - p0);
     bool ok = true;
@@ -1053,8 +1069,9 @@ __global__ void __launch_bounds__(kLayerThreads, CPT <= 3 ? 2 : 1) k_layer(const
           }
         }
         // this thread is done with its chunks of the stage: refill them
-        // (position p0 + g + S maps to the same stage)
-        if (p0 + g + S < nloc) fill(st, list[p0 + g + S]);
+        // (position p0 + g + S maps to the same stage; before the split is
+        // settled, only positions below k_safe)
+        if (p0 + g + S < (settled ? nloc : k_safe)) fill(st, list[p0 + g + S]);
       }
     }
     st0 += ng;
@@ -1066,7 +1083,10 @@ __global__ void __launch_bounds__(kLayerThreads, CPT <= 3 ? 2 : 1) k_layer(const
   }
   if (failed) {
     cp_async_wait_all();
-    if (a.cluster == 2) cluster_wait();  // phase 2 of the pair exchange
+    if (a.cluster == 2) {  // phase 2 of the pair exchange (arrived here if the split was not settled)
+      if (!settled) cluster_arrive();
+      cluster_wait();
+    }
     return;
   }
 

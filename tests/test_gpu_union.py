@@ -65,6 +65,38 @@ def test_union_ragged(sffn, shape):
             check_elementwise(Yg[s, b], ref, dt)
 
 
+# Wide predictor ranks on the batch path (the OPT-175B shape's rank is 1024):
+# ragged 16-row groups of the hidden layer's clusters, every token-column
+# width, and the ReGLU form.
+WIDE_RANK = [  # (d_model, d_ff, rank, dtype, act, batch, mean activity)
+    (4096, 3000, 1024, "f16", "relu", 8, 0.15),
+    (1536, 2500, 1088, "bf16", "reglu", 20, 0.12),  # 17 row tiles, three jobs per block
+    (2048, 1500, 1024, "bf16", "relu", 32, 0.2),
+]
+
+
+@pytest.mark.parametrize("shape", WIDE_RANK, ids=lambda s: "d%d_f%d_r%d_%s_%s_b%d_p%g" % s)
+def test_union_wide_rank_predictor(sffn, shape):
+    """Masks and outputs against the oracle token by token (masks outside the
+    band), and the same lists from a second run of the same inputs (the
+    hidden layer's cluster reduction runs in a fixed order)."""
+    d, f, r, dt, act, batch, p = shape
+    wl = W.tiny_workload(d_model=d, d_ff=f, rank=r, dtype=dt, act=act, mean_p=p, name=f"widerank{shape}")
+    lw = W.make_layer(wl, device=DEV)
+    ol = oracle_layer(lw)
+    layer = sffn.Layer.from_weights(lw, max_batch=batch)
+    X = W.make_tokens(wl, 2, batch=batch, device=DEV)
+    Y, I, N = run_tokens(sffn, layer, X)
+    Y2, I2, N2 = run_tokens(sffn, layer, X)
+    assert same_lists(I, N, I2, N2)
+    assert np.array_equal(N, N2)
+    Xh = st(X)
+    for s in range(2):
+        for b in range(batch):
+            m = mask_from_list(I[s, b], N[s, b], f)
+            check_token(ol, Xh[s, b], m, Y[s, b], TOL[dt])
+
+
 @pytest.mark.parametrize("batch", [8, 32])
 @pytest.mark.parametrize("tau,expect", [(1e30, "none"), (-1e30, "all")])
 def test_union_degenerate_masks(sffn, tau, expect, batch):

@@ -262,7 +262,8 @@ __global__ void __launch_bounds__(kLayerThreads, CPT <= 3 ? 2 : 1) k_layer(const
       const int j = q / ulines, l = q - j * ulines;
       prefetch_l2(Ub + (size_t)(c + (size_t)j * G) * urow_bytes + l * 128);
     }
-    // the LayerNorm's gamma and beta: every block reads all of them right
+    // the LayerNorm's gamma and beta, and the previous layer's token (which
+    // that kernel wrote at its start): every block reads all of them right
     // after the wait, so each block warms every G-th line of them
     if (a.y_prev != nullptr) {
       const int glines = (d * 4 + 127) / 128;
@@ -270,6 +271,9 @@ __global__ void __launch_bounds__(kLayerThreads, CPT <= 3 ? 2 : 1) k_layer(const
         if (a.ln_gamma != nullptr) prefetch_l2(reinterpret_cast<const char*>(a.ln_gamma) + (size_t)l * 128);
         if (a.ln_beta != nullptr) prefetch_l2(reinterpret_cast<const char*>(a.ln_beta) + (size_t)l * 128);
       }
+      const int xlines = (int)((row_bytes + 127) / 128);
+      for (int l = c + tid * G; l < xlines; l += kLayerThreads * G)
+        prefetch_l2(static_cast<const char*>(a.x) + (size_t)l * 128);
     }
     const int nw = !ponly && c < a.warm_rows ? min(n_own, (a.warm_rows - c + G - 1) / G) : 0;
     const int rlines = (row_bytes + 127) / 128;

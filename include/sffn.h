@@ -140,7 +140,8 @@ typedef struct {
  * same assignment, keeping its own rows up to its share and taking the surplus
  * of others).  Costs about four global round trips; pays off when the uneven
  * split of active rows costs more (wide rows, many rows per SM).  Needs d_ff
- * of at least 8 rows per SM, otherwise ignored. */
+ * of at least 8 rows per block and a grid of at most 256 blocks (layers that
+ * run two blocks per SM use 2 x the SM count), otherwise ignored. */
 #define SFFN_FLAG_BALANCE 2
 /* Batches of 3 to 32 tokens with fp16/bf16 weights (d_model a multiple of 128)
  * normally run on the tensor-core union path: the union of the tokens' active

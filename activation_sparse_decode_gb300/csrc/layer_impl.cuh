@@ -20,10 +20,12 @@
 // neuronas").
 //
 // Overlap.  Under programmatic dependent launch the kernel warms L2 with its
-// V rows, U rows, biases and hot rows while the previous kernel finishes; its
-// U rows and biases are staged in shared memory and its hot rows -- the first
-// owned neurons, almost always active -- in the first ring stages before the
-// predictor has decided.  The active rows stream through a ring of
+// V rows, U rows (when it stages them), biases, hot rows and the LayerNorm's
+// inputs while the previous kernel finishes; its first V rows go to
+// registers, its U rows and biases to shared memory, and its hot rows -- the
+// first owned neurons, almost always active -- to the first ring stages before
+// the predictor has decided (before the wait, or right behind the LayerNorm's
+// loads when the token is formed from the previous layer).  The active rows stream through a ring of
 // one-neuron stages filled by per-thread 16-byte cp.async (each thread copies
 // the chunks it later reads), and the block's partial output is added into y
 // with vector float atomics, so there is no second grid-wide step.
@@ -55,9 +57,9 @@ namespace sffn {
 constexpr int kLayerThreads = 256;
 constexpr int kLayerWarps = kLayerThreads / 32;
 constexpr int kGroup = 2;  // neurons per block-wide reduction in the row ring
-// Warps 0..6 do the copying of phase 0; lane 0 of warp 7 runs the grid
-// barrier, so that no copies of its warp are in flight when it fences.
 constexpr int kSlotStride = 16;  // launch slots: one per 128-byte line (16 words)
+// The thread that publishes the balancing exchange's count (its fence waits
+// for its own copies in flight).
 constexpr int kBarrierThread = kLayerThreads - 32;
 
 // The ring's stage wait once the first test has failed: kept out of line so

@@ -554,7 +554,8 @@ def measure(sffn, W, torch, model, B, steps, warmup, dev, world, args, stats=Tru
     rec.update(st_rec)
     rec.update(la_rec)
     if stack and B > 1:
-        rec["union_per_layer"] = [round(float(np.mean(per_layer_union[l])), 1) for l in range(L)]
+        if all(per_layer_union.get(l) for l in range(L)):  # filled by the statistics pass
+            rec["union_per_layer"] = [round(float(np.mean(per_layer_union[l])), 1) for l in range(L)]
         p = [np.asarray(lw.p) for lw in model.lws]
         rec["union_if_independent"] = round(float(np.mean([np.sum(1 - (1 - q) ** B) for q in p])), 1)
     if dense and not stack:

@@ -160,6 +160,7 @@ SMALL = [  # (d_model, d_ff, rank, dtype, act, batch); batch-1 shapes run both p
     (8, 64, 8, "bf16", "reglu", 1),
     (512, 333, 16, "f32", "reglu", 1),
     (12288, 500, 1024, "f16", "relu", 1),
+    (12288, 20000, 1024, "f16", "relu", 1),  # U rows scored from L2, five words a block: quarter-word tasks only
     (2048, 6000, 384, "bf16", "reglu", 1),
     (1000, 777, 8, "f16", "relu", 3),
     (8, 64, 8, "bf16", "reglu", 2),
